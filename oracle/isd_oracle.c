@@ -34,6 +34,7 @@
  * Nothing is blocked, fused or reordered beyond the definitions: every sum
  * runs in vocabulary order in double precision.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -290,7 +291,9 @@ static void load_rows(const void* base, int dtype, int64_t ld, int64_t first_row
             out[(size_t)r * V + v] = logit_value(base, dtype, ld, first_row + r, v);
 }
 
-static int temperature_ok(float T) { return isfinite(T) && T >= 0.0f; }
+/* T = 0 (greedy) or a finite normal positive float; subnormal temperatures
+ * are rejected (log2(e)/T would overflow a float scale). */
+static int temperature_ok(float T) { return isfinite(T) && (T == 0.0f || T >= FLT_MIN); }
 
 static void set_threads(int nthreads) {
 #ifdef _OPENMP
@@ -314,8 +317,8 @@ ORACLE_API int oracle_max_threads(int nthreads) {
  *   sequence i has L_i = seq_offsets[i+1] - seq_offsets[i] proposals;
  *   p row of position k (1..L_i+1) is seq_offsets[i] + i + k - 1;
  *   q row and token of position k (1..L_i) are seq_offsets[i] + k - 1.
- * A sequence with L_i outside [1, 32], a temperature that is negative or not
- * finite, or a token outside [0, V) is invalid: accept_len = -1, its output
+ * A sequence with L_i outside [1, 32], a temperature that is negative,
+ * subnormal or not finite, or a token outside [0, V) is invalid: accept_len = -1, its output
  * slots -1, its ratios and alpha NaN.
  * `seqs` (optional, n_sel entries) restricts the work to those sequences;
  * the other sequences' outputs are left untouched. */
