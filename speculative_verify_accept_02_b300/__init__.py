@@ -1,0 +1,8 @@
+"""ISD verify-and-propose on one B300: Python binding of libisd (include/isd.h).
+
+The computation runs in libisd.so (hand-written sm_103a CUDA); this package
+marshals torch CUDA tensors into its C ABI.  ``workloads`` makes seeded
+synthetic inputs.
+"""
+from .api import (ProposeOut, VerifyOut, isd_alpha, isd_propose, isd_propose_workspace_bytes,  # noqa: F401
+                  isd_verify, isd_verify_workspace_bytes, workspace)

@@ -1,0 +1,151 @@
+"""Python binding of libisd: the entry points of include/isd.h over torch
+CUDA tensors.  Argument marshalling only — every step of the computation runs
+in the library's kernels; torch supplies device memory and the stream.
+
+Tensors:
+  p [sum L + C, ld_p], q [sum L, ld_q], qnew [sum L, ld]: torch.bfloat16 or
+      torch.float32 on one CUDA device, unit stride along the vocabulary
+      (row padding allowed), base pointer 16-byte aligned;
+  tokens [sum L] int32, seq_offsets [C+1] int32, temperature [C] float32.
+``total`` (= seq_offsets[-1]) must be passed to avoid a device->host read.
+"""
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.bfloat16: _lib.ISD_DTYPE_BF16, torch.float32: _lib.ISD_DTYPE_F32}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"logits must be bfloat16 or float32, not {t.dtype}") from None
+
+
+def _rows(t: torch.Tensor, name: str):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit stride along the vocabulary")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.data_ptr(), t.stride(0)
+
+
+def _int32(t: torch.Tensor, name: str):
+    if t.dtype != torch.int32 or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    return t.data_ptr()
+
+
+def _f32(t: torch.Tensor, name: str):
+    if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _total(seq_offsets: torch.Tensor, total: Optional[int]) -> int:
+    return int(seq_offsets[-1].item()) if total is None else int(total)
+
+
+def isd_verify_workspace_bytes(num_seqs: int, total: int, vocab: int, dtype: torch.dtype) -> int:
+    return int(_lib.load().isd_verify_workspace_bytes(num_seqs, total, vocab, _DTYPES[dtype]))
+
+
+def isd_propose_workspace_bytes(num_seqs: int, total: int, vocab: int, dtype: torch.dtype) -> int:
+    return int(_lib.load().isd_propose_workspace_bytes(num_seqs, total, vocab, _DTYPES[dtype]))
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled, 256-byte aligned workspace (torch's allocator aligns to 512)."""
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+@dataclass
+class VerifyOut:
+    accept_len: torch.Tensor   # [C] int32
+    out_tokens: torch.Tensor   # [sum L + C] int32
+    ratio: torch.Tensor        # [sum L] float32
+    alpha: torch.Tensor        # [C] float32
+
+
+@dataclass
+class ProposeOut:
+    proposals: torch.Tensor    # [sum L] int32
+    valid: torch.Tensor        # [C] uint8
+
+
+def isd_verify(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, seq_offsets: torch.Tensor,
+               temperature: torch.Tensor, seed: int = 0, offset: int = 0, *, vocab: Optional[int] = None,
+               total: Optional[int] = None, out: Optional[VerifyOut] = None,
+               ws: Optional[torch.Tensor] = None, stream=None) -> VerifyOut:
+    device = p.device
+    C = seq_offsets.numel() - 1
+    total = _total(seq_offsets, total)
+    V = p.shape[1] if vocab is None else int(vocab)
+    if p.dtype != q.dtype:
+        raise TypeError("p and q must share a dtype")
+    pp, ldp = _rows(p, "p")
+    qp, ldq = _rows(q, "q")
+    if out is None:
+        out = VerifyOut(torch.empty(C, dtype=torch.int32, device=device),
+                        torch.empty(total + C, dtype=torch.int32, device=device),
+                        torch.empty(total, dtype=torch.float32, device=device),
+                        torch.empty(C, dtype=torch.float32, device=device))
+    need = isd_verify_workspace_bytes(C, total, V, p.dtype)
+    if ws is None:
+        ws = workspace(need, device)
+    status = _lib.load().isd_verify(
+        pp, ldp, qp, ldq, _dtype_code(p), V, _int32(tokens, "tokens"), _int32(seq_offsets, "seq_offsets"),
+        C, total, _f32(temperature, "temperature"), int(seed), int(offset),
+        out.accept_len.data_ptr(), out.out_tokens.data_ptr(), out.ratio.data_ptr(), out.alpha.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
+    _lib.check("isd_verify", status)
+    return out
+
+
+def isd_propose(qnew: torch.Tensor, seq_offsets: torch.Tensor, temperature: torch.Tensor,
+                seed: int = 0, offset: int = 0, accept_len: Optional[torch.Tensor] = None, *,
+                vocab: Optional[int] = None, total: Optional[int] = None,
+                out: Optional[ProposeOut] = None, ws: Optional[torch.Tensor] = None,
+                stream=None) -> ProposeOut:
+    device = qnew.device
+    C = seq_offsets.numel() - 1
+    total = _total(seq_offsets, total)
+    V = qnew.shape[1] if vocab is None else int(vocab)
+    qp, ld = _rows(qnew, "qnew")
+    if out is None:
+        out = ProposeOut(torch.empty(total, dtype=torch.int32, device=device),
+                         torch.empty(C, dtype=torch.uint8, device=device))
+    need = isd_propose_workspace_bytes(C, total, V, qnew.dtype)
+    if ws is None:
+        ws = workspace(need, device)
+    acc = None if accept_len is None else _int32(accept_len, "accept_len")
+    status = _lib.load().isd_propose(
+        qp, ld, _dtype_code(qnew), V, _int32(seq_offsets, "seq_offsets"), C, total,
+        _f32(temperature, "temperature"), int(seed), int(offset), acc, out.proposals.data_ptr(),
+        out.valid.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
+    _lib.check("isd_propose", status)
+    return out
+
+
+def isd_alpha(ratio: torch.Tensor, seq_offsets: torch.Tensor, *, total: Optional[int] = None,
+              stream=None):
+    """Returns (alpha_per_seq [C] float32, alpha_mean [1] float32)."""
+    device = ratio.device
+    C = seq_offsets.numel() - 1
+    total = _total(seq_offsets, total)
+    per = torch.empty(C, dtype=torch.float32, device=device)
+    mean = torch.empty(1, dtype=torch.float32, device=device)
+    status = _lib.load().isd_alpha(_f32(ratio, "ratio"), _int32(seq_offsets, "seq_offsets"), C, total,
+                                   per.data_ptr(), mean.data_ptr(), _stream(device, stream))
+    _lib.check("isd_alpha", status)
+    return per, mean

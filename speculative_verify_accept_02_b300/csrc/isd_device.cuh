@@ -1,0 +1,229 @@
+// Device helpers of libisd: counter-based uniforms, inline PTX for mbarriers,
+// bulk copies and programmatic dependent launch, warp reductions, sequence
+// lookup.  sm_103a only.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <math.h>
+
+namespace isd {
+
+constexpr int kMaxStride = 32;
+constexpr uint64_t kTagAccept = 0, kTagCorrect = 1, kTagBonus = 2, kTagPropose = 3;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Bound on every spin-wait (mbarrier polls with back-off): a wait that never
+// completes ends after roughly a second instead of hanging the device.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+// Error word bits (workspace): set when a bounded wait gave up.
+constexpr int kErrWaitTimeout = 1;
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 — Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3" (SC'11), the 4-word, 64-bit Philox bijection with ten
+// rounds and the Weyl key schedule.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t philox4x64_10_word0(uint64_t c0, uint64_t c1, uint64_t c2,
+                                                        uint64_t c3, uint64_t k0, uint64_t k1) {
+    constexpr uint64_t kMul0 = 0xD2E7470EE14C6C93ULL, kMul1 = 0xCA5A826395121157ULL;
+    constexpr uint64_t kWeyl0 = 0x9E3779B97F4A7C15ULL, kWeyl1 = 0xBB67AE8584CAA73BULL;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += kWeyl0;
+            k1 += kWeyl1;
+        }
+        const uint64_t hi0 = __umul64hi(kMul0, c0), lo0 = kMul0 * c0;
+        const uint64_t hi1 = __umul64hi(kMul1, c2), lo1 = kMul1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0;
+        const uint64_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return c0;
+}
+
+// The uniform of one decision: counter (offset, sequence, position, purpose),
+// key (seed, 0); top 24 bits of word 0 times 2^-24 (exact in float).
+__device__ __forceinline__ float decision_uniform(uint64_t seed, uint64_t offset, uint64_t seq,
+                                                  uint64_t pos, uint64_t tag) {
+    const uint64_t w = philox4x64_10_word0(offset, seq, pos, tag, seed, 0);
+    return (float)(uint32_t)(w >> 40) * (1.0f / 16777216.0f);
+}
+
+// ---------------------------------------------------------------------------
+// Arithmetic
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(e)/T for T > 0; the same expression everywhere so every kernel derives
+// bit-identical scales.
+__device__ __forceinline__ float inv_temp_log2e(float T) { return __fdiv_rn(kLog2e, T); }
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_min_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_max_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Softmax partial (running max m, sum s of exp2((x - m) * c2)) merged into
+// (M, S); a partial with m = -inf holds no mass.
+__device__ __forceinline__ void merge_softmax(float& M, float& S, float m, float s, float c2) {
+    if (m == -INFINITY) return;
+    if (M == -INFINITY) {
+        M = m;
+        S = s;
+        return;
+    }
+    if (m > M) {
+        S = S * exp2f((M - m) * c2) + s;
+        M = m;
+    } else {
+        S += s * exp2f((m - M) * c2);
+    }
+}
+
+// Argmax partial: larger value wins, equal values go to the lower index.
+__device__ __forceinline__ void merge_argmax(float& M, int& I, float m, int i) {
+    if (m > M || (m == M && i < I)) {
+        M = m;
+        I = i;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Batch layout
+// ---------------------------------------------------------------------------
+struct SeqInfo {
+    int start;
+    int len;
+    float T;
+    bool in_range;  // 0 <= start <= end <= total
+    bool ok;        // in range, stride in [1, 32], temperature valid
+};
+
+__device__ __forceinline__ bool temperature_ok(float T) {
+    return isfinite(T) && (T == 0.0f || T >= 1.17549435e-38f);
+}
+
+__device__ __forceinline__ SeqInfo seq_info(const int32_t* offs, const float* temp, int i,
+                                            int total) {
+    SeqInfo s;
+    s.start = __ldg(offs + i);
+    const int end = __ldg(offs + i + 1);
+    s.len = end - s.start;
+    s.T = __ldg(temp + i);
+    s.in_range = s.start >= 0 && end <= total && s.len >= 0;
+    s.ok = s.in_range && s.len >= 1 && s.len <= kMaxStride && temperature_ok(s.T);
+    return s;
+}
+
+// Largest i in [0, C) with offs[i] <= r (offsets non-decreasing).
+__device__ __forceinline__ int seq_of_position(const int32_t* offs, int C, int r) {
+    int lo = 0, hi = C - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(offs + mid) <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory barriers, bulk copies, PDL (inline PTX)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (it > 64) __nanosleep(128);
+    }
+    return false;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on, and
+// allow the dependent grid to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+}  // namespace isd

@@ -1,0 +1,109 @@
+"""The C-ABI library: builds for sm_103a, loads, exports every declared entry
+point, and rejects bad arguments on the host before touching the device.
+No compute call runs here (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+from speculative_verify_accept_02_b300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "isd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"ISD_API\s+[\w\s\*]+?\b(isd_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("isd_verify", "isd_propose", "isd_alpha", "isd_verify_workspace_bytes",
+              "isd_propose_workspace_bytes", "isd_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_build_targets_sm103a_only():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.isd_status_string(code)
+    assert lib.isd_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    # Grows with the batch, 256-byte granular, 0 for bad shapes.
+    a = lib.isd_verify_workspace_bytes(64, 512, 151936, 0)
+    b = lib.isd_verify_workspace_bytes(128, 1024, 151936, 0)
+    assert 0 < a < b and a % 256 == 0
+    assert lib.isd_verify_workspace_bytes(-1, 0, 10, 0) == 0
+    assert lib.isd_verify_workspace_bytes(1, 1, 0, 0) == 0
+    assert lib.isd_verify_workspace_bytes(1, 1, 10, 7) == 0
+    assert lib.isd_propose_workspace_bytes(64, 512, 151936, 1) > 0
+
+
+# A 16-byte aligned address that is never dereferenced: every call below has
+# at least one bad argument (or an empty batch), so it returns on the host
+# before any launch.
+FAKE = 0x10000
+
+
+def _verify(lib, **kw):
+    args = dict(p=FAKE, ldp=1024, q=FAKE, ldq=1024, dtype=0, vocab=1024, tokens=FAKE, offs=FAKE,
+                C=2, total=4, temp=FAKE, seed=0, offset=0, acc=FAKE, out=FAKE, ratio=FAKE, alpha=FAKE,
+                ws=FAKE, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return lib.isd_verify(*args.values())
+
+
+def test_verify_host_checks(lib):
+    assert _verify(lib, C=0) == _lib.ISD_OK                          # empty batch: nothing to do
+    assert _verify(lib, C=-1) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, total=-1) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, vocab=0) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, dtype=5) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, p=None) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, tokens=None) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, ws=None) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, ldq=1000) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify(lib, p=FAKE + 2) == _lib.ISD_ERR_UNSUPPORTED
+    assert _verify(lib, q=FAKE + 8) == _lib.ISD_ERR_UNSUPPORTED
+    assert _verify(lib, wsb=16) == _lib.ISD_ERR_WORKSPACE
+    assert _verify(lib, ws=FAKE + 16) == _lib.ISD_ERR_WORKSPACE
+
+
+def test_propose_and_alpha_host_checks(lib):
+    base = [FAKE, 1024, 0, 1024, FAKE, 2, 4, FAKE, 0, 0, None, FAKE, FAKE, FAKE, 1 << 30, None]
+    bad = list(base); bad[1] = 10
+    assert lib.isd_propose(*bad) == _lib.ISD_ERR_INVALID_ARG
+    bad = list(base); bad[0] = FAKE + 4
+    assert lib.isd_propose(*bad) == _lib.ISD_ERR_UNSUPPORTED
+    bad = list(base); bad[14] = 8
+    assert lib.isd_propose(*bad) == _lib.ISD_ERR_WORKSPACE
+    bad = list(base); bad[5] = 0
+    assert lib.isd_propose(*bad) == _lib.ISD_OK
+    assert lib.isd_alpha(FAKE, FAKE, 0, 0, FAKE, FAKE, None) == _lib.ISD_OK
+    assert lib.isd_alpha(None, FAKE, 3, 4, FAKE, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
+    assert lib.isd_alpha(FAKE, FAKE, -3, 4, FAKE, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIBRARY", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _lib.load()

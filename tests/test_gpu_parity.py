@@ -1,0 +1,206 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, element by element,
+on the same seeded inputs: small batches of every workload at sizes the
+oracle finishes in seconds (several chunks, ragged tails, padded rows, both
+dtypes), the full-size workloads on sampled sequences, and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import Report, compare_propose, compare_verify
+from speculative_verify_accept_02_b300 import build, isd_alpha, isd_propose, isd_verify, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+
+
+def host(batch):
+    return dict(p=workloads.host_logits(batch.p), q=workloads.host_logits(batch.q),
+                qnew=workloads.host_logits(batch.qnew), tokens=batch.tokens.cpu().numpy(),
+                offs=batch.seq_offsets.cpu().numpy(), temp=batch.temperature.cpu().numpy())
+
+
+def gpu_step(batch, seed=0, offset=0, skip_rejected=True):
+    b = batch.to("cuda")
+    v = isd_verify(b.p, b.q, b.tokens, b.seq_offsets, b.temperature, seed, offset, vocab=b.vocab,
+                   total=b.total)
+    pr = isd_propose(b.qnew, b.seq_offsets, b.temperature, seed, offset,
+                     accept_len=v.accept_len if skip_rejected else None, vocab=b.vocab, total=b.total)
+    torch.cuda.synchronize()
+    ver = dict(accept_len=v.accept_len.cpu().numpy(), out_tokens=v.out_tokens.cpu().numpy(),
+               ratio=v.ratio.cpu().numpy(), alpha=v.alpha.cpu().numpy())
+    pro = dict(proposals=pr.proposals.cpu().numpy(), valid=pr.valid.cpu().numpy())
+    return ver, pro
+
+
+def oracle_step(h, vocab, seed=0, offset=0, seqs=None, accept_len=None):
+    ver = oracle.verify(h["p"], h["q"], vocab, h["tokens"], h["offs"], h["temp"], seed, offset, seqs=seqs)
+    acc = ver["accept_len"] if accept_len is None else accept_len
+    pro = oracle.propose(h["qnew"], vocab, h["offs"], h["temp"], seed, offset, accept_len=acc, seqs=seqs)
+    return ver, pro
+
+
+SMALL = [
+    ("tiny", dict()),
+    ("c64", dict(num_seqs=5)),                                   # full V: 19 chunks, short last chunk
+    ("c64", dict(num_seqs=7, vocab=20003)),                      # V not a multiple of the vector width
+    ("c64", dict(num_seqs=4, vocab=5000, ld=5003)),              # padded, 16-byte-misaligned rows
+    ("c64", dict(num_seqs=3, stride=32, vocab=4099)),            # the largest stride
+    ("greedy", dict(num_seqs=9)),
+    ("greedy", dict(num_seqs=6, vocab=3001, ld=3005)),
+    ("highconc", dict(num_seqs=5)),
+    ("highconc", dict(num_seqs=8, vocab=8191)),
+    ("ragged", dict(num_seqs=16)),
+    ("ragged", dict(num_seqs=24, vocab=1537, dtype=torch.float32)),
+    ("ragged", dict(num_seqs=12, vocab=777, ld=781, dtype=torch.float32)),
+    ("tiny", dict(num_seqs=6, vocab=5)),
+    ("tiny", dict(num_seqs=4, vocab=1)),
+    ("tiny", dict(num_seqs=5, vocab=17, dtype=torch.bfloat16)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[f"{n}-{i}" for i, (n, _) in enumerate(SMALL)])
+def test_small_parity(name, kw):
+    batch = workloads.make(name, **kw)
+    h = host(batch)
+    rep = Report()
+    for seed, offset in ((0, 0), (7, 3)):
+        gv, gp = gpu_step(batch, seed, offset)
+        ov, op = oracle_step(h, batch.vocab, seed, offset)
+        compare_verify(ov, gv, h["offs"], report=rep)
+        # Proposals are compared for the sequences whose accept lengths agree.
+        agree = [i for i in range(batch.num_seqs) if ov["accept_len"][i] == gv["accept_len"][i]]
+        op = oracle.propose(h["qnew"], batch.vocab, h["offs"], h["temp"], seed, offset,
+                            accept_len=gv["accept_len"])
+        compare_propose(op, gp, h["offs"], seqs=agree, report=rep)
+    rep.check()
+    assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 20), rep
+
+
+@pytest.mark.parametrize("name", ["c64", "ragged", "tiny"])
+def test_propose_without_skip(name):
+    batch = workloads.make(name, **({} if name == "tiny" else dict(num_seqs=6)))
+    h = host(batch)
+    _, gp = gpu_step(batch, 5, 11, skip_rejected=False)
+    op = oracle.propose(h["qnew"], batch.vocab, h["offs"], h["temp"], 5, 11)
+    rep = compare_propose(op, gp, h["offs"])
+    rep.check()
+    assert np.all(gp["valid"] == 1)
+
+
+def test_alpha_entry_point():
+    batch = workloads.make("ragged", num_seqs=20, vocab=3000)
+    gv, _ = gpu_step(batch)
+    offs = batch.seq_offsets
+    ratio = torch.from_numpy(gv["ratio"]).cuda()
+    per, mean = isd_alpha(ratio, offs.cuda(), total=batch.total)
+    o_per, o_mean = oracle.alpha(gv["ratio"].astype(np.float32), offs.numpy())
+    assert np.allclose(per.cpu().numpy(), o_per, rtol=1e-5)
+    assert abs(mean.item() - o_mean) <= 1e-5 * abs(o_mean)
+    # The verify step's own alpha is the same quantity.
+    assert np.allclose(gv["alpha"], o_per, rtol=1e-4)
+
+
+FULL = ["c64", "greedy", "highconc", "ragged"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """The full workload in the configuration the benchmark times; the oracle
+    checks a sample of sequences one by one."""
+    batch = workloads.make(name, device="cuda")
+    gv, gp = gpu_step(batch)
+    C = batch.num_seqs
+    rng = np.random.default_rng(3)
+    seqs = sorted(set([0, C - 1] + list(rng.choice(C, size=min(C, 10), replace=False))))
+    h = host(batch)
+    ov, op = oracle_step(h, batch.vocab, seqs=seqs, accept_len=gv["accept_len"])
+    rep = compare_verify(ov, gv, h["offs"], seqs=seqs)
+    compare_propose(op, gp, h["offs"], seqs=[i for i in seqs if ov["accept_len"][i] == gv["accept_len"][i]],
+                    report=rep)
+    rep.check()
+    # Properties that hold at any size, on every sequence.
+    acc = gv["accept_len"]
+    L = np.diff(h["offs"])
+    assert np.all((acc >= 0) & (acc <= L))
+    for i in range(C):
+        s = h["offs"][i]
+        slots = gv["out_tokens"][s + i: s + i + L[i] + 1]
+        assert np.array_equal(slots[:acc[i]], h["tokens"][s: s + acc[i]])
+        assert 0 <= slots[acc[i]] < batch.vocab and np.all(slots[acc[i] + 1:] == -1)
+    assert np.all((gv["ratio"] >= 0) & (gv["ratio"] <= 1))
+    if name == "ragged":
+        even = np.arange(0, C, 2)
+        assert np.all(acc[even] == L[even])                 # q == p accepts everything
+    if name == "greedy":
+        assert np.all(np.isin(gv["ratio"], [0.0, 1.0]))
+
+
+def test_repeatable_and_seeded():
+    batch = workloads.make("c64", num_seqs=8, vocab=30000)
+    a1, p1 = gpu_step(batch, 1, 2)
+    a2, p2 = gpu_step(batch, 1, 2)
+    for k in a1:
+        assert np.array_equal(a1[k], a2[k], equal_nan=True), k
+    assert np.array_equal(p1["proposals"], p2["proposals"])
+    b1, _ = gpu_step(batch, 1, 3)
+    assert not np.array_equal(a1["out_tokens"], b1["out_tokens"])
+
+
+def test_invalid_sequences_and_empty_batch():
+    V = 300
+    Ls = [2, 0, 33, 2, 2, 2, 1, 3]
+    temps = np.array([1.0, 1.0, 1.0, -0.5, np.nan, 1.0, 1e-40, 0.0], np.float32)
+    C = len(Ls)
+    offs = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int32)
+    total = int(offs[-1])
+    g = torch.Generator().manual_seed(1)
+    P = torch.randn(total + C, V, generator=g).to(torch.bfloat16)
+    Q = torch.randn(total, V, generator=g).to(torch.bfloat16)
+    tokens = torch.randint(0, V, (total,), generator=g, dtype=torch.int32)
+    tokens[offs[5] + 1] = V
+    d = "cuda"
+    out = isd_verify(P.to(d), Q.to(d), tokens.to(d), torch.from_numpy(offs).to(d),
+                     torch.from_numpy(temps).to(d), 0, 0, total=total)
+    torch.cuda.synchronize()
+    ov = oracle.verify(workloads.host_logits(P), workloads.host_logits(Q), V, tokens.numpy(), offs, temps, 0, 0)
+    gv = dict(accept_len=out.accept_len.cpu().numpy(), out_tokens=out.out_tokens.cpu().numpy(),
+              ratio=out.ratio.cpu().numpy(), alpha=out.alpha.cpu().numpy())
+    assert list(gv["accept_len"][1:7]) == [-1] * 6
+    compare_verify(ov, gv, offs).check()
+    # Empty batch: nothing launched, nothing written.
+    e = torch.zeros(1, dtype=torch.int32, device=d)
+    r = isd_verify(P.to(d), Q.to(d), tokens.to(d), e, torch.zeros(0, device=d), total=0)
+    assert r.accept_len.numel() == 0
+
+
+def test_greedy_ties_lowest_id():
+    """bf16 ties at the maximum: the lowest id is the argmax everywhere."""
+    V, L, C = 4099, 3, 4
+    offs = torch.arange(C + 1, dtype=torch.int32) * L
+    P = torch.zeros(C * (L + 1), V)
+    for r in range(P.shape[0]):
+        P[r, (37 * r + 5) % V] = 3.0
+        P[r, (37 * r + 900) % V] = 3.0
+        P[r, V - 1] = 3.0
+    Q = torch.zeros(C * L, V)
+    lo = torch.tensor([min((37 * r + 5) % V, (37 * r + 900) % V) for r in range(P.shape[0])])
+    tokens = torch.empty(C * L, dtype=torch.int32)
+    for i in range(C):
+        for k in range(L):
+            tokens[i * L + k] = lo[i * L + i + k] if k != i else (lo[i * L + i + k] + 1) % V
+    temps = torch.zeros(C)
+    d = "cuda"
+    Pb, Qb = P.to(torch.bfloat16), Q.to(torch.bfloat16)
+    out = isd_verify(Pb.to(d), Qb.to(d), tokens.to(d), offs.to(d), temps.to(d), total=C * L)
+    torch.cuda.synchronize()
+    acc = out.accept_len.cpu().tolist()
+    assert acc == [0, 1, 2, 3]
+    ov = oracle.verify(workloads.host_logits(Pb), workloads.host_logits(Qb), V, tokens.numpy(),
+                       offs.numpy(), temps.numpy(), 0, 0)
+    assert np.array_equal(ov["out_tokens"], out.out_tokens.cpu().numpy())
