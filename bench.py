@@ -1,0 +1,386 @@
+"""Benchmark of the ISD verify-and-propose step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c64]
+
+One step = isd_verify + isd_propose (every stage of the hot path) over one
+batch of synthetic logits resident in HBM: C=64 sequences, stride L=8,
+V=151936, bf16, T=1 by default.  Prints ONE JSON line (rank 0).
+
+Metric: verified stride-positions per second (sum of L_i per step / step
+time); the line also carries logit GB/s against the measured HBM peak.
+N > 1 (torchrun, one process per GPU): every rank runs its own replica of the
+batch (the step has no cross-GPU exchange), value = all ranks' positions /
+max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this step) on a bounded sample of the same workload, on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified stride-positions/sec and logit GB/s (% of B300 HBM peak), C=64 V=151936"
+UNIT = "positions/s"
+FALLBACK_HBM_GBS = 6400.0
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c64", choices=["c64", "greedy", "highconc", "ragged"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def workload_config(batch, extra):
+    Ls = batch.strides()
+    cfg = {"workload": f"{batch.name}: {batch.meta['description']}", "num_seqs": batch.num_seqs,
+           "sum_stride": int(sum(Ls)), "vocab": batch.vocab,
+           "logits": str(batch.dtype).replace("torch.", ""), "seed": batch.seed, "offset": batch.offset,
+           "data_seed": batch.meta["data_seed"]}
+    cfg.update(extra)
+    return cfg
+
+
+def algorithmic_bytes(batch, accept_len, valid):
+    """Logit bytes the step must read: for every sequence its p_k and q_k rows
+    (k <= L_i; greedy sequences read no q), the final anchor row where every
+    proposal was accepted, and the qnew rows of sequences whose proposals are
+    drawn.  The re-read of a rejected row pair is not counted."""
+    esz = 2 if str(batch.dtype).endswith("bfloat16") else 4
+    row = esz * batch.vocab
+    Ls = batch.strides()
+    temps = batch.temperature.cpu().tolist()
+    verify = propose = 0
+    for i, L in enumerate(Ls):
+        a = int(accept_len[i])
+        per = L if temps[i] == 0.0 else 2 * L
+        verify += row * (per + (1 if a == L else 0))
+        if int(valid[i]):
+            propose += row * L
+    return verify, propose
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_verify_accept_02_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per isd_verify call from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(workload)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_verify")
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index):
+        import torch
+        self.proc = None
+        self.lines = []
+        try:
+            ident = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = ident if ident.startswith("GPU-") else f"GPU-{ident}"
+        except Exception:
+            ident = str(device_index)
+        self.cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                    "-lms", "200", "-i", ident]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.REASONS, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# The fp64 oracle as it stands (CPU baseline, reference arm)
+# ---------------------------------------------------------------------------
+
+def _host_inputs(batch):
+    from speculative_verify_accept_02_b300 import workloads
+    return dict(p=workloads.host_logits(batch.p), q=workloads.host_logits(batch.q),
+                qnew=workloads.host_logits(batch.qnew), tokens=batch.tokens.cpu().numpy(),
+                offs=batch.seq_offsets.cpu().numpy(), temp=batch.temperature.cpu().numpy())
+
+
+def _oracle_step(h, batch, seqs):
+    import oracle
+    v = oracle.verify(h["p"], h["q"], batch.vocab, h["tokens"], h["offs"], h["temp"], batch.seed,
+                      batch.offset, seqs=seqs)
+    oracle.propose(h["qnew"], batch.vocab, h["offs"], h["temp"], batch.seed, batch.offset,
+                   accept_len=v["accept_len"], seqs=seqs)
+
+
+def time_oracle(batch, seconds):
+    """oracle verify+propose on the whole batch, repeated for about `seconds`."""
+    import oracle
+    h = _host_inputs(batch)
+    seqs = list(range(batch.num_seqs))
+    positions = sum(batch.strides())
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        _oracle_step(h, batch, seqs)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return positions * reps / el, oracle.threads(), reps, el, positions
+
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return  # the oracle runs once, on rank 0
+    import oracle
+    from speculative_verify_accept_02_b300 import workloads
+    batch = workloads.make(args.workload, device="cpu")
+    sample = list(range(0, batch.num_seqs, max(1, batch.num_seqs // 8)))[:8]
+    Ls = batch.strides()
+    positions = sum(Ls[i] for i in sample)
+    h = _host_inputs(batch)
+    for _ in range(args.warmup):
+        _oracle_step(h, batch, sample)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_step(h, batch, sample)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = positions / (ms / 1e3)
+    desc = f"{len(sample)} of {batch.num_seqs} sequences ({positions} positions) per step, verify+propose"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(batch, {"sample": desc}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# The CUDA path
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_verify_accept_02_b300 import (_lib, build, isd_propose, isd_propose_workspace_bytes,
+                                                   isd_verify, isd_verify_workspace_bytes, workloads)
+    from speculative_verify_accept_02_b300.api import ProposeOut, VerifyOut, workspace
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    distributed = world > 1
+    dev = torch.device("cuda", local if distributed else 0)
+    torch.cuda.set_device(dev)
+    if distributed:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        build.build()
+    if distributed:
+        dist.barrier()
+    _lib.load()
+
+    batch = workloads.make(args.workload, device=dev)
+    C, total, V = batch.num_seqs, batch.total, batch.vocab
+    i32, f32 = torch.int32, torch.float32
+    vout = VerifyOut(torch.empty(C, dtype=i32, device=dev), torch.empty(total + C, dtype=i32, device=dev),
+                     torch.empty(total, dtype=f32, device=dev), torch.empty(C, dtype=f32, device=dev))
+    pout = ProposeOut(torch.empty(total, dtype=i32, device=dev), torch.empty(C, dtype=torch.uint8, device=dev))
+    vws = workspace(isd_verify_workspace_bytes(C, total, V, batch.dtype), dev)
+    pws = workspace(isd_propose_workspace_bytes(C, total, V, batch.dtype), dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def verify(b):
+        isd_verify(b["p"], b["q"], b["tokens"], b["seq_offsets"], b["temperature"], batch.seed, batch.offset,
+                   vocab=V, total=total, out=vout, ws=vws, stream=stream)
+
+    def propose(b):
+        isd_propose(b["qnew"], b["seq_offsets"], b["temperature"], batch.seed, batch.offset,
+                    accept_len=vout.accept_len, vocab=V, total=total, out=pout, ws=pws, stream=stream)
+
+    names = ("p", "q", "qnew", "tokens", "seq_offsets", "temperature")
+    resident = {n: getattr(batch, n) for n in names}
+    for _ in range(max(3, args.warmup)):
+        verify(resident)
+        propose(resident)
+    torch.cuda.synchronize(dev)
+    vbytes, pbytes = algorithmic_bytes(batch, vout.accept_len.cpu().tolist(), pout.valid.cpu().tolist())
+
+    # Timed region: K steps, each bracketed by its own events; the L2 flush
+    # between steps lies outside them.
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    if distributed:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        t_wall = time.perf_counter()
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            verify(resident)
+            ev[k][1].record(stream)
+            propose(resident)
+            ev[k][2].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if distributed:
+        dist.barrier()
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
+    verify_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if distributed:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = total * world * K / (total_ms / 1e3)
+    logit_gbs = (vbytes + pbytes) * world * K / (total_ms / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    verify_avg_s = verify_ms / K / 1e3
+    achieved = vbytes / verify_avg_s / 1e9
+
+    # End to end through the public API: every step copies its inputs from
+    # pinned host memory, runs, and reads every result back.
+    host_in = {n: resident[n].cpu().pin_memory() for n in names}
+    dev_in = {n: torch.empty_like(resident[n]) for n in names}
+    results = (vout.accept_len, vout.out_tokens, vout.ratio, vout.alpha, pout.proposals, pout.valid)
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in results]
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.e2e_steps)]
+    for k in range(args.e2e_steps):
+        e2e_ev[k][0].record(stream)
+        for n in names:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        verify(dev_in)
+        propose(dev_in)
+        for hbuf, dbuf in zip(host_out, results):
+            hbuf.copy_(dbuf, non_blocking=True)
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.e2e_steps
+    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if distributed:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = total * world / (float(te.item()) / 1e3)
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    cpu = None
+    if not distributed:  # the CPU baseline is taken at N=1 only
+        rate, threads, reps, el, pos = time_oracle(batch, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"full batch ({pos} positions) verify+propose, {reps} repetition(s) in {el:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": workload_config(batch, {
+            "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write between timed steps",
+            "parallelism": f"replicas x{world}", "step": "isd_verify + isd_propose"}),
+        "logit_gbs": logit_gbs, "hbm_frac": logit_gbs / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                     "kernel": "isd_verify (streaming pass + finish)", "algorithmic_bytes": vbytes,
+                     "peak_source": f"{peak_kind} hbm_gbs", "avg_launch_us": verify_avg_s * 1e6},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * K,
+        "clocks": sampler.summary(),
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    if distributed:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
