@@ -168,6 +168,41 @@ ISD_API isd_status isd_propose(const void* qnew_logits, int64_t ld, isd_dtype dt
 ISD_API isd_status isd_alpha(const float* ratio, const int32_t* seq_offsets, int num_seqs,
                      int total_positions, float* alpha_per_seq, float* alpha_mean, void* stream);
 
+/*
+ * isd_verify_noalloc — isd_verify for callers that cannot allocate device
+ * memory.  The method has no counterpart of this call; it exists for hosts
+ * that are given only the logits and output buffers and may not call
+ * cudaMalloc themselves: a plug-in running inside another engine's memory
+ * pool, code that runs while an allocator is locked or being resized, or a
+ * caller that must not add to the device's memory use per request.
+ *
+ * Arguments, layout, outputs and results are those of isd_verify, without
+ * the workspace.  The scratch is a fixed array of ISD_NOALLOC_SCRATCH_BYTES
+ * inside the library, reserved on every device that loads the library until
+ * the process exits.  The call allocates nothing: it clears the part of the
+ * array the batch needs (cudaMemsetAsync on `stream`) and then runs
+ * isd_verify's kernels on it.
+ *
+ * Limits and rules:
+ *   - a batch whose isd_verify_workspace_bytes() exceeds
+ *     ISD_NOALLOC_SCRATCH_BYTES returns ISD_ERR_WORKSPACE and launches
+ *     nothing (isd_verify_workspace_bytes() gives any batch's need; bf16
+ *     rows of V = 151936 at C = 256, L = 16 need about a third of it);
+ *   - the first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture;
+ *   - every call on a device shares the one array: two calls that can
+ *     overlap on the GPU (different streams without an event between them)
+ *     race and give wrong results.  Order them, or use isd_verify with
+ *     workspaces of your own.
+ */
+#define ISD_NOALLOC_SCRATCH_BYTES (4u << 20)
+ISD_API isd_status isd_verify_noalloc(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                                      isd_dtype dtype, int vocab, const int32_t* tokens,
+                                      const int32_t* seq_offsets, int num_seqs, int total_positions,
+                                      const float* temperature, uint64_t seed, uint64_t offset,
+                                      int32_t* accept_len, int32_t* out_tokens, float* ratio,
+                                      float* alpha, void* stream);
+
 /* Static, human-readable name of a status code. */
 ISD_API const char* isd_status_string(isd_status status);
 

@@ -26,7 +26,14 @@ SIGNATURES = {
     "isd_alpha": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                             C.c_void_p]),
     "isd_status_string": (C.c_char_p, [C.c_int]),
+    "isd_verify_noalloc": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_int,
+                                     C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_uint64,
+                                     C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                     C.c_void_p]),
 }
+
+# Size of the library's built-in scratch array (ISD_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class IsdError(RuntimeError):
