@@ -85,7 +85,8 @@ extern "C" {
 typedef enum {
     ISD_OK = 0,
     ISD_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld < vocab, bad dtype */
-    ISD_ERR_UNSUPPORTED = 2,   /* logits base not 16-byte aligned */
+    ISD_ERR_UNSUPPORTED = 2,   /* logits base not 16-byte aligned; isd_verify: vocab above
+                                  523,264 (bf16) or 261,632 (fp32) */
     ISD_ERR_WORKSPACE = 3,     /* workspace too small or not 256-byte aligned */
     ISD_ERR_CUDA = 4           /* a CUDA call failed (launch or device query) */
 } isd_status;

@@ -21,26 +21,61 @@ bool dtype_ok(int dtype) { return dtype == ISD_DTYPE_BF16 || dtype == ISD_DTYPE_
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Workspace of isd_verify:
-//   [err word | chunk partials of the p and q rows | gathered logits |
-//    tail partials | tail counters]
-struct VerifyLayout {
-    size_t err, part, zx, tail_part, tail_count, bytes;
+// Workspace of isd_verify (persistent kernel):
+//   [control block | per-sequence counters | per-sequence tail state |
+//    tail-task queue and flags | per (row slot, segment) partials |
+//    gathered logits | per tail sub-chunk partials]
+struct VerifyPlan {
+    int ck, nck, spseg, nseg, ckt, nt, tpt, ntask;
 };
 
-VerifyLayout verify_layout(int num_seqs, int total, const Chunking& ck) {
+constexpr int kSubChunksPerSegment = 4;  // one main item: 4 x 16 KB
+constexpr int kTailSubChunksPerTask = 4;
+
+VerifyPlan verify_plan(int vocab, int esz) {
+    VerifyPlan pl;
+    const Chunking main = isd::make_chunking(vocab, esz);
+    pl.ck = main.chunk;
+    pl.nck = main.nchunks;
+    pl.spseg = kSubChunksPerSegment;
+    pl.nseg = (pl.nck + pl.spseg - 1) / pl.spseg;
+    // Tail sub-chunks hold one piece of p and one of q: half a stage each.
+    const int vec = 16 / esz;
+    const int tmax = ((isd::kStageBytes / 2 - 16) / esz) / vec * vec;
+    pl.nt = (vocab + tmax - 1) / tmax;
+    const int even = (vocab + pl.nt - 1) / pl.nt;
+    pl.ckt = (even + vec - 1) / vec * vec;
+    pl.tpt = kTailSubChunksPerTask;
+    pl.ntask = (pl.nt + pl.tpt - 1) / pl.tpt;
+    return pl;
+}
+
+struct VerifyLayout {
+    size_t ctl, seq_count, tail_count, tails, tasks, task_ready, part, zx, tpart, bytes;
+};
+
+VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl) {
     VerifyLayout l;
+    const size_t C = static_cast<size_t>(num_seqs);
     size_t off = 0;
-    l.err = off;
-    off = align_up(off + sizeof(int));
+    l.ctl = off;
+    off = align_up(off + sizeof(isd::VerifyCtl));
+    l.seq_count = off;
+    off = align_up(off + sizeof(int) * C);
+    l.tail_count = off;
+    off = align_up(off + sizeof(int) * C);
+    l.tails = off;
+    off = align_up(off + sizeof(isd::SeqTail) * C);
+    l.tasks = off;
+    off = align_up(off + sizeof(int2) * C * pl.ntask);
+    l.task_ready = off;
+    off = align_up(off + sizeof(int) * C * pl.ntask);
     l.part = off;
-    off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * ck.nchunks);
+    off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * pl.nseg);
     l.zx = off;
     off = align_up(off + sizeof(float) * 2 * static_cast<size_t>(total));
-    l.tail_part = off;
-    off = align_up(off + sizeof(float2) * static_cast<size_t>(num_seqs) * ck.nchunks);
-    l.tail_count = off;
-    off = align_up(off + sizeof(int) * static_cast<size_t>(num_seqs));
+    l.tpart = off;
+    off = align_up(off + sizeof(float2) * C * pl.nt * 8);  // 8 consumer-warp slices per tail sub-chunk
     l.bytes = off;
     return l;
 }
@@ -61,17 +96,19 @@ ProposeLayout propose_layout(int total, const Chunking& ck) {
     return l;
 }
 
-// Streaming grid: resident CTAs of the current device, at most one per item.
-isd_status stats_grid(long long n_items, int* grid) {
+// Persistent grid: resident CTAs of the current device, at most one per item.
+isd_status resident_grid(long long n_items, int ctas_per_sm, int* grid) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ISD_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return ISD_ERR_CUDA;
-    long long g = static_cast<long long>(sms) * isd::kStatsCtasPerSm;
+    long long g = static_cast<long long>(sms) * ctas_per_sm;
     if (n_items < g) g = n_items;
     *grid = static_cast<int>(g < 1 ? 1 : g);
     return ISD_OK;
 }
+
+isd_status stats_grid(long long n_items, int* grid) { return resident_grid(n_items, isd::kStatsCtasPerSm, grid); }
 
 }  // namespace
 
@@ -79,7 +116,7 @@ extern "C" {
 
 size_t isd_verify_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
     if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return 0;
-    return verify_layout(num_seqs, total_positions, isd::make_chunking(vocab, elem_bytes_of(dtype))).bytes;
+    return verify_layout(num_seqs, total_positions, verify_plan(vocab, elem_bytes_of(dtype))).bytes;
 }
 
 size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
@@ -101,71 +138,51 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
     if (ld_p < vocab || ld_q < vocab) return ISD_ERR_INVALID_ARG;
     if (!aligned16(p_logits) || !aligned16(q_logits)) return ISD_ERR_UNSUPPORTED;
     const int esz = elem_bytes_of(dtype);
-    const Chunking ck = isd::make_chunking(vocab, esz);
-    const VerifyLayout lay = verify_layout(num_seqs, total_positions, ck);
+    const VerifyPlan pl = verify_plan(vocab, esz);
+    if (pl.nt > isd::kMaxTailChunks) return ISD_ERR_UNSUPPORTED;
+    const VerifyLayout lay = verify_layout(num_seqs, total_positions, pl);
     if (workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
         return ISD_ERR_WORKSPACE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
-    int* err = reinterpret_cast<int*>(ws + lay.err);
-    float2* part = reinterpret_cast<float2*>(ws + lay.part);
-    float* zx = reinterpret_cast<float*>(ws + lay.zx);
-    float2* tail_part = reinterpret_cast<float2*>(ws + lay.tail_part);
-    int* tail_count = reinterpret_cast<int*>(ws + lay.tail_count);
-
-    const long long n_items = 2LL * total_positions * ck.nchunks;
-    if (n_items > 0) {
-        isd::StatsArgs sa{};
-        sa.rows0 = static_cast<const char*>(p_logits);
-        sa.ld0_bytes = ld_p * esz;
-        sa.rows1 = static_cast<const char*>(q_logits);
-        sa.ld1_bytes = ld_q * esz;
-        sa.tokens = tokens;
-        sa.seq_offsets = seq_offsets;
-        sa.temperature = temperature;
-        sa.accept_len = nullptr;
-        sa.num_seqs = num_seqs;
-        sa.total = total_positions;
-        sa.vocab = vocab;
-        sa.chunk = ck.chunk;
-        sa.nchunks = ck.nchunks;
-        sa.two_rows = 1;
-        sa.n_items = n_items;
-        sa.part = part;
-        sa.zx = zx;
-        sa.zero_ptr = tail_count;
-        sa.zero_count = num_seqs;
-        sa.err = err;
-        int grid = 1;
-        const isd_status gs = stats_grid(n_items, &grid);
-        if (gs != ISD_OK) return gs;
-        if (isd::launch_stats(sa, esz, grid, st) != cudaSuccess) return ISD_ERR_CUDA;
-    }
-    isd::VerifyFinishArgs fa{};
-    fa.p = static_cast<const char*>(p_logits);
-    fa.ldp_bytes = ld_p * esz;
-    fa.q = static_cast<const char*>(q_logits);
-    fa.ldq_bytes = ld_q * esz;
-    fa.tokens = tokens;
-    fa.seq_offsets = seq_offsets;
-    fa.temperature = temperature;
-    fa.num_seqs = num_seqs;
-    fa.total = total_positions;
-    fa.vocab = vocab;
-    fa.chunk = ck.chunk;
-    fa.nchunks = ck.nchunks;
-    fa.seed = seed;
-    fa.offset = offset;
-    fa.part = part;
-    fa.zx = zx;
-    fa.tail_part = tail_part;
-    fa.tail_count = tail_count;
-    fa.err = err;
-    fa.accept_len = accept_len;
-    fa.out_tokens = out_tokens;
-    fa.ratio = ratio;
-    fa.alpha = alpha;
-    if (isd::launch_verify_finish(fa, esz, st) != cudaSuccess) return ISD_ERR_CUDA;
+    isd::VerifyArgs va{};
+    va.p = static_cast<const char*>(p_logits);
+    va.ldp_bytes = ld_p * esz;
+    va.q = static_cast<const char*>(q_logits);
+    va.ldq_bytes = ld_q * esz;
+    va.tokens = tokens;
+    va.seq_offsets = seq_offsets;
+    va.temperature = temperature;
+    va.num_seqs = num_seqs;
+    va.total = total_positions;
+    va.vocab = vocab;
+    va.ck = pl.ck;
+    va.nck = pl.nck;
+    va.spseg = pl.spseg;
+    va.nseg = pl.nseg;
+    va.ckt = pl.ckt;
+    va.nt = pl.nt;
+    va.tpt = pl.tpt;
+    va.ntask = pl.ntask;
+    va.n_main = 2LL * total_positions * pl.nseg;
+    va.seed = seed;
+    va.offset = offset;
+    va.ctl = reinterpret_cast<isd::VerifyCtl*>(ws + lay.ctl);
+    va.seq_count = reinterpret_cast<int*>(ws + lay.seq_count);
+    va.tail_count = reinterpret_cast<int*>(ws + lay.tail_count);
+    va.tails = reinterpret_cast<isd::SeqTail*>(ws + lay.tails);
+    va.tasks = reinterpret_cast<int2*>(ws + lay.tasks);
+    va.task_ready = reinterpret_cast<int*>(ws + lay.task_ready);
+    va.part = reinterpret_cast<float2*>(ws + lay.part);
+    va.zx = reinterpret_cast<float*>(ws + lay.zx);
+    va.tpart = reinterpret_cast<float2*>(ws + lay.tpart);
+    va.accept_len = accept_len;
+    va.out_tokens = out_tokens;
+    va.ratio = ratio;
+    va.alpha = alpha;
+    int grid = 1;
+    const isd_status gs = resident_grid(va.n_main, isd::kVerifyCtasPerSm, &grid);
+    if (gs != ISD_OK) return gs;
+    if (isd::launch_verify(va, esz, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ISD_ERR_CUDA;
     return ISD_OK;
 }
 

@@ -16,6 +16,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Bound on every spin-wait (mbarrier polls with back-off): a wait that never
 // completes ends after roughly a second instead of hanging the device.
 constexpr uint32_t kWaitLimit = 1u << 22;
+// Time bounds of the persistent verify kernel's waits, in nanoseconds of the
+// global timer: far above any legitimate wait, far below a hang.
+constexpr uint64_t kWaitNs = 1000000000ull;       // stage barriers, task flags
+constexpr uint64_t kDrainWaitNs = 4000000000ull;  // waiting for other CTAs' work
 
 // Error word bits (workspace): set when a bounded wait gave up.
 constexpr int kErrWaitTimeout = 1;
@@ -157,6 +161,61 @@ __device__ __forceinline__ int seq_of_position(const int32_t* offs, int C, int r
     return lo;
 }
 
+// Packed arithmetic of sm_100+: two bf16 maxima, two fp32 fused multiply-adds
+// or additions per instruction.  A float pair lives in one 64-bit register.
+__device__ __forceinline__ uint32_t hmax2_bf16(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f2(uint64_t r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Global-memory communication between CTAs of one grid
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Loads that bypass L1 (data written by other CTAs of the running grid).
+__device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+__device__ __forceinline__ void st_volatile(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }
+// Device-scope add that publishes this thread's earlier writes and acquires
+// the writes published by earlier adds to the same counter.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory barriers, bulk copies, PDL (inline PTX)
 // ---------------------------------------------------------------------------
@@ -204,6 +263,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// Wait bounded by the global timer; false on timeout.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    for (int it = 0; it < 64; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+        __nanosleep(64);
+    }
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
@@ -217,6 +288,20 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
 }
 
 // Programmatic dependent launch: wait for the grids this one depends on, and

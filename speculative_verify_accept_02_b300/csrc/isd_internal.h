@@ -57,32 +57,6 @@ struct StatsArgs {
     int* err;                   // error word (bounded waits)
 };
 
-struct VerifyFinishArgs {
-    const char* p;
-    int64_t ldp_bytes;
-    const char* q;
-    int64_t ldq_bytes;
-    const int32_t* tokens;
-    const int32_t* seq_offsets;
-    const float* temperature;
-    int num_seqs;
-    int total;
-    int vocab;
-    int chunk;
-    int nchunks;
-    uint64_t seed;
-    uint64_t offset;
-    const float2* part;
-    const float* zx;
-    float2* tail_part;          // [num_seqs * nchunks]
-    int* tail_count;            // [num_seqs]
-    const int* err;
-    int32_t* accept_len;
-    int32_t* out_tokens;
-    float* ratio;
-    float* alpha;
-};
-
 struct ProposeSampleArgs {
     const char* rows;
     int64_t ld_bytes;
@@ -102,9 +76,88 @@ struct ProposeSampleArgs {
     uint8_t* valid;
 };
 
+// ---------------------------------------------------------------------------
+// Persistent verify kernel
+// ---------------------------------------------------------------------------
+
+// Control block (workspace); every call leaves it zero for the next one.
+// Each counter has a 128-byte line of its own: hundreds of CTAs poll and
+// update them concurrently.
+struct VerifyCtl {
+    alignas(128) int err;                  // error word (bounded waits)
+    alignas(128) unsigned long long grab;  // main items handed out (dynamic scheduling)
+    alignas(128) int tail_reserve;         // tail-task slots reserved by decisions
+    alignas(128) int tail_claim;           // tail-task tickets handed to producers
+    alignas(128) int finalized;            // sequences whose outputs are complete
+    alignas(128) int exited;               // CTAs that have finished
+};
+
+// Tail kinds: which row(s) the work after a decision reads.
+enum TailMode : int {
+    kTailRes = 2,   // T > 0, rejection: residual max(0, p_j - q_j) over row pair j
+    kTailSoft = 3,  // T > 0, all accepted: softmax of the final anchor p_{L+1}
+    kTailArg = 4    // T = 0, all accepted: argmax of p_{L+1}
+};
+
+// What a sequence's tail needs, written by its decision (48 bytes).
+struct alignas(16) SeqTail {
+    int mode;
+    int a;            // accept length
+    int prow, qrow;   // tail rows in p and in q
+    float c2;         // log2(e) / T
+    float mc0, inv0;  // p_j: (max logit) * c2 and 1 / sum of exp2(x c2 - mc0)
+    float mc1, inv1;  // q_j: the same
+    float pad[3];
+};
+
+struct VerifyArgs {
+    const char* p;
+    int64_t ldp_bytes;
+    const char* q;
+    int64_t ldq_bytes;
+    const int32_t* tokens;
+    const int32_t* seq_offsets;
+    const float* temperature;
+    int num_seqs;
+    int total;
+    int vocab;
+    int ck;           // elements of a main sub-chunk (one stage)
+    int nck;          // main sub-chunks per row
+    int spseg;        // sub-chunks per segment (one main item)
+    int nseg;         // segments per row
+    int ckt;          // elements of a tail sub-chunk (half a stage per row)
+    int nt;           // tail sub-chunks per row
+    int tpt;          // tail sub-chunks per tail task
+    int ntask;        // tail tasks per sequence
+    long long n_main; // 2 * total * nseg main items
+    uint64_t seed;
+    uint64_t offset;
+    VerifyCtl* ctl;
+    int* seq_count;   // [C] main items finished
+    int* tail_count;  // [C] tail tasks finished
+    SeqTail* tails;   // [C]
+    int2* tasks;      // [C * ntask] (sequence, task) in reservation order
+    int* task_ready;  // [C * ntask] 1 once the slot's task is published
+    float2* part;     // [2 * total * nseg] per (row slot, segment) partials
+    float* zx;        // [2 * total] logit of the proposed token, p and q rows
+    float2* tpart;    // [C * nt * 8] per (tail sub-chunk, consumer warp) slice partials
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    float* ratio;
+    float* alpha;
+};
+
+// Largest number of tail sub-chunks per row the verify kernel supports
+// (vocabularies up to 523,264 bf16 or 261,632 fp32 ids).
+constexpr int kMaxTailChunks = 128;
+
+// Resident CTAs of the verify kernel per SM.
+constexpr int kVerifyCtasPerSm = 2;
+
+cudaError_t launch_verify(const VerifyArgs& a, int elem_bytes, int grid, cudaStream_t stream);
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_stats(const StatsArgs& a, int elem_bytes, int grid, cudaStream_t stream);
-cudaError_t launch_verify_finish(const VerifyFinishArgs& a, int elem_bytes, cudaStream_t stream);
 cudaError_t launch_propose_sample(const ProposeSampleArgs& a, int elem_bytes, cudaStream_t stream);
 cudaError_t launch_alpha(const float* ratio, const int32_t* seq_offsets, int num_seqs, int total,
                          float* alpha_per_seq, float* alpha_mean, cudaStream_t stream);

@@ -1,0 +1,1177 @@
+// The verify step of Introspective Strided Decoding as one persistent kernel
+// ("Introspective Diffusion Language Models | Summary", §2 acceptance rate,
+// §3.2 strict acceptance, residual correction and bonus token, §3.3 online
+// softmax over the vocabulary and a common acceptance path free of
+// correction work).
+//
+// Work is handed out dynamically, in sequence order, by a global counter:
+//   main item   one segment (four 16 KB sub-chunks) of one p_k or q_k row.
+//   decision    once a sequence's last item is done: ratio_k =
+//               min(1, p_k(x_k) / q_k(x_k)), alpha, the accept prefix
+//               (Philox uniforms, one warp ballot) and the emitted prefix.  A
+//               greedy rejection is complete here (argmax of p_j).
+//   tail task   otherwise the decision publishes tail tasks on a device queue:
+//               the residual max(0, p_j - q_j) of the one rejected row pair,
+//               or the final anchor row p_{L+1}.  Producers take queued tail
+//               tasks before new main items, so the rejected rows are re-read
+//               while they are still in L2.
+//   selection   once a sequence's last tail task is done: the token by
+//               inverse CDF, the sub-chunk from the tail partials, then an
+//               in-order scan of that one sub-chunk.
+//
+// Warp roles of a CTA:
+//   scheduler   (one thread) takes work: the next main item from the global
+//               counter, or a published tail task; it absorbs every global
+//               memory round trip and keeps a 2-entry work ring filled;
+//   issuer      (one thread) streams the scheduled sub-chunks into a 5-stage
+//               shared-memory ring with 1-D bulk copies and never waits on
+//               global memory;
+//   consumers   (8 warps) fold each stage into per-thread online softmax
+//               partials (packed bf16 maxima, packed fp32 FMAs, one ex2 per
+//               logit) or an exact argmax; at the end of an item every warp
+//               hands its warp partial to the bookkeeper through a record
+//               ring and moves on: consumers never wait on each other or on
+//               global memory;
+//   bookkeeper  (one warp) merges the records, stores partials, counts
+//               finished items per sequence with device-scope atomics, and
+//               runs decisions and selections itself.
+// The grid exits once every sequence is final; its last CTA re-zeroes the
+// control block for the next call.  Every wait is bounded by the global timer.
+#include <climits>
+
+#include "isd_device.cuh"
+#include "isd_internal.h"
+
+namespace isd {
+namespace {
+
+constexpr int kCW = 8;                    // consumer warps
+constexpr int kCT = kCW * 32;             // consumer threads
+constexpr int kIssuerWarp = kCW;
+constexpr int kBookWarp = kCW + 1;
+constexpr int kSchedWarp = kCW + 2;
+constexpr int kFinWarp = kCW + 3;
+constexpr int kThreadsV = kCT + 128;      // + issuer, bookkeeper, scheduler and finisher warps
+constexpr int kStagesV = 4;
+constexpr int kJobs = 16;                 // job ring between bookkeeper and finisher
+constexpr int kWork = 2;                  // work ring between scheduler and issuer
+constexpr int kRecs = 8;                  // record ring between consumers and bookkeeper
+constexpr int kVecPT = kStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
+constexpr int kHalf = kStageBytes / 2;          // tail stages: [p piece | q piece]
+constexpr int kSmemSeqs = 512;                  // batches up to this size keep offsets in shared memory
+constexpr int kSliceMax = 512;                  // ids in one tail slice (tail sub-chunk / 8 warps)
+static_assert(kHalf / 2 <= kSliceMax * kCW, "a tail sub-chunk of bf16 ids splits into slices of at most kSliceMax");
+static_assert(kVecPT * 16 * kCT == kStageBytes, "stage split");
+
+enum : int { kEnd = 0, kMain = 1 };  // descriptor / record kinds besides the TailMode values
+enum : int { kFirst = 1, kLast = 2 };
+
+struct Desc {
+    int kind;
+    int flags;
+    int seq;
+    int slot;      // main: row slot (2 r + {0: p, 1: q}); tail: tail sub-chunk
+    int seg;
+    int expect;    // main: items of the sequence
+    int e0;        // first element of the sub-chunk in its row
+    int n;         // elements of the sub-chunk
+    int nvec;      // main: 16-byte vectors in the stage
+    int nsm0, skip0, nsm1, skip1;
+    const char* tail0;  // global address of the first element not in shared memory
+    const char* tail1;
+    float c2, mc0, inv0, mc1, inv1;
+};
+
+// flags of a main record: which partial the warps hand in.
+enum : int { kRecSoft = 0, kRecArg = 1 };
+
+struct Rec {
+    int kind, flags, seq, slot, seg, expect;
+    float2 wp[kCW];  // one partial per consumer warp
+};
+
+// One unit of scheduled streaming: sub-chunks [c0, c1) of one row (main item)
+// or of a tail row (pair).
+struct Work {
+    int kind;
+    int seq, slot, seg, expect, c0, c1;
+    float c2, mc0, inv0, mc1, inv1;
+    const char* row0;
+    const char* row1;
+};
+
+// A finisher job: decide or select one sequence, or stop.
+enum : int { kJobEnd = 0, kJobDecide = 1, kJobSelect = 2 };
+struct Job {
+    int kind, seq;
+};
+
+struct SmemV {
+    alignas(128) unsigned char stage[kStagesV][kStageBytes];
+    uint64_t full[kStagesV];
+    uint64_t empty[kStagesV];
+    uint64_t rec_full[kRecs];
+    uint64_t rec_empty[kRecs];
+    uint64_t work_full[kWork];
+    uint64_t work_empty[kWork];
+    uint64_t job_full[kJobs];
+    uint64_t job_empty[kJobs];
+    Job job[kJobs];
+    float2 tsel[kMaxTailChunks * kCW];  // finisher's copy of one sequence's slice partials
+    Desc desc[kStagesV];
+    Work work[kWork];
+    Rec rec[kRecs];
+    int n_valid;
+    int batch_bad;
+    int offs[kSmemSeqs + 1];
+    float temp[kSmemSeqs];
+};
+
+template <typename Elem>
+__device__ __forceinline__ float load_elem(const void* p) {
+    if constexpr (sizeof(Elem) == 2)
+        return __uint_as_float(static_cast<uint32_t>(*static_cast<const uint16_t*>(p)) << 16);
+    else
+        return *static_cast<const float*>(p);
+}
+
+// Element e of a staged piece: shared memory first, then the unaligned tail.
+template <typename Elem>
+__device__ __forceinline__ float piece_elem(const unsigned char* st, int nsm, int skip, const char* tail, int e) {
+    return e < nsm ? load_elem<Elem>(st + static_cast<size_t>(e + skip) * sizeof(Elem))
+                   : load_elem<Elem>(tail + static_cast<size_t>(e - nsm) * sizeof(Elem));
+}
+
+// Tempered softmax weight relative to a reference mc = max * c2.
+__device__ __forceinline__ float soft_w(float x, float c2, float mc) { return ex2_approx(__fmaf_rn(x, c2, -mc)); }
+
+// Residual weight max(0, p - q) of one id, and p itself.
+__device__ __forceinline__ float resid_w(float xp, float xq, float c2, float mc0, float inv0, float mc1,
+                                         float inv1, float& pv) {
+    pv = __fmul_rn(soft_w(xp, c2, mc0), inv0);
+    const float qv = __fmul_rn(soft_w(xq, c2, mc1), inv1);
+    return fmaxf(0.0f, __fsub_rn(pv, qv));
+}
+
+// Softmax partials in the mc domain: (mc, s) holds sum exp2(x c2 - mc).
+__device__ __forceinline__ void merge_mc(float& M, float& S, float m, float s) {
+    if (m == -INFINITY) return;
+    if (m > M) {
+        S = (M == -INFINITY) ? s : S * ex2_approx(M - m) + s;
+        M = m;
+    } else {
+        S += s * ex2_approx(m - M);
+    }
+}
+
+__device__ __forceinline__ void warp_merge_mc(float& M, float& S) {
+    const float W = warp_max(M);
+    S = (M == -INFINITY) ? 0.0f : S * ex2_approx(M - W);
+    S = warp_sum(S);
+    M = W;
+}
+
+__device__ __forceinline__ void warp_merge_arg(float& M, int& I) {
+    const float W = warp_max(M);
+    I = warp_min_int(M == W ? I : INT_MAX);
+    M = W;
+}
+
+// Sequence lookups on a table in shared memory (small batches) or global memory.
+__device__ __forceinline__ int seq_of_position_t(const int* offs, int C, int r) {
+    int lo = 0, hi = C - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offs[mid] <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ SeqInfo seq_info_t(const int* offs, const float* temp, int i, int total) {
+    SeqInfo s;
+    s.start = offs[i];
+    const int end = offs[i + 1];
+    s.len = end - s.start;
+    s.T = temp[i];
+    s.in_range = s.start >= 0 && end <= total && s.len >= 0;
+    s.ok = s.in_range && s.len >= 1 && s.len <= kMaxStride && temperature_ok(s.T);
+    return s;
+}
+
+__device__ __forceinline__ SeqInfo seq_lookup(const VerifyArgs& a, const SmemV& sm, int i) {
+    return a.num_seqs <= kSmemSeqs ? seq_info_t(sm.offs, sm.temp, i, a.total)
+                                   : seq_info_t(a.seq_offsets, a.temperature, i, a.total);
+}
+
+// ---- outputs of an invalid sequence (one warp) -------------------------------
+__device__ void write_invalid(const VerifyArgs& a, int i, const SeqInfo& s, int lane, int code) {
+    if (s.in_range) {
+        for (int m = lane; m <= s.len; m += 32) a.out_tokens[s.start + i + m] = -1;
+        for (int k = lane; k < s.len; k += 32) a.ratio[s.start + k] = NAN;
+    }
+    if (lane == 0) {
+        a.accept_len[i] = code;
+        a.alpha[i] = NAN;
+    }
+}
+
+__device__ __forceinline__ void finalize(const VerifyArgs& a) { atomicAdd(&a.ctl->finalized, 1); }
+
+// ---- pieces of rows for 1-D bulk copies ---------------------------------------
+struct Piece {
+    uintptr_t lo;
+    int bytes, nsm, skip;
+    const char* tail;
+};
+
+// The 16-byte aligned part of elements [e0, e0 + n) of a row goes to shared
+// memory by bulk copy; the unaligned end (fewer than 16 bytes) is read from
+// global memory.
+template <int E>
+__device__ __forceinline__ Piece make_piece(const char* row, int e0, int n) {
+    Piece pc;
+    const uintptr_t sb = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(e0) * E;
+    const uintptr_t eb = sb + static_cast<uintptr_t>(n) * E;
+    const uintptr_t lo = sb & ~static_cast<uintptr_t>(15), hi = eb & ~static_cast<uintptr_t>(15);
+    pc.lo = lo;
+    if (hi > lo) {
+        pc.bytes = static_cast<int>(hi - lo);
+        pc.skip = static_cast<int>((sb - lo) / E);
+        pc.nsm = static_cast<int>((hi - sb) / E);
+    } else {
+        pc.bytes = 0;
+        pc.skip = 0;
+        pc.nsm = 0;
+    }
+    pc.tail = reinterpret_cast<const char*>(sb) + static_cast<size_t>(pc.nsm) * E;
+    return pc;
+}
+
+// =============================================================================
+// Bookkeeper warp
+// =============================================================================
+
+// Decision of sequence i (L <= 32: lane k handles position k + 1).
+template <typename Elem>
+__device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lane) {
+    constexpr int E = sizeof(Elem);
+    // The bookkeeper's acquiring count saw every partial of this sequence
+    // published; the job ring orders that before this warp's loads.
+    const SeqInfo s = seq_lookup(a, sm, i);
+    const int L = s.len;
+    const float T = s.T;
+    const float c2 = T > 0.0f ? inv_temp_log2e(T) : 0.0f;
+    const int r = s.start + lane;
+    const bool mine = lane < L;
+    const int x = mine ? __ldg(a.tokens + r) : 0;
+    if (__any_sync(0xffffffffu, mine && (x < 0 || x >= a.vocab))) {
+        write_invalid(a, i, s, lane, -1);
+        if (lane == 0) {
+            a.seq_count[i] = 0;
+            finalize(a);
+        }
+        return;
+    }
+    float ratio = 0.0f, Mp = -INFINITY, Sp = 0.0f, Mq = -INFINITY, Sq = 0.0f;
+    int amax = INT_MAX;
+    if (mine) {
+        const float2* pp = a.part + static_cast<size_t>(2 * r) * a.nseg;
+        const float2* pq = pp + a.nseg;
+        // Every load of this lane is issued before any is used.
+        float zp = 0.0f, zq = 0.0f;
+        if (T > 0.0f) {  // the proposed token's logits, from rows read moments ago
+            zp = load_elem<Elem>(a.p + static_cast<int64_t>(r + i) * a.ldp_bytes + static_cast<size_t>(x) * E);
+            zq = load_elem<Elem>(a.q + static_cast<int64_t>(r) * a.ldq_bytes + static_cast<size_t>(x) * E);
+        }
+        float M = -INFINITY;
+        for (int j0 = 0; j0 < a.nseg; j0 += 8) {
+            float2 u[8], v[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = j0 + jj;
+                u[jj] = j < a.nseg ? __ldcg(pp + j) : make_float2(-INFINITY, 0.0f);
+                v[jj] = (T > 0.0f && j < a.nseg) ? __ldcg(pq + j) : make_float2(-INFINITY, 0.0f);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (T > 0.0f) {
+                    merge_mc(Mp, Sp, u[jj].x, u[jj].y);
+                    merge_mc(Mq, Sq, v[jj].x, v[jj].y);
+                } else if (j0 + jj < a.nseg) {
+                    merge_argmax(M, amax, u[jj].x, __float_as_int(u[jj].y));
+                }
+            }
+        }
+        if (T > 0.0f) {
+            const float lp = __fmaf_rn(zp, c2, -Mp) - log2f(Sp);
+            const float lq = __fmaf_rn(zq, c2, -Mq) - log2f(Sq);
+            ratio = lq == -INFINITY ? 1.0f : fminf(1.0f, exp2f(lp - lq));
+        } else {
+            ratio = x == amax ? 1.0f : 0.0f;
+        }
+    }
+    bool acc = false;
+    if (mine) acc = T > 0.0f ? decision_uniform(a.seed, a.offset, i, lane + 1, kTagAccept) < ratio : ratio == 1.0f;
+    const unsigned bits = __ballot_sync(0xffffffffu, acc);
+    const int na = min(bits == 0xffffffffu ? 32 : __ffs(~bits) - 1, L);
+    const float total = warp_sum(ratio);
+    if (mine) a.ratio[r] = ratio;
+    for (int m = lane; m <= L; m += 32) {
+        if (m < na) a.out_tokens[s.start + i + m] = __ldg(a.tokens + s.start + m);
+        else if (m > na) a.out_tokens[s.start + i + m] = -1;
+    }
+    const int amax_j = __shfl_sync(0xffffffffu, amax, na & 31);
+    const float mc0 = __shfl_sync(0xffffffffu, Mp, na & 31), sp0 = __shfl_sync(0xffffffffu, Sp, na & 31);
+    const float mc1 = __shfl_sync(0xffffffffu, Mq, na & 31), sq0 = __shfl_sync(0xffffffffu, Sq, na & 31);
+    if (lane == 0) {
+        a.accept_len[i] = na;
+        a.alpha[i] = total / static_cast<float>(L);
+    }
+    if (T == 0.0f && na < L) {  // greedy correction: argmax of p_j, already known
+        if (lane == 0) {
+            a.out_tokens[s.start + i + na] = amax_j;
+            a.seq_count[i] = 0;
+            finalize(a);
+        }
+        return;
+    }
+    int base = 0;
+    if (lane == 0) {
+        SeqTail t = {};
+        t.mode = na < L ? kTailRes : (T > 0.0f ? kTailSoft : kTailArg);
+        t.a = na;
+        t.prow = s.start + i + na;  // p_j, or p_{L+1} when na == L
+        t.qrow = s.start + na;
+        t.c2 = c2;
+        if (na < L) {
+            t.mc0 = mc0;
+            t.inv0 = 1.0f / sp0;
+            t.mc1 = mc1;
+            t.inv1 = 1.0f / sq0;
+        }
+        a.tails[i] = t;
+        a.seq_count[i] = 0;
+        base = atomicAdd(&a.ctl->tail_reserve, a.ntask);
+    }
+    base = __shfl_sync(0xffffffffu, base, 0);
+    for (int y = lane; y < a.ntask; y += 32) a.tasks[base + y] = make_int2(i, y);
+    // Tail state and tasks are visible before any task is flagged ready.
+    __threadfence();
+    __syncwarp();
+    for (int y = lane; y < a.ntask; y += 32) st_volatile(a.task_ready + base + y, 1);
+}
+
+// Selection of sequence i's token from its tail partials (one warp).  The
+// partials are per (tail sub-chunk, consumer warp) slice of about 500 ids;
+// the draw picks a slice from them, then scans that slice in vocabulary
+// order from registers.
+template <typename Elem>
+__device__ void select_warp(const VerifyArgs& a, SmemV& sm, int i, int lane) {
+    constexpr int E = sizeof(Elem);
+    // One round trip: the tail state (written by the decision before its tasks
+    // were published) and every slice partial, into shared memory.
+    const int4* tw = reinterpret_cast<const int4*>(a.tails + i);
+    int4 tv = make_int4(0, 0, 0, 0);
+    if (lane < 3) tv = __ldcg(tw + lane);
+    const int U = a.nt * kCW;
+    const float2* tp = a.tpart + static_cast<size_t>(i) * U;
+    for (int u = lane; u < U; u += 32) sm.tsel[u] = __ldcg(tp + u);
+    SeqTail t;
+    t.mode = __shfl_sync(0xffffffffu, tv.x, 0);
+    t.a = __shfl_sync(0xffffffffu, tv.y, 0);
+    t.prow = __shfl_sync(0xffffffffu, tv.z, 0);
+    t.qrow = __shfl_sync(0xffffffffu, tv.w, 0);
+    t.c2 = __int_as_float(__shfl_sync(0xffffffffu, tv.x, 1));
+    t.mc0 = __int_as_float(__shfl_sync(0xffffffffu, tv.y, 1));
+    t.inv0 = __int_as_float(__shfl_sync(0xffffffffu, tv.z, 1));
+    t.mc1 = __int_as_float(__shfl_sync(0xffffffffu, tv.w, 1));
+    t.inv1 = __int_as_float(__shfl_sync(0xffffffffu, tv.x, 2));
+    __syncwarp();
+    const SeqInfo s = seq_lookup(a, sm, i);
+    const int out_slot = s.start + i + t.a;
+    if (t.mode == kTailArg) {
+        float M = -INFINITY;
+        int I = INT_MAX;
+        for (int u = lane; u < U; u += 32) merge_argmax(M, I, sm.tsel[u].x, __float_as_int(sm.tsel[u].y));
+        warp_merge_arg(M, I);
+        if (lane == 0) {
+            a.out_tokens[out_slot] = I;
+            a.tail_count[i] = 0;
+            finalize(a);
+        }
+        return;
+    }
+    // Slice weights in one scale, the target u * total, and its slice.
+    float MC = -INFINITY;
+    if (t.mode == kTailSoft)
+        for (int u = lane; u < U; u += 32) MC = fmaxf(MC, sm.tsel[u].x);
+    MC = warp_max(MC);
+    bool fallback = false;
+    if (t.mode == kTailRes) {
+        float W = 0.0f;
+        for (int u = lane; u < U; u += 32) W += sm.tsel[u].x;
+        fallback = !(warp_sum(W) > 0.0f);  // residual rounded to zero: draw from p_j
+    }
+    auto slice_w = [&](int u) -> float {
+        if (u >= U) return 0.0f;
+        const float2 v = sm.tsel[u];
+        if (t.mode == kTailSoft) return v.x == -INFINITY ? 0.0f : v.y * ex2_approx(v.x - MC);
+        return fallback ? v.y : v.x;
+    };
+    const float rnd = t.mode == kTailSoft ? decision_uniform(a.seed, a.offset, i, s.len + 1, kTagBonus)
+                                          : decision_uniform(a.seed, a.offset, i, t.a + 1, kTagCorrect);
+    float total = 0.0f;
+    for (int u0 = 0; u0 < U; u0 += 32) total += warp_sum(slice_w(u0 + lane));
+    const float target = rnd * total;
+    int chosen = -1, last_pos = -1;
+    float tloc = INFINITY, carry = 0.0f;
+    for (int u0 = 0; u0 < U && chosen < 0; u0 += 32) {
+        const float w = slice_w(u0 + lane);
+        float incl = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        incl += carry;
+        const unsigned hit = __ballot_sync(0xffffffffu, u0 + lane < U && incl > target);
+        const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
+        if (pos) last_pos = u0 + 31 - __clz(pos);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            chosen = u0 + l;
+            tloc = target - (__shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, w, l));
+        }
+        carry = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (chosen < 0) {  // rounding left the target past the last weight
+        chosen = last_pos >= 0 ? last_pos : 0;
+        tloc = INFINITY;
+    }
+    // The chosen slice: ids [lo, lo + len) of the tail row(s).
+    const int c = chosen / kCW, w = chosen % kCW;
+    const int nc = min(a.ckt, a.vocab - c * a.ckt);
+    const int spw = (nc + kCW - 1) / kCW;
+    const int lo = c * a.ckt + min(nc, w * spw);
+    const int len = min(nc, w * spw + spw) - min(nc, w * spw);
+    const char* prow = a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
+    const char* qrow = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes;
+    const int q = (len + 31) / 32;  // at most kSliceMax / 32 ids per lane
+    const int b = lane * q;
+    const int cnt = max(0, min(q, len - b));
+    float wv[kSliceMax / 32];
+#pragma unroll
+    for (int k = 0; k < kSliceMax / 32; ++k) {
+        wv[k] = 0.0f;
+        if (k < cnt) {
+            const size_t e = static_cast<size_t>(lo + b + k);
+            const float xp = load_elem<Elem>(prow + e * E);
+            if (t.mode == kTailSoft) {
+                wv[k] = soft_w(xp, t.c2, MC);
+            } else {
+                float pv;
+                const float rw = resid_w(xp, load_elem<Elem>(qrow + e * E), t.c2, t.mc0, t.inv0, t.mc1, t.inv1, pv);
+                wv[k] = fallback ? pv : rw;
+            }
+        }
+    }
+    float own = 0.0f;
+    int lp = -1;
+#pragma unroll
+    for (int k = 0; k < kSliceMax / 32; ++k) {
+        own += wv[k];
+        if (wv[k] > 0.0f) lp = b + k;
+    }
+    float incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && incl > tloc);
+    int found = -1;
+    if (hit) {
+        const int owner = __ffs(hit) - 1;
+        if (lane == owner) {
+            float cum = incl - own;
+#pragma unroll
+            for (int k = 0; k < kSliceMax / 32; ++k) {
+                cum += wv[k];
+                if (found < 0 && k < cnt && cum > tloc) found = b + k;
+            }
+            if (found < 0) found = lp;  // rounding inside this lane's ids
+        }
+        found = __shfl_sync(0xffffffffu, found, owner);
+    }
+    const int last = warp_max_int(lp);
+    if (lane == 0) {
+        const int v = found >= 0 ? found : (last >= 0 ? last : 0);
+        a.out_tokens[out_slot] = lo + v;
+        a.tail_count[i] = 0;
+        finalize(a);
+    }
+}
+
+// Hand a decision or selection to the finisher warp (lane 0 of the bookkeeper).
+__device__ __forceinline__ void push_job(const VerifyArgs& a, SmemV& sm, long long& nj, int kind, int seq) {
+    const int js = static_cast<int>(nj % kJobs);
+    const uint32_t parity = (static_cast<uint32_t>(nj / kJobs) & 1u) ^ 1u;
+    ++nj;
+    if (!mbar_wait_ns(&sm.job_empty[js], parity, kDrainWaitNs)) atomicOr(&a.ctl->err, kErrWaitTimeout);
+    sm.job[js].kind = kind;
+    sm.job[js].seq = seq;
+    mbar_arrive(&sm.job_full[js]);
+}
+
+__device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
+    long long nj = 0;
+    for (long long r = 0;; ++r) {
+        const int slot = static_cast<int>(r % kRecs);
+        const uint32_t parity = static_cast<uint32_t>(r / kRecs) & 1u;
+        // Consumers may idle until other CTAs finish, hence the long bound.
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&sm.rec_full[slot], parity, kDrainWaitNs + kWaitNs));
+        if (!ok) {
+            if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+            break;
+        }
+        const Rec& rc = sm.rec[slot];
+        const int kind = rc.kind, flags = rc.flags, seq = rc.seq, rslot = rc.slot, seg = rc.seg, expect = rc.expect;
+        const float2 v = lane < kCW ? rc.wp[lane] : make_float2(-INFINITY, 0.0f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
+        if (kind == kEnd) break;
+        if (kind == kMain) {
+            // One partial per (row slot, segment): merge the eight warps.
+            float2 res;
+            if (flags == kRecArg) {
+                float M = v.x;
+                int I = lane < kCW ? __float_as_int(v.y) : INT_MAX;
+                warp_merge_arg(M, I);
+                res = make_float2(M, __int_as_float(I));
+            } else {
+                float M = v.x, S = v.y;
+                warp_merge_mc(M, S);
+                res = make_float2(M, S);
+            }
+            if (lane == 0) {
+                a.part[static_cast<size_t>(rslot) * a.nseg + seg] = res;
+                if (atomic_add_acq_rel(a.seq_count + seq, 1) == expect - 1) push_job(a, sm, nj, kJobDecide, seq);
+            }
+        } else {
+            // Tail sub-chunks keep every warp's slice partial.
+            if (lane < kCW) a.tpart[(static_cast<size_t>(seq) * a.nt + rslot) * kCW + lane] = v;
+            __syncwarp();
+            if (lane == 0 && (flags & kLast)) {
+                if (atomic_add_acq_rel(a.tail_count + seq, 1) == a.ntask - 1) push_job(a, sm, nj, kJobSelect, seq);
+            }
+        }
+        __syncwarp();
+    }
+    if (lane == 0) push_job(a, sm, nj, kJobEnd, 0);
+}
+
+template <typename Elem>
+__device__ void finisher(const VerifyArgs& a, SmemV& sm, int lane) {
+    for (long long j = 0;; ++j) {
+        const int js = static_cast<int>(j % kJobs);
+        const uint32_t parity = static_cast<uint32_t>(j / kJobs) & 1u;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&sm.job_full[js], parity, kDrainWaitNs + 2 * kWaitNs));
+        if (!ok) {
+            if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+            return;
+        }
+        const int kind = sm.job[js].kind, seq = sm.job[js].seq;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.job_empty[js]);
+        if (kind == kJobEnd) return;
+        if (kind == kJobDecide)
+            decide_warp<Elem>(a, sm, seq, lane);
+        else
+            select_warp<Elem>(a, sm, seq, lane);
+    }
+}
+
+// =============================================================================
+// Scheduler thread: decides what to stream next, absorbing every global
+// memory round trip (work counter, ticket flags, task records, sequence
+// lookups) so that the issuer never waits on one.
+// =============================================================================
+
+struct SeqCache {
+    int i, start, end, len;
+    float T;
+    bool ok;
+};
+
+// Main item w as work for the issuer; false if the item reads nothing.
+__device__ bool main_work(const VerifyArgs& a, const SmemV& sm, long long w, SeqCache& sc, Work& wk) {
+    const int slot = static_cast<int>(w / a.nseg);
+    const int seg = static_cast<int>(w - static_cast<long long>(slot) * a.nseg);
+    const int r = slot >> 1, kind = slot & 1;
+    if (!(r >= sc.start && r < sc.end)) {
+        const bool small = a.num_seqs <= kSmemSeqs;
+        const int* offs = small ? sm.offs : a.seq_offsets;
+        const int i = seq_of_position_t(offs, a.num_seqs, r);
+        const SeqInfo s = seq_lookup(a, sm, i);
+        sc.i = i;
+        sc.start = s.start;
+        sc.len = s.len;
+        sc.end = s.in_range ? s.start + max(s.len, 0) : s.start;
+        sc.T = s.T;
+        sc.ok = s.ok;
+        if (!(r >= sc.start && r < sc.end)) {
+            sc.start = sc.end = 0;
+            return false;  // position outside every sequence
+        }
+    }
+    if (!sc.ok) return false;
+    if (kind == 1 && sc.T == 0.0f) return false;  // greedy verification never reads q
+    wk.kind = kMain;
+    wk.seq = sc.i;
+    wk.slot = slot;
+    wk.seg = seg;
+    wk.expect = (sc.T > 0.0f ? 2 : 1) * sc.len * a.nseg;
+    wk.c0 = seg * a.spseg;
+    wk.c1 = min(wk.c0 + a.spseg, a.nck);
+    wk.c2 = sc.T > 0.0f ? inv_temp_log2e(sc.T) : 0.0f;
+    wk.row0 = kind ? a.q + static_cast<int64_t>(r) * a.ldq_bytes : a.p + static_cast<int64_t>(r + sc.i) * a.ldp_bytes;
+    wk.row1 = nullptr;
+    return true;
+}
+
+// Tail task of a published queue slot as work for the issuer.
+__device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
+    st_volatile(a.task_ready + slot, 0);  // the flag was read with acquire
+    const int2 task = __ldcg(a.tasks + slot);
+    const int i = task.x, y = task.y;
+    const int4* tw = reinterpret_cast<const int4*>(a.tails + i);
+    const int4 w0 = __ldcg(tw), w1 = __ldcg(tw + 1), w2 = __ldcg(tw + 2);
+    wk.kind = w0.x;
+    wk.seq = i;
+    wk.slot = 0;
+    wk.seg = 0;
+    wk.expect = 0;
+    wk.c0 = y * a.tpt;
+    wk.c1 = min(wk.c0 + a.tpt, a.nt);
+    wk.c2 = __int_as_float(w1.x);
+    wk.mc0 = __int_as_float(w1.y);
+    wk.inv0 = __int_as_float(w1.z);
+    wk.mc1 = __int_as_float(w1.w);
+    wk.inv1 = __int_as_float(w2.x);
+    wk.row0 = a.p + static_cast<int64_t>(w0.z) * a.ldp_bytes;
+    wk.row1 = a.q + static_cast<int64_t>(w0.w) * a.ldq_bytes;
+}
+
+__device__ void scheduler(const VerifyArgs& a, SmemV& sm, unsigned long long next) {
+    bool main_done = sm.batch_bad != 0 || a.n_main == 0;
+    SeqCache sc = {0, 0, 0, 0, 0.0f, false};
+    // Tail tasks are handed out as tickets: every scheduler holds at most one
+    // ticket (a task-queue slot, one atomic to take it) and schedules that
+    // slot's task as soon as a decision publishes it, ahead of main items.
+    const int cap = a.num_seqs * a.ntask;
+    int ticket = -1;
+    bool tickets_left = cap > 0;
+    bool failed = false;
+    for (long long k = 0;; ++k) {
+        const int ws = static_cast<int>(k % kWork);
+        const uint32_t parity = (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u;
+        if (!mbar_wait_ns(&sm.work_empty[ws], parity, kDrainWaitNs + kWaitNs)) {
+            atomicOr(&a.ctl->err, kErrWaitTimeout);
+            return;  // the issuer times out on its own wait
+        }
+        Work& wk = sm.work[ws];
+        bool have = false;
+        uint64_t t_idle = 0;
+        while (!have) {
+            if (ticket < 0 && tickets_left) {
+                ticket = atomicAdd(&a.ctl->tail_claim, 1);
+                if (ticket >= cap) {
+                    ticket = -1;
+                    tickets_left = false;
+                }
+            }
+            if (ticket >= 0 && ld_acquire(a.task_ready + ticket) != 0) {
+                tail_work(a, ticket, wk);
+                ticket = -1;
+                have = true;
+                break;
+            }
+            if (!main_done) {
+                const unsigned long long w = next;
+                if (w < static_cast<unsigned long long>(a.n_main)) {
+                    next = atomicAdd(&a.ctl->grab, 1ull);
+                    have = main_work(a, sm, static_cast<long long>(w), sc, wk);
+                    t_idle = 0;
+                    continue;
+                }
+                main_done = true;
+            }
+            if (ld_volatile(&a.ctl->finalized) >= sm.n_valid) break;  // every sequence is final
+            if (t_idle == 0) {
+                t_idle = global_timer_ns();
+            } else if (global_timer_ns() - t_idle > kDrainWaitNs) {
+                atomicOr(&a.ctl->err, kErrWaitTimeout);
+                failed = true;
+                break;
+            }
+            __nanosleep(100);
+        }
+        if (!have) wk.kind = kEnd;
+        mbar_arrive(&sm.work_full[ws]);
+        if (!have || failed) return;
+    }
+}
+
+// =============================================================================
+// Issuer thread: streams the scheduled work's sub-chunks into the stage ring.
+// =============================================================================
+
+__device__ __forceinline__ int acquire_stage(SmemV& sm, long long n, int* err) {
+    const int stage = static_cast<int>(n % kStagesV);
+    const uint32_t parity = (static_cast<uint32_t>(n / kStagesV) & 1u) ^ 1u;
+    if (!mbar_wait_ns(&sm.empty[stage], parity, kWaitNs)) {
+        atomicOr(err, kErrWaitTimeout);
+        return -1;
+    }
+    return stage;
+}
+
+template <typename Elem>
+__device__ void issuer(const VerifyArgs& a, SmemV& sm) {
+    constexpr int E = sizeof(Elem);
+    long long n = 0;
+    for (long long k = 0;; ++k) {
+        const int ws = static_cast<int>(k % kWork);
+        const uint32_t parity = static_cast<uint32_t>(k / kWork) & 1u;
+        if (!mbar_wait_ns(&sm.work_full[ws], parity, kDrainWaitNs + kWaitNs)) {
+            atomicOr(&a.ctl->err, kErrWaitTimeout);
+            break;
+        }
+        const Work wk = sm.work[ws];
+        mbar_arrive(&sm.work_empty[ws]);
+        if (wk.kind == kEnd) break;
+        const bool main = wk.kind == kMain;
+        const int ck = main ? a.ck : a.ckt;
+        bool ok = true;
+        for (int c = wk.c0; c < wk.c1 && ok; ++c) {
+            const int e0 = c * ck;
+            const int nel = min(ck, a.vocab - e0);
+            const Piece pa = make_piece<E>(wk.row0, e0, nel);
+            Piece pb = {};
+            if (wk.kind == kTailRes) pb = make_piece<E>(wk.row1, e0, nel);
+            const int stage = acquire_stage(sm, n, &a.ctl->err);
+            if (stage < 0) {
+                ok = false;
+                break;
+            }
+            Desc& d = sm.desc[stage];
+            d.kind = wk.kind;
+            d.flags = main ? ((c == wk.c0 ? kFirst : 0) | (c == wk.c1 - 1 ? kLast : 0)) : (c == wk.c1 - 1 ? kLast : 0);
+            d.seq = wk.seq;
+            d.slot = main ? wk.slot : c;
+            d.seg = wk.seg;
+            d.expect = wk.expect;
+            d.e0 = e0;
+            d.n = nel;
+            d.nvec = pa.bytes >> 4;
+            d.nsm0 = pa.nsm;
+            d.skip0 = pa.skip;
+            d.tail0 = pa.tail;
+            d.nsm1 = pb.nsm;
+            d.skip1 = pb.skip;
+            d.tail1 = pb.tail;
+            d.c2 = wk.c2;
+            d.mc0 = wk.mc0;
+            d.inv0 = wk.inv0;
+            d.mc1 = wk.mc1;
+            d.inv1 = wk.inv1;
+            const int bytes = pa.bytes + pb.bytes;
+            if (bytes > 0) {
+                mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(bytes));
+                if (pa.bytes > 0)
+                    bulk_copy_g2s(sm.stage[stage], reinterpret_cast<const void*>(pa.lo),
+                                  static_cast<uint32_t>(pa.bytes), &sm.full[stage]);
+                if (pb.bytes > 0)
+                    bulk_copy_g2s(sm.stage[stage] + kHalf, reinterpret_cast<const void*>(pb.lo),
+                                  static_cast<uint32_t>(pb.bytes), &sm.full[stage]);
+            } else {
+                mbar_arrive(&sm.full[stage]);
+            }
+            ++n;
+        }
+        if (!ok) break;
+    }
+    const int stage = acquire_stage(sm, n, &a.ctl->err);
+    if (stage >= 0) {
+        sm.desc[stage].kind = kEnd;
+        mbar_arrive(&sm.full[stage]);
+    }
+}
+
+// =============================================================================
+// Consumer warps
+// =============================================================================
+
+struct MainState {
+    float m, mc;
+    uint64_t acc0, acc1;
+    int amx;
+};
+
+// Hand this warp's partial for the current record to the bookkeeper.
+__device__ __forceinline__ void push_record(const VerifyArgs& a, SmemV& sm, long long& nrec, int warp, int lane,
+                                            float2 part, int kind, int flags, int seq, int slot, int seg,
+                                            int expect) {
+    const int rs = static_cast<int>(nrec % kRecs);
+    const uint32_t parity = (static_cast<uint32_t>(nrec / kRecs) & 1u) ^ 1u;
+    ++nrec;
+    if (lane == 0) {
+        if (!mbar_wait_ns(&sm.rec_empty[rs], parity, kDrainWaitNs)) atomicOr(&a.ctl->err, kErrWaitTimeout);
+        Rec& rc = sm.rec[rs];
+        rc.wp[warp] = part;
+        if (warp == 0) {
+            rc.kind = kind;
+            rc.flags = flags;
+            rc.seq = seq;
+            rc.slot = slot;
+            rc.seg = seg;
+            rc.expect = expect;
+        }
+        mbar_arrive(&sm.rec_full[rs]);
+    }
+    __syncwarp();
+}
+
+template <typename Elem>
+__device__ __forceinline__ void main_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int tid,
+                                           int warp, int lane, MainState& ms, long long& nrec) {
+    constexpr bool kBf16 = sizeof(Elem) == 2;
+    constexpr uint32_t kNeg = kBf16 ? 0xff80ff80u : 0xff800000u;  // -inf pattern
+    uint32_t w[kVecPT * 4];
+    const uint4* sv = reinterpret_cast<const uint4*>(sm.stage[stage]);
+#pragma unroll
+    for (int k = 0; k < kVecPT; ++k) {
+        const int vi = tid + k * kCT;
+        const uint4 v = vi < d.nvec ? sv[vi] : make_uint4(kNeg, kNeg, kNeg, kNeg);
+        w[4 * k] = v.x;
+        w[4 * k + 1] = v.y;
+        w[4 * k + 2] = v.z;
+        w[4 * k + 3] = v.w;
+    }
+    if (d.skip0 != 0 && tid == 0) {  // elements before the sub-chunk in the first vector
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if constexpr (kBf16) {
+                if (2 * j < d.skip0) w[j] = (w[j] & 0xffff0000u) | 0xff80u;
+                if (2 * j + 1 < d.skip0) w[j] = (w[j] & 0x0000ffffu) | 0xff800000u;
+            } else {
+                if (j < d.skip0) w[j] = kNeg;
+            }
+        }
+    }
+    const int ntail = d.n - d.nsm0;
+    float tv = -INFINITY;
+    if (tid < ntail) tv = load_elem<Elem>(d.tail0 + static_cast<size_t>(tid) * sizeof(Elem));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+
+    if (d.flags & kFirst) {
+        ms.m = -INFINITY;
+        ms.mc = -INFINITY;
+        ms.acc0 = 0;
+        ms.acc1 = 0;
+        ms.amx = INT_MAX;
+    }
+    float cm;
+    if constexpr (kBf16) {
+        uint32_t mx = w[0];
+#pragma unroll
+        for (int j = 1; j < kVecPT * 4; ++j) mx = hmax2_bf16(mx, w[j]);
+        cm = fmaxf(bf16lo(mx), bf16hi(mx));
+    } else {
+        cm = __uint_as_float(w[0]);
+#pragma unroll
+        for (int j = 1; j < kVecPT * 4; ++j) cm = fmaxf(cm, __uint_as_float(w[j]));
+    }
+    cm = fmaxf(cm, tv);
+    const float c2 = d.c2;
+    if (c2 > 0.0f) {
+        if (cm > ms.m) {
+            const float mcn = cm * c2;
+            if (ms.m != -INFINITY) {
+                const float sc = ex2_approx(ms.mc - mcn);
+                const uint64_t sc2 = pack_f2(sc, sc);
+                ms.acc0 = mul_f2(ms.acc0, sc2);
+                ms.acc1 = mul_f2(ms.acc1, sc2);
+            }
+            ms.m = cm;
+            ms.mc = mcn;
+        }
+        if (ms.m != -INFINITY) {
+            const uint64_t C2 = pack_f2(c2, c2), NMC = pack_f2(-ms.mc, -ms.mc);
+#pragma unroll
+            for (int j = 0; j < kVecPT * 4; j += 2) {
+                if constexpr (kBf16) {
+                    float y0, y1, y2, y3;
+                    unpack_f2(fma_f2(pack_f2(bf16lo(w[j]), bf16hi(w[j])), C2, NMC), y0, y1);
+                    unpack_f2(fma_f2(pack_f2(bf16lo(w[j + 1]), bf16hi(w[j + 1])), C2, NMC), y2, y3);
+                    ms.acc0 = add_f2(ms.acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+                    ms.acc1 = add_f2(ms.acc1, pack_f2(ex2_approx(y2), ex2_approx(y3)));
+                } else {
+                    float y0, y1;
+                    unpack_f2(fma_f2(pack_f2(__uint_as_float(w[j]), __uint_as_float(w[j + 1])), C2, NMC), y0, y1);
+                    if (j & 2)
+                        ms.acc1 = add_f2(ms.acc1, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+                    else
+                        ms.acc0 = add_f2(ms.acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+                }
+            }
+            if (tv != -INFINITY) ms.acc1 = add_f2(ms.acc1, pack_f2(soft_w(tv, c2, ms.mc), 0.0f));
+        }
+    } else if (cm > ms.m) {
+        // First position of the new maximum in this thread's (ascending) elements.
+        constexpr int kPer = kBf16 ? 8 : 4;
+        int idx = INT_MAX;
+        if (tv == cm) idx = d.nsm0 + tid;
+#pragma unroll
+        for (int k = kVecPT - 1; k >= 0; --k) {
+#pragma unroll
+            for (int j = 3; j >= 0; --j) {
+                const uint32_t x = w[4 * k + j];
+                const int base = (tid + k * kCT) * kPer - d.skip0;
+                if constexpr (kBf16) {
+                    if (bf16hi(x) == cm) idx = base + 2 * j + 1;
+                    if (bf16lo(x) == cm) idx = base + 2 * j;
+                } else {
+                    if (__uint_as_float(x) == cm) idx = base + j;
+                }
+            }
+        }
+        ms.m = cm;
+        ms.amx = d.e0 + idx;
+    }
+
+    if (d.flags & kLast) {
+        float2 part;
+        int mode;
+        if (c2 > 0.0f) {
+            float s0, s1, s2, s3;
+            unpack_f2(ms.acc0, s0, s1);
+            unpack_f2(ms.acc1, s2, s3);
+            float M = ms.m == -INFINITY ? -INFINITY : ms.mc, S = (s0 + s1) + (s2 + s3);
+            warp_merge_mc(M, S);
+            part = make_float2(M, S);
+            mode = kRecSoft;
+        } else {
+            float M = ms.m;
+            int I = ms.amx;
+            warp_merge_arg(M, I);
+            part = make_float2(M, __int_as_float(I));
+            mode = kRecArg;
+        }
+        push_record(a, sm, nrec, warp, lane, part, kMain, mode, d.seq, d.slot, d.seg, d.expect);
+    }
+}
+
+// A tail stage: each consumer warp reduces its own contiguous slice of the
+// sub-chunk (about 1/8 of it), so the selection can later narrow a draw down
+// to one slice.
+template <typename Elem>
+__device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int warp,
+                                           int lane, long long& nrec) {
+    const unsigned char* s0 = sm.stage[stage];
+    const unsigned char* s1 = s0 + kHalf;
+    const int spw = (d.n + kCW - 1) / kCW;
+    const int wb = min(d.n, warp * spw), we = min(d.n, wb + spw);
+    float2 part;
+    if (d.kind == kTailRes) {
+        float sw = 0.0f, sp = 0.0f;
+#pragma unroll 4
+        for (int e = wb + lane; e < we; e += 32) {
+            const float xp = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
+            const float xq = piece_elem<Elem>(s1, d.nsm1, d.skip1, d.tail1, e);
+            float pv;
+            sw += resid_w(xp, xq, d.c2, d.mc0, d.inv0, d.mc1, d.inv1, pv);
+            sp += pv;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+        part = make_float2(warp_sum(sw), warp_sum(sp));
+    } else if (d.kind == kTailSoft) {
+        float mt = -INFINITY;
+        for (int e = wb + lane; e < we; e += 32) mt = fmaxf(mt, piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e));
+        const float mct = mt * d.c2;
+        float st = 0.0f;
+        if (mt != -INFINITY)
+            for (int e = wb + lane; e < we; e += 32)
+                st += soft_w(piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e), d.c2, mct);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+        float M = mt == -INFINITY ? -INFINITY : mct, S = st;
+        warp_merge_mc(M, S);
+        part = make_float2(M, S);
+    } else {  // kTailArg
+        float mt = -INFINITY;
+        int it = INT_MAX;
+        for (int e = wb + lane; e < we; e += 32) {
+            const float x = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
+            if (x > mt) {
+                mt = x;
+                it = d.e0 + e;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+        warp_merge_arg(mt, it);
+        part = make_float2(mt, __int_as_float(it));
+    }
+    push_record(a, sm, nrec, warp, lane, part, d.kind, d.flags, d.seq, d.slot, 0, 0);
+}
+
+template <typename Elem>
+__device__ void consumer(const VerifyArgs& a, SmemV& sm, int tid, int warp, int lane) {
+    MainState ms = {-INFINITY, -INFINITY, 0, 0, INT_MAX};
+    long long nrec = 0;
+    long long n = 0;
+    for (;; ++n) {
+        const int stage = static_cast<int>(n % kStagesV);
+        const uint32_t parity = static_cast<uint32_t>(n / kStagesV) & 1u;
+        // The issuer may idle until other CTAs finish, hence the long bound.
+        if (!__all_sync(0xffffffffu, mbar_wait_ns(&sm.full[stage], parity, kDrainWaitNs + kWaitNs))) {
+            if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+            break;
+        }
+        const Desc d = sm.desc[stage];
+        if (d.kind == kEnd) break;
+        if (d.kind == kMain)
+            main_stage<Elem>(a, sm, stage, d, tid, warp, lane, ms, nrec);
+        else
+            tail_stage<Elem>(a, sm, stage, d, warp, lane, nrec);
+    }
+    // Tell the bookkeeper there is no more work (a record of kind kEnd).
+    push_record(a, sm, nrec, warp, lane, make_float2(0.0f, 0.0f), kEnd, 0, 0, 0, 0, 0);
+}
+
+// =============================================================================
+// Kernel
+// =============================================================================
+
+template <typename Elem>
+__global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(const VerifyArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    SmemV& sm = *reinterpret_cast<SmemV*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    pdl_wait();
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < kStagesV; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kCW);
+        }
+        for (int s = 0; s < kRecs; ++s) {
+            mbar_init(&sm.rec_full[s], kCW);
+            mbar_init(&sm.rec_empty[s], 1);
+        }
+        for (int s = 0; s < kWork; ++s) {
+            mbar_init(&sm.work_full[s], 1);
+            mbar_init(&sm.work_empty[s], 1);
+        }
+        for (int s = 0; s < kJobs; ++s) {
+            mbar_init(&sm.job_full[s], 1);
+            mbar_init(&sm.job_empty[s], 1);
+        }
+        fence_mbarrier_init();
+        sm.n_valid = 0;
+    }
+    // The scheduler's first main item, requested while the prologue runs.
+    unsigned long long first = 0;
+    if (tid == kSchedWarp * 32 && a.n_main > 0) first = atomicAdd(&a.ctl->grab, 1ull);
+    // Every CTA counts the valid sequences (the grid's exit condition) and
+    // checks that the offsets never decrease; small batches keep the offsets
+    // and temperatures in shared memory.
+    int nv = 0;
+    bool bad = false;
+    const bool small = a.num_seqs <= kSmemSeqs;
+    for (int i = tid; i < a.num_seqs; i += kThreadsV) {
+        const SeqInfo s = seq_info(a.seq_offsets, a.temperature, i, a.total);
+        nv += s.ok ? 1 : 0;
+        const int end = __ldg(a.seq_offsets + i + 1);
+        bad = bad || end < s.start;
+        if (small) {
+            sm.offs[i] = s.start;
+            sm.temp[i] = s.T;
+            if (i == a.num_seqs - 1) sm.offs[i + 1] = end;
+        }
+    }
+    __syncthreads();
+    if (nv) atomicAdd(&sm.n_valid, nv);
+    bad = __syncthreads_or(bad);
+    if (tid == 0) {
+        sm.batch_bad = bad;
+        if (bad) sm.n_valid = 0;
+    }
+    __syncthreads();
+
+    if (warp == kIssuerWarp) {
+        if (lane == 0) issuer<Elem>(a, sm);
+    } else if (warp == kSchedWarp) {
+        if (lane == 0) scheduler(a, sm, first);
+    } else if (warp == kBookWarp) {
+        bookkeeper(a, sm, lane);
+    } else if (warp == kFinWarp) {
+        finisher<Elem>(a, sm, lane);
+    } else {
+        // This CTA's share of the sequences that are invalid as laid out.
+        for (long long i = blockIdx.x + static_cast<long long>(warp) * gridDim.x; i < a.num_seqs;
+             i += static_cast<long long>(kCW) * gridDim.x) {
+            const SeqInfo s = seq_info(a.seq_offsets, a.temperature, static_cast<int>(i), a.total);
+            if (bad || !s.ok) write_invalid(a, static_cast<int>(i), s, lane, -1);
+        }
+        consumer<Elem>(a, sm, tid, warp, lane);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&a.ctl->exited, 1) == static_cast<int>(gridDim.x) - 1) {
+            __threadfence();
+            if (ld_volatile(&a.ctl->err) != 0)
+                for (int i = 0; i < a.num_seqs; ++i) a.accept_len[i] = -2;
+            a.ctl->grab = 0;
+            a.ctl->tail_reserve = 0;
+            a.ctl->tail_claim = 0;
+            a.ctl->finalized = 0;
+            a.ctl->exited = 0;
+        }
+    }
+}
+
+template <typename Elem>
+cudaError_t launch_verify_t(const VerifyArgs& a, int grid, cudaStream_t stream) {
+    const size_t smem = sizeof(SmemV) + 128;
+    cudaError_t err = cudaFuncSetAttribute(verify_kernel<Elem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsV);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, verify_kernel<Elem>, a);
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyArgs& a, int elem_bytes, int grid, cudaStream_t stream) {
+    return elem_bytes == 2 ? launch_verify_t<__nv_bfloat16>(a, grid, stream) : launch_verify_t<float>(a, grid, stream);
+}
+
+}  // namespace isd
