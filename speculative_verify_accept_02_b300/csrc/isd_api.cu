@@ -29,7 +29,7 @@ struct VerifyPlan {
     int ck, nck, spseg, nseg, ckt, nt, tpt, ntask;
 };
 
-constexpr int kSubChunksPerSegment = 4;  // one main item: 4 x 16 KB
+constexpr int kSubChunksPerSegment = 8;  // one main item: 8 x 16 KB
 constexpr int kTailSubChunksPerTask = 4;
 
 VerifyPlan verify_plan(int vocab, int esz) {

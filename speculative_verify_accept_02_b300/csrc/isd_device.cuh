@@ -263,15 +263,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
-// Wait bounded by the global timer; false on timeout.
+// Non-blocking check whether the phase of `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait with a suspend-time hint: the thread sleeps in hardware until the phase
+// completes or about `ns` nanoseconds pass; true if the phase completed.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return done != 0;
+}
+
+// Wait bounded by the global timer; false on timeout.  Sleeps in hardware
+// between checks, so a waiting warp issues almost no instructions.
 __device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-    for (int it = 0; it < 64; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_for(bar, parity, 1000)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_for(bar, parity, 10000)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
-        __nanosleep(64);
     }
 }
 

@@ -21,20 +21,21 @@
 //
 // Warp roles of a CTA:
 //   scheduler   (one thread) takes work: the next main item from the global
-//               counter, or a published tail task; it absorbs every global
-//               memory round trip and keeps a 2-entry work ring filled;
-//   issuer      (one thread) streams the scheduled sub-chunks into a 5-stage
-//               shared-memory ring with 1-D bulk copies and never waits on
-//               global memory;
+//               counter into a 4-entry work ring, a published tail task into
+//               a priority slot; it absorbs every global memory round trip;
+//   issuer      (one thread) streams the scheduled sub-chunks into a 4-stage
+//               shared-memory ring with 1-D bulk copies, serving the priority
+//               slot between any two sub-chunks; it never waits on global
+//               memory;
 //   consumers   (8 warps) fold each stage into per-thread online softmax
 //               partials (packed bf16 maxima, packed fp32 FMAs, one ex2 per
 //               logit) or an exact argmax; at the end of an item every warp
 //               hands its warp partial to the bookkeeper through a record
 //               ring and moves on: consumers never wait on each other or on
 //               global memory;
-//   bookkeeper  (one warp) merges the records, stores partials, counts
-//               finished items per sequence with device-scope atomics, and
-//               runs decisions and selections itself.
+//   bookkeeper  (one warp) merges the records in batches, stores partials and
+//               counts finished items per sequence with device-scope atomics;
+//   finishers   (two warps) run the decisions and selections it triggers.
 // The grid exits once every sequence is final; its last CTA re-zeroes the
 // control block for the next call.  Every wait is bounded by the global timer.
 #include <climits>
@@ -50,11 +51,12 @@ constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kIssuerWarp = kCW;
 constexpr int kBookWarp = kCW + 1;
 constexpr int kSchedWarp = kCW + 2;
-constexpr int kFinWarp = kCW + 3;
-constexpr int kThreadsV = kCT + 128;      // + issuer, bookkeeper, scheduler and finisher warps
+constexpr int kFinWarp = kCW + 3;         // first of kFinishers finisher warps
+constexpr int kFinishers = 2;
+constexpr int kThreadsV = kCT + 32 * (3 + kFinishers);  // + issuer, bookkeeper, scheduler, finishers
 constexpr int kStagesV = 4;
 constexpr int kJobs = 16;                 // job ring between bookkeeper and finisher
-constexpr int kWork = 2;                  // work ring between scheduler and issuer
+constexpr int kWork = 4;                  // work ring between scheduler and issuer
 constexpr int kRecs = 8;                  // record ring between consumers and bookkeeper
 constexpr int kVecPT = kStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
 constexpr int kHalf = kStageBytes / 2;          // tail stages: [p piece | q piece]
@@ -114,12 +116,16 @@ struct SmemV {
     uint64_t rec_empty[kRecs];
     uint64_t work_full[kWork];
     uint64_t work_empty[kWork];
+    uint64_t prio_full;   // scheduler -> issuer: one tail task ahead of queued main items
+    uint64_t prio_empty;
     uint64_t job_full[kJobs];
     uint64_t job_empty[kJobs];
     Job job[kJobs];
-    float2 tsel[kMaxTailChunks * kCW];  // finisher's copy of one sequence's slice partials
+    float2 tsel[kFinishers][kMaxTailChunks * kCW];  // each finisher's copy of one sequence's slice partials
+    int job_take;
     Desc desc[kStagesV];
     Work work[kWork];
+    Work prio;
     Rec rec[kRecs];
     int n_valid;
     int batch_bad;
@@ -250,6 +256,16 @@ __device__ __forceinline__ Piece make_piece(const char* row, int e0, int n) {
     return pc;
 }
 
+// Slice of a tail sub-chunk of n ids owned by consumer warp w: ids [b, e).
+// Slices start on 16-byte boundaries of the sub-chunk.
+template <int E>
+__device__ __forceinline__ void tail_slice(int n, int w, int& b, int& e) {
+    constexpr int vec = 16 / E;
+    const int spw = ((n + kCW - 1) / kCW + vec - 1) / vec * vec;
+    b = min(n, w * spw);
+    e = min(n, b + spw);
+}
+
 // =============================================================================
 // Bookkeeper warp
 // =============================================================================
@@ -369,7 +385,7 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
 // the draw picks a slice from them, then scans that slice in vocabulary
 // order from registers.
 template <typename Elem>
-__device__ void select_warp(const VerifyArgs& a, SmemV& sm, int i, int lane) {
+__device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int lane) {
     constexpr int E = sizeof(Elem);
     // One round trip: the tail state (written by the decision before its tasks
     // were published) and every slice partial, into shared memory.
@@ -378,7 +394,7 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int i, int lane) {
     if (lane < 3) tv = __ldcg(tw + lane);
     const int U = a.nt * kCW;
     const float2* tp = a.tpart + static_cast<size_t>(i) * U;
-    for (int u = lane; u < U; u += 32) sm.tsel[u] = __ldcg(tp + u);
+    for (int u = lane; u < U; u += 32) sm.tsel[fi][u] = __ldcg(tp + u);
     SeqTail t;
     t.mode = __shfl_sync(0xffffffffu, tv.x, 0);
     t.a = __shfl_sync(0xffffffffu, tv.y, 0);
@@ -395,7 +411,7 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int i, int lane) {
     if (t.mode == kTailArg) {
         float M = -INFINITY;
         int I = INT_MAX;
-        for (int u = lane; u < U; u += 32) merge_argmax(M, I, sm.tsel[u].x, __float_as_int(sm.tsel[u].y));
+        for (int u = lane; u < U; u += 32) merge_argmax(M, I, sm.tsel[fi][u].x, __float_as_int(sm.tsel[fi][u].y));
         warp_merge_arg(M, I);
         if (lane == 0) {
             a.out_tokens[out_slot] = I;
@@ -407,17 +423,17 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int i, int lane) {
     // Slice weights in one scale, the target u * total, and its slice.
     float MC = -INFINITY;
     if (t.mode == kTailSoft)
-        for (int u = lane; u < U; u += 32) MC = fmaxf(MC, sm.tsel[u].x);
+        for (int u = lane; u < U; u += 32) MC = fmaxf(MC, sm.tsel[fi][u].x);
     MC = warp_max(MC);
     bool fallback = false;
     if (t.mode == kTailRes) {
         float W = 0.0f;
-        for (int u = lane; u < U; u += 32) W += sm.tsel[u].x;
+        for (int u = lane; u < U; u += 32) W += sm.tsel[fi][u].x;
         fallback = !(warp_sum(W) > 0.0f);  // residual rounded to zero: draw from p_j
     }
     auto slice_w = [&](int u) -> float {
         if (u >= U) return 0.0f;
-        const float2 v = sm.tsel[u];
+        const float2 v = sm.tsel[fi][u];
         if (t.mode == kTailSoft) return v.x == -INFINITY ? 0.0f : v.y * ex2_approx(v.x - MC);
         return fallback ? v.y : v.x;
     };
@@ -454,9 +470,10 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int i, int lane) {
     // The chosen slice: ids [lo, lo + len) of the tail row(s).
     const int c = chosen / kCW, w = chosen % kCW;
     const int nc = min(a.ckt, a.vocab - c * a.ckt);
-    const int spw = (nc + kCW - 1) / kCW;
-    const int lo = c * a.ckt + min(nc, w * spw);
-    const int len = min(nc, w * spw + spw) - min(nc, w * spw);
+    int sb, se;
+    tail_slice<E>(nc, w, sb, se);
+    const int lo = c * a.ckt + sb;
+    const int len = se - sb;
     const char* prow = a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
     const char* qrow = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes;
     const int q = (len + 31) / 32;  // at most kSliceMax / 32 ids per lane
@@ -526,57 +543,105 @@ __device__ __forceinline__ void push_job(const VerifyArgs& a, SmemV& sm, long lo
     mbar_arrive(&sm.job_full[js]);
 }
 
+// Warp reductions within aligned groups of 8 lanes.
+__device__ __forceinline__ void group8_merge_mc(float& M, float& S) {
+    float W = M;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) W = fmaxf(W, __shfl_xor_sync(0xffffffffu, W, o, 8));
+    S = (M == -INFINITY) ? 0.0f : S * ex2_approx(M - W);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o, 8);
+    M = W;
+}
+__device__ __forceinline__ void group8_merge_arg(float& M, int& I) {
+    float W = M;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) W = fmaxf(W, __shfl_xor_sync(0xffffffffu, W, o, 8));
+    I = M == W ? I : INT_MAX;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) I = min(I, __shfl_xor_sync(0xffffffffu, I, o, 8));
+    M = W;
+}
+
+// Records are taken in batches of up to four that are already complete; lane
+// group g (8 lanes, one per consumer warp) handles record r + g, so the
+// device-scope counts of a batch overlap in one round trip.
 __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
     long long nj = 0;
-    for (long long r = 0;; ++r) {
-        const int slot = static_cast<int>(r % kRecs);
-        const uint32_t parity = static_cast<uint32_t>(r / kRecs) & 1u;
+    const int g = lane >> 3, wl = lane & 7;
+    for (long long r = 0;;) {
         // Consumers may idle until other CTAs finish, hence the long bound.
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&sm.rec_full[slot], parity, kDrainWaitNs + kWaitNs));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&sm.rec_full[r % kRecs],
+                                                             static_cast<uint32_t>(r / kRecs) & 1u,
+                                                             kDrainWaitNs + kWaitNs));
         if (!ok) {
             if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
             break;
         }
-        const Rec& rc = sm.rec[slot];
+        int nb = 1;
+        while (nb < 4 && mbar_test(&sm.rec_full[(r + nb) % kRecs], static_cast<uint32_t>((r + nb) / kRecs) & 1u))
+            ++nb;
+        const bool mine = g < nb;
+        const Rec& rc = sm.rec[(r + (mine ? g : 0)) % kRecs];
         const int kind = rc.kind, flags = rc.flags, seq = rc.seq, rslot = rc.slot, seg = rc.seg, expect = rc.expect;
-        const float2 v = lane < kCW ? rc.wp[lane] : make_float2(-INFINITY, 0.0f);
+        const float2 v = rc.wp[wl];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
-        if (kind == kEnd) break;
-        if (kind == kMain) {
-            // One partial per (row slot, segment): merge the eight warps.
-            float2 res;
-            if (flags == kRecArg) {
-                float M = v.x;
-                int I = lane < kCW ? __float_as_int(v.y) : INT_MAX;
-                warp_merge_arg(M, I);
-                res = make_float2(M, __int_as_float(I));
+        if (lane < nb) mbar_arrive(&sm.rec_empty[(r + lane) % kRecs]);
+        // An end marker is the last record: the batch stops there.
+        const unsigned end_mask = __ballot_sync(0xffffffffu, mine && wl == 0 && kind == kEnd);
+        const int n_real = end_mask ? (__ffs(end_mask) - 1) / 8 : nb;
+        const bool act = g < n_real;
+        int trig = 0;  // 1: decide this sequence, 2: select its token
+        // Both merges run on every lane (shuffles need the whole warp); each
+        // group keeps the one its record asks for.
+        float Mm = v.x, Sm = v.y;
+        group8_merge_mc(Mm, Sm);
+        float Ma = v.x;
+        int Ia = __float_as_int(v.y);
+        group8_merge_arg(Ma, Ia);
+        // A tail record's eight slice partials, gathered to the group leader so
+        // that its releasing count publishes them.
+        float2 sl[kCW];
+#pragma unroll
+        for (int k = 0; k < kCW; ++k) {
+            sl[k].x = __shfl_sync(0xffffffffu, v.x, (lane & ~7) + k);
+            sl[k].y = __shfl_sync(0xffffffffu, v.y, (lane & ~7) + k);
+        }
+        if (act && wl == 0) {
+            if (kind == kMain) {
+                a.part[static_cast<size_t>(rslot) * a.nseg + seg] =
+                    flags == kRecArg ? make_float2(Ma, __int_as_float(Ia)) : make_float2(Mm, Sm);
+                if (atomic_add_acq_rel(a.seq_count + seq, 1) == expect - 1) trig = 1;
             } else {
-                float M = v.x, S = v.y;
-                warp_merge_mc(M, S);
-                res = make_float2(M, S);
-            }
-            if (lane == 0) {
-                a.part[static_cast<size_t>(rslot) * a.nseg + seg] = res;
-                if (atomic_add_acq_rel(a.seq_count + seq, 1) == expect - 1) push_job(a, sm, nj, kJobDecide, seq);
-            }
-        } else {
-            // Tail sub-chunks keep every warp's slice partial.
-            if (lane < kCW) a.tpart[(static_cast<size_t>(seq) * a.nt + rslot) * kCW + lane] = v;
-            __syncwarp();
-            if (lane == 0 && (flags & kLast)) {
-                if (atomic_add_acq_rel(a.tail_count + seq, 1) == a.ntask - 1) push_job(a, sm, nj, kJobSelect, seq);
+                float4* dst = reinterpret_cast<float4*>(a.tpart + (static_cast<size_t>(seq) * a.nt + rslot) * kCW);
+#pragma unroll
+                for (int k = 0; k < kCW / 2; ++k) dst[k] = make_float4(sl[2 * k].x, sl[2 * k].y, sl[2 * k + 1].x, sl[2 * k + 1].y);
+                if ((flags & kLast) && atomic_add_acq_rel(a.tail_count + seq, 1) == a.ntask - 1) trig = 2;
             }
         }
+        // Hand the triggered jobs to the finishers, in record order.
+        const unsigned tmask = __ballot_sync(0xffffffffu, trig != 0);
+        for (unsigned m = tmask; m; m &= m - 1) {
+            const int src = __ffs(m) - 1;
+            const int tk = __shfl_sync(0xffffffffu, trig, src), ts = __shfl_sync(0xffffffffu, seq, src);
+            if (lane == 0) push_job(a, sm, nj, tk == 1 ? kJobDecide : kJobSelect, ts);
+        }
         __syncwarp();
+        r += nb;
+        if (end_mask) break;
     }
-    if (lane == 0) push_job(a, sm, nj, kJobEnd, 0);
+    if (lane == 0)
+        for (int f = 0; f < kFinishers; ++f) push_job(a, sm, nj, kJobEnd, 0);
 }
 
 template <typename Elem>
-__device__ void finisher(const VerifyArgs& a, SmemV& sm, int lane) {
-    for (long long j = 0;; ++j) {
-        const int js = static_cast<int>(j % kJobs);
+__device__ void finisher(const VerifyArgs& a, SmemV& sm, int fi, int lane) {
+    for (;;) {
+        // Jobs are claimed in order by whichever finisher is free.
+        int j = 0;
+        if (lane == 0) j = atomicAdd(&sm.job_take, 1);
+        j = __shfl_sync(0xffffffffu, j, 0);
+        const int js = j % kJobs;
         const uint32_t parity = static_cast<uint32_t>(j / kJobs) & 1u;
         const bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&sm.job_full[js], parity, kDrainWaitNs + 2 * kWaitNs));
         if (!ok) {
@@ -590,7 +655,7 @@ __device__ void finisher(const VerifyArgs& a, SmemV& sm, int lane) {
         if (kind == kJobDecide)
             decide_warp<Elem>(a, sm, seq, lane);
         else
-            select_warp<Elem>(a, sm, seq, lane);
+            select_warp<Elem>(a, sm, fi, seq, lane);
     }
 }
 
@@ -644,7 +709,7 @@ __device__ bool main_work(const VerifyArgs& a, const SmemV& sm, long long w, Seq
 
 // Tail task of a published queue slot as work for the issuer.
 __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
-    st_volatile(a.task_ready + slot, 0);  // the flag was read with acquire
+    st_volatile(a.task_ready + slot, 0);
     const int2 task = __ldcg(a.tasks + slot);
     const int i = task.x, y = task.y;
     const int4* tw = reinterpret_cast<const int4*>(a.tails + i);
@@ -669,60 +734,100 @@ __device__ void scheduler(const VerifyArgs& a, SmemV& sm, unsigned long long nex
     bool main_done = sm.batch_bad != 0 || a.n_main == 0;
     SeqCache sc = {0, 0, 0, 0, 0.0f, false};
     // Tail tasks are handed out as tickets: every scheduler holds at most one
-    // ticket (a task-queue slot, one atomic to take it) and schedules that
-    // slot's task as soon as a decision publishes it, ahead of main items.
+    // ticket (a task-queue slot, one atomic to take it) and passes that slot's
+    // task to the issuer through a priority slot as soon as a decision
+    // publishes it, ahead of the main items already queued.  Every global
+    // round trip is issued one pass before its result is looked at.
     const int cap = a.num_seqs * a.ntask;
-    int ticket = -1;
     bool tickets_left = cap > 0;
-    bool failed = false;
-    for (long long k = 0;; ++k) {
-        const int ws = static_cast<int>(k % kWork);
-        const uint32_t parity = (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u;
-        if (!mbar_wait_ns(&sm.work_empty[ws], parity, kDrainWaitNs + kWaitNs)) {
+    int ticket = -1, claim = 0, flag = 0;
+    bool claim_pending = false, claim_started = false;
+    long long k = 0, kp = 0;  // work items and priority items handed over
+    uint64_t t_idle = 0;
+    while (true) {
+        bool progress = false;
+        // 1. A published tail task goes to the priority slot.
+        if (claim_pending && ticket < 0) {
+            claim_pending = false;
+            if (claim < cap) {
+                ticket = claim;
+                flag = 0;
+            } else {
+                tickets_left = false;
+            }
+        }
+        if (ticket >= 0 && flag != 0 && mbar_test(&sm.prio_empty, (static_cast<uint32_t>(kp) & 1u) ^ 1u)) {
+            __threadfence();  // acquire: the task was published before its flag
+            tail_work(a, ticket, sm.prio);
+            mbar_arrive(&sm.prio_full);
+            ++kp;
+            ticket = -1;
+            flag = 0;
+            if (tickets_left) {
+                claim = atomicAdd(&a.ctl->tail_claim, 1);
+                claim_pending = true;
+            }
+            progress = true;
+        }
+        // 2. The next main item, while the work ring has room.
+        if (!main_done) {
+            const int ws = static_cast<int>(k % kWork);
+            if (mbar_test(&sm.work_empty[ws], (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u)) {
+                Work& wk = sm.work[ws];
+                bool have = false;
+                while (!have && !main_done) {
+                    const unsigned long long w = next;
+                    if (w < static_cast<unsigned long long>(a.n_main)) {
+                        next = atomicAdd(&a.ctl->grab, 1ull);
+                        have = main_work(a, sm, static_cast<long long>(w), sc, wk);
+                    } else {
+                        main_done = true;
+                    }
+                }
+                if (have) {
+                    mbar_arrive(&sm.work_full[ws]);
+                    ++k;
+                    progress = true;
+                }
+                // The first ticket is claimed once the first main item is on its way.
+                if (!claim_started && tickets_left) {
+                    claim_started = true;
+                    claim = atomicAdd(&a.ctl->tail_claim, 1);
+                    claim_pending = true;
+                }
+            }
+        }
+        // 3. Refresh the held ticket's flag (looked at on the next pass).
+        if (ticket >= 0) flag = ld_volatile(a.task_ready + ticket);
+        if (!claim_started && main_done && tickets_left) {
+            claim_started = true;
+            claim = atomicAdd(&a.ctl->tail_claim, 1);
+            claim_pending = true;
+        }
+        if (progress) {
+            t_idle = 0;
+            continue;
+        }
+        if (main_done && ld_volatile(&a.ctl->finalized) >= sm.n_valid) break;  // every sequence is final
+        if (t_idle == 0) {
+            t_idle = global_timer_ns();
+        } else if (global_timer_ns() - t_idle > kDrainWaitNs) {
             atomicOr(&a.ctl->err, kErrWaitTimeout);
-            return;  // the issuer times out on its own wait
+            break;
         }
-        Work& wk = sm.work[ws];
-        bool have = false;
-        uint64_t t_idle = 0;
-        while (!have) {
-            if (ticket < 0 && tickets_left) {
-                ticket = atomicAdd(&a.ctl->tail_claim, 1);
-                if (ticket >= cap) {
-                    ticket = -1;
-                    tickets_left = false;
-                }
-            }
-            if (ticket >= 0 && ld_acquire(a.task_ready + ticket) != 0) {
-                tail_work(a, ticket, wk);
-                ticket = -1;
-                have = true;
-                break;
-            }
-            if (!main_done) {
-                const unsigned long long w = next;
-                if (w < static_cast<unsigned long long>(a.n_main)) {
-                    next = atomicAdd(&a.ctl->grab, 1ull);
-                    have = main_work(a, sm, static_cast<long long>(w), sc, wk);
-                    t_idle = 0;
-                    continue;
-                }
-                main_done = true;
-            }
-            if (ld_volatile(&a.ctl->finalized) >= sm.n_valid) break;  // every sequence is final
-            if (t_idle == 0) {
-                t_idle = global_timer_ns();
-            } else if (global_timer_ns() - t_idle > kDrainWaitNs) {
-                atomicOr(&a.ctl->err, kErrWaitTimeout);
-                failed = true;
-                break;
-            }
-            __nanosleep(100);
-        }
-        if (!have) wk.kind = kEnd;
-        mbar_arrive(&sm.work_full[ws]);
-        if (!have || failed) return;
+        if (!main_done)  // work ring full: sleep until a slot frees (or ~1 us, to look at the ticket)
+            (void)mbar_try_wait_for(&sm.work_empty[k % kWork], (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u, 1000);
+        else
+            __nanosleep(200);
     }
+    // Stop the issuer: an end marker in the work ring (bounded wait for room).
+    const int ws = static_cast<int>(k % kWork);
+    if (!mbar_wait_ns(&sm.work_empty[ws], (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u, kWaitNs)) {
+        atomicOr(&a.ctl->err, kErrWaitTimeout);
+        return;
+    }
+    sm.work[ws].kind = kEnd;
+    mbar_arrive(&sm.work_full[ws]);
 }
 
 // =============================================================================
@@ -739,70 +844,94 @@ __device__ __forceinline__ int acquire_stage(SmemV& sm, long long n, int* err) {
     return stage;
 }
 
+// Stream sub-chunks [c0, c1) of one unit of work into the stage ring.
+template <typename Elem>
+__device__ bool issue_work(const VerifyArgs& a, SmemV& sm, const Work& wk, int c0, int c1, long long& n) {
+    constexpr int E = sizeof(Elem);
+    const bool main = wk.kind == kMain;
+    const int ck = main ? a.ck : a.ckt;
+    for (int c = c0; c < c1; ++c) {
+        const int e0 = c * ck;
+        const int nel = min(ck, a.vocab - e0);
+        const Piece pa = make_piece<E>(wk.row0, e0, nel);
+        Piece pb = {};
+        if (wk.kind == kTailRes) pb = make_piece<E>(wk.row1, e0, nel);
+        const int stage = acquire_stage(sm, n, &a.ctl->err);
+        if (stage < 0) return false;
+        Desc& d = sm.desc[stage];
+        d.kind = wk.kind;
+        d.flags = main ? ((c == wk.c0 ? kFirst : 0) | (c == wk.c1 - 1 ? kLast : 0)) : (c == wk.c1 - 1 ? kLast : 0);
+        d.seq = wk.seq;
+        d.slot = main ? wk.slot : c;
+        d.seg = wk.seg;
+        d.expect = wk.expect;
+        d.e0 = e0;
+        d.n = nel;
+        d.nvec = pa.bytes >> 4;
+        d.nsm0 = pa.nsm;
+        d.skip0 = pa.skip;
+        d.tail0 = pa.tail;
+        d.nsm1 = pb.nsm;
+        d.skip1 = pb.skip;
+        d.tail1 = pb.tail;
+        d.c2 = wk.c2;
+        d.mc0 = wk.mc0;
+        d.inv0 = wk.inv0;
+        d.mc1 = wk.mc1;
+        d.inv1 = wk.inv1;
+        const int bytes = pa.bytes + pb.bytes;
+        if (bytes > 0) {
+            mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(bytes));
+            if (pa.bytes > 0)
+                bulk_copy_g2s(sm.stage[stage], reinterpret_cast<const void*>(pa.lo),
+                              static_cast<uint32_t>(pa.bytes), &sm.full[stage]);
+            if (pb.bytes > 0)
+                bulk_copy_g2s(sm.stage[stage] + kHalf, reinterpret_cast<const void*>(pb.lo),
+                              static_cast<uint32_t>(pb.bytes), &sm.full[stage]);
+        } else {
+            mbar_arrive(&sm.full[stage]);
+        }
+        ++n;
+    }
+    return true;
+}
+
 template <typename Elem>
 __device__ void issuer(const VerifyArgs& a, SmemV& sm) {
-    constexpr int E = sizeof(Elem);
-    long long n = 0;
-    for (long long k = 0;; ++k) {
+    long long n = 0, kp = 0;
+    bool ok = true;
+    // Tail work waiting in the priority slot goes first, between any two
+    // stages; returns -1 on a timeout, 1 if it issued work, 0 otherwise.
+    auto priority = [&]() -> int {
+        if (!mbar_test(&sm.prio_full, static_cast<uint32_t>(kp) & 1u)) return 0;
+        const Work pw = sm.prio;
+        mbar_arrive(&sm.prio_empty);
+        ++kp;
+        return issue_work<Elem>(a, sm, pw, pw.c0, pw.c1, n) ? 1 : -1;
+    };
+    for (long long k = 0; ok; ++k) {
         const int ws = static_cast<int>(k % kWork);
         const uint32_t parity = static_cast<uint32_t>(k / kWork) & 1u;
-        if (!mbar_wait_ns(&sm.work_full[ws], parity, kDrainWaitNs + kWaitNs)) {
-            atomicOr(&a.ctl->err, kErrWaitTimeout);
-            break;
+        // Wait for the next main item, serving the priority slot meanwhile.
+        const uint64_t t0 = global_timer_ns();
+        bool got = false;
+        while (ok && !(got = mbar_test(&sm.work_full[ws], parity))) {
+            const int pr = priority();
+            ok = pr >= 0;
+            if (global_timer_ns() - t0 > kDrainWaitNs + kWaitNs) {
+                atomicOr(&a.ctl->err, kErrWaitTimeout);
+                ok = false;
+            }
+            if (pr == 0) __nanosleep(200);
         }
+        if (!got) break;
         const Work wk = sm.work[ws];
         mbar_arrive(&sm.work_empty[ws]);
         if (wk.kind == kEnd) break;
-        const bool main = wk.kind == kMain;
-        const int ck = main ? a.ck : a.ckt;
-        bool ok = true;
         for (int c = wk.c0; c < wk.c1 && ok; ++c) {
-            const int e0 = c * ck;
-            const int nel = min(ck, a.vocab - e0);
-            const Piece pa = make_piece<E>(wk.row0, e0, nel);
-            Piece pb = {};
-            if (wk.kind == kTailRes) pb = make_piece<E>(wk.row1, e0, nel);
-            const int stage = acquire_stage(sm, n, &a.ctl->err);
-            if (stage < 0) {
-                ok = false;
-                break;
-            }
-            Desc& d = sm.desc[stage];
-            d.kind = wk.kind;
-            d.flags = main ? ((c == wk.c0 ? kFirst : 0) | (c == wk.c1 - 1 ? kLast : 0)) : (c == wk.c1 - 1 ? kLast : 0);
-            d.seq = wk.seq;
-            d.slot = main ? wk.slot : c;
-            d.seg = wk.seg;
-            d.expect = wk.expect;
-            d.e0 = e0;
-            d.n = nel;
-            d.nvec = pa.bytes >> 4;
-            d.nsm0 = pa.nsm;
-            d.skip0 = pa.skip;
-            d.tail0 = pa.tail;
-            d.nsm1 = pb.nsm;
-            d.skip1 = pb.skip;
-            d.tail1 = pb.tail;
-            d.c2 = wk.c2;
-            d.mc0 = wk.mc0;
-            d.inv0 = wk.inv0;
-            d.mc1 = wk.mc1;
-            d.inv1 = wk.inv1;
-            const int bytes = pa.bytes + pb.bytes;
-            if (bytes > 0) {
-                mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(bytes));
-                if (pa.bytes > 0)
-                    bulk_copy_g2s(sm.stage[stage], reinterpret_cast<const void*>(pa.lo),
-                                  static_cast<uint32_t>(pa.bytes), &sm.full[stage]);
-                if (pb.bytes > 0)
-                    bulk_copy_g2s(sm.stage[stage] + kHalf, reinterpret_cast<const void*>(pb.lo),
-                                  static_cast<uint32_t>(pb.bytes), &sm.full[stage]);
-            } else {
-                mbar_arrive(&sm.full[stage]);
-            }
-            ++n;
+            ok = priority() >= 0;
+            if (ok) ok = issue_work<Elem>(a, sm, wk, c, c + 1, n);
         }
-        if (!ok) break;
     }
     const int stage = acquire_stage(sm, n, &a.ctl->err);
     if (stage >= 0) {
@@ -979,27 +1108,75 @@ __device__ __forceinline__ void main_stage(const VerifyArgs& a, SmemV& sm, int s
 // A tail stage: each consumer warp reduces its own contiguous slice of the
 // sub-chunk (about 1/8 of it), so the selection can later narrow a draw down
 // to one slice.
+// Residual weights of two ids from packed p and q logits: accumulates the
+// residual sum and the p sum (bit-identical to resid_w per id).
+__device__ __forceinline__ void resid_pair(float xp0, float xp1, float xq0, float xq1, uint64_t C2, uint64_t NMC0,
+                                           uint64_t INV0, uint64_t NMC1, uint64_t INV1, uint64_t& sw, uint64_t& sp) {
+    float a0, a1, b0, b1;
+    unpack_f2(fma_f2(pack_f2(xp0, xp1), C2, NMC0), a0, a1);
+    unpack_f2(fma_f2(pack_f2(xq0, xq1), C2, NMC1), b0, b1);
+    const uint64_t pv = mul_f2(pack_f2(ex2_approx(a0), ex2_approx(a1)), INV0);
+    const uint64_t qv = mul_f2(pack_f2(ex2_approx(b0), ex2_approx(b1)), INV1);
+    float d0, d1;
+    unpack_f2(fma_f2(qv, pack_f2(-1.0f, -1.0f), pv), d0, d1);  // pv - qv, one rounding
+    sw = add_f2(sw, pack_f2(fmaxf(0.0f, d0), fmaxf(0.0f, d1)));
+    sp = add_f2(sp, pv);
+}
+
+// A tail stage: each consumer warp reduces its own contiguous slice of the
+// sub-chunk (about 1/8 of it), so the selection can later narrow a draw down
+// to one slice.
 template <typename Elem>
 __device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int warp,
                                            int lane, long long& nrec) {
+    constexpr int E = sizeof(Elem);
+    constexpr int kVec = 16 / E;
     const unsigned char* s0 = sm.stage[stage];
     const unsigned char* s1 = s0 + kHalf;
-    const int spw = (d.n + kCW - 1) / kCW;
-    const int wb = min(d.n, warp * spw), we = min(d.n, wb + spw);
+    int wb, we;
+    tail_slice<E>(d.n, warp, wb, we);
     float2 part;
     if (d.kind == kTailRes) {
-        float sw = 0.0f, sp = 0.0f;
-#pragma unroll 4
-        for (int e = wb + lane; e < we; e += 32) {
+        uint64_t sw = 0, sp = 0;
+        int e_scalar = wb;
+        if (d.skip0 == 0 && d.skip1 == 0 && d.nsm0 == d.n && d.nsm1 == d.n) {
+            // Both pieces whole and aligned in shared memory: 16-byte vectors.
+            const uint4* p4 = reinterpret_cast<const uint4*>(s0);
+            const uint4* q4 = reinterpret_cast<const uint4*>(s1);
+            const int vb = wb / kVec, ve = we / kVec;
+            const uint64_t C2 = pack_f2(d.c2, d.c2);
+            const uint64_t NMC0 = pack_f2(-d.mc0, -d.mc0), INV0 = pack_f2(d.inv0, d.inv0);
+            const uint64_t NMC1 = pack_f2(-d.mc1, -d.mc1), INV1 = pack_f2(d.inv1, d.inv1);
+            for (int v = vb + lane; v < ve; v += 32) {
+                const uint4 A = p4[v], B = q4[v];
+                if constexpr (E == 2) {
+                    resid_pair(bf16lo(A.x), bf16hi(A.x), bf16lo(B.x), bf16hi(B.x), C2, NMC0, INV0, NMC1, INV1, sw, sp);
+                    resid_pair(bf16lo(A.y), bf16hi(A.y), bf16lo(B.y), bf16hi(B.y), C2, NMC0, INV0, NMC1, INV1, sw, sp);
+                    resid_pair(bf16lo(A.z), bf16hi(A.z), bf16lo(B.z), bf16hi(B.z), C2, NMC0, INV0, NMC1, INV1, sw, sp);
+                    resid_pair(bf16lo(A.w), bf16hi(A.w), bf16lo(B.w), bf16hi(B.w), C2, NMC0, INV0, NMC1, INV1, sw, sp);
+                } else {
+                    resid_pair(__uint_as_float(A.x), __uint_as_float(A.y), __uint_as_float(B.x), __uint_as_float(B.y),
+                               C2, NMC0, INV0, NMC1, INV1, sw, sp);
+                    resid_pair(__uint_as_float(A.z), __uint_as_float(A.w), __uint_as_float(B.z), __uint_as_float(B.w),
+                               C2, NMC0, INV0, NMC1, INV1, sw, sp);
+                }
+            }
+            e_scalar = ve * kVec;
+        }
+        float sws = 0.0f, sps = 0.0f;
+        for (int e = e_scalar + lane; e < we; e += 32) {
             const float xp = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
             const float xq = piece_elem<Elem>(s1, d.nsm1, d.skip1, d.tail1, e);
             float pv;
-            sw += resid_w(xp, xq, d.c2, d.mc0, d.inv0, d.mc1, d.inv1, pv);
-            sp += pv;
+            sws += resid_w(xp, xq, d.c2, d.mc0, d.inv0, d.mc1, d.inv1, pv);
+            sps += pv;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        part = make_float2(warp_sum(sw), warp_sum(sp));
+        float w0, w1, p0, p1;
+        unpack_f2(sw, w0, w1);
+        unpack_f2(sp, p0, p1);
+        part = make_float2(warp_sum((w0 + w1) + sws), warp_sum((p0 + p1) + sps));
     } else if (d.kind == kTailSoft) {
         float mt = -INFINITY;
         for (int e = wb + lane; e < we; e += 32) mt = fmaxf(mt, piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e));
@@ -1080,12 +1257,15 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
             mbar_init(&sm.work_full[s], 1);
             mbar_init(&sm.work_empty[s], 1);
         }
+        mbar_init(&sm.prio_full, 1);
+        mbar_init(&sm.prio_empty, 1);
         for (int s = 0; s < kJobs; ++s) {
             mbar_init(&sm.job_full[s], 1);
             mbar_init(&sm.job_empty[s], 1);
         }
         fence_mbarrier_init();
         sm.n_valid = 0;
+        sm.job_take = 0;
     }
     // The scheduler's first main item, requested while the prologue runs.
     unsigned long long first = 0;
@@ -1122,8 +1302,8 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
         if (lane == 0) scheduler(a, sm, first);
     } else if (warp == kBookWarp) {
         bookkeeper(a, sm, lane);
-    } else if (warp == kFinWarp) {
-        finisher<Elem>(a, sm, lane);
+    } else if (warp >= kFinWarp) {
+        finisher<Elem>(a, sm, warp - kFinWarp, lane);
     } else {
         // This CTA's share of the sequences that are invalid as laid out.
         for (long long i = blockIdx.x + static_cast<long long>(warp) * gridDim.x; i < a.num_seqs;
