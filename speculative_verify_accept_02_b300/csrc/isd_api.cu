@@ -30,7 +30,7 @@ struct VerifyPlan {
 };
 
 constexpr int kSubChunksPerSegment = 8;  // one main item: 8 x 16 KB
-constexpr int kTailSubChunksPerTask = 4;
+constexpr int kTailSubChunksPerTask = 2;
 
 VerifyPlan verify_plan(int vocab, int esz) {
     VerifyPlan pl;

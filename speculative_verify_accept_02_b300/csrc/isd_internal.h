@@ -105,9 +105,9 @@ struct alignas(16) SeqTail {
     int a;            // accept length
     int prow, qrow;   // tail rows in p and in q
     float c2;         // log2(e) / T
-    float mc0, inv0;  // p_j: (max logit) * c2 and 1 / sum of exp2(x c2 - mc0)
-    float mc1, inv1;  // q_j: the same
-    float pad[3];
+    float nz0;        // p_j: log2 of its normaliser, p_j(v) = exp2(x_v c2 - nz0)
+    float nz1;        // q_j: the same
+    float pad[5];
 };
 
 struct VerifyArgs {

@@ -64,6 +64,7 @@ constexpr int kSmemSeqs = 512;                  // batches up to this size keep 
 constexpr int kSliceMax = 512;                  // ids in one tail slice (tail sub-chunk / 8 warps)
 static_assert(kHalf / 2 <= kSliceMax * kCW, "a tail sub-chunk of bf16 ids splits into slices of at most kSliceMax");
 static_assert(kVecPT * 16 * kCT == kStageBytes, "stage split");
+static_assert(kHalf / kCW <= 64 * 16, "a tail slice is at most two 16-byte vectors per lane");
 
 enum : int { kEnd = 0, kMain = 1 };  // descriptor / record kinds besides the TailMode values
 enum : int { kFirst = 1, kLast = 2 };
@@ -81,7 +82,7 @@ struct Desc {
     int nsm0, skip0, nsm1, skip1;
     const char* tail0;  // global address of the first element not in shared memory
     const char* tail1;
-    float c2, mc0, inv0, mc1, inv1;
+    float c2, nz0, nz1;
 };
 
 // flags of a main record: which partial the warps hand in.
@@ -97,7 +98,7 @@ struct Rec {
 struct Work {
     int kind;
     int seq, slot, seg, expect, c0, c1;
-    float c2, mc0, inv0, mc1, inv1;
+    float c2, nz0, nz1;
     const char* row0;
     const char* row1;
 };
@@ -152,10 +153,11 @@ __device__ __forceinline__ float piece_elem(const unsigned char* st, int nsm, in
 __device__ __forceinline__ float soft_w(float x, float c2, float mc) { return ex2_approx(__fmaf_rn(x, c2, -mc)); }
 
 // Residual weight max(0, p - q) of one id, and p itself.
-__device__ __forceinline__ float resid_w(float xp, float xq, float c2, float mc0, float inv0, float mc1,
-                                         float inv1, float& pv) {
-    pv = __fmul_rn(soft_w(xp, c2, mc0), inv0);
-    const float qv = __fmul_rn(soft_w(xq, c2, mc1), inv1);
+// nz0, nz1: log2 of the normalisers of p and q in the exp2 domain, so that
+// p(v) = exp2(x_v c2 - nz0).
+__device__ __forceinline__ float resid_w(float xp, float xq, float c2, float nz0, float nz1, float& pv) {
+    pv = soft_w(xp, c2, nz0);
+    const float qv = soft_w(xq, c2, nz1);
     return fmaxf(0.0f, __fsub_rn(pv, qv));
 }
 
@@ -363,10 +365,8 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         t.qrow = s.start + na;
         t.c2 = c2;
         if (na < L) {
-            t.mc0 = mc0;
-            t.inv0 = 1.0f / sp0;
-            t.mc1 = mc1;
-            t.inv1 = 1.0f / sq0;
+            t.nz0 = __fadd_rn(mc0, log2f(sp0));
+            t.nz1 = __fadd_rn(mc1, log2f(sq0));
         }
         a.tails[i] = t;
         a.seq_count[i] = 0;
@@ -401,10 +401,8 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
     t.prow = __shfl_sync(0xffffffffu, tv.z, 0);
     t.qrow = __shfl_sync(0xffffffffu, tv.w, 0);
     t.c2 = __int_as_float(__shfl_sync(0xffffffffu, tv.x, 1));
-    t.mc0 = __int_as_float(__shfl_sync(0xffffffffu, tv.y, 1));
-    t.inv0 = __int_as_float(__shfl_sync(0xffffffffu, tv.z, 1));
-    t.mc1 = __int_as_float(__shfl_sync(0xffffffffu, tv.w, 1));
-    t.inv1 = __int_as_float(__shfl_sync(0xffffffffu, tv.x, 2));
+    t.nz0 = __int_as_float(__shfl_sync(0xffffffffu, tv.y, 1));
+    t.nz1 = __int_as_float(__shfl_sync(0xffffffffu, tv.z, 1));
     __syncwarp();
     const SeqInfo s = seq_lookup(a, sm, i);
     const int out_slot = s.start + i + t.a;
@@ -490,7 +488,7 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
                 wv[k] = soft_w(xp, t.c2, MC);
             } else {
                 float pv;
-                const float rw = resid_w(xp, load_elem<Elem>(qrow + e * E), t.c2, t.mc0, t.inv0, t.mc1, t.inv1, pv);
+                const float rw = resid_w(xp, load_elem<Elem>(qrow + e * E), t.c2, t.nz0, t.nz1, pv);
                 wv[k] = fallback ? pv : rw;
             }
         }
@@ -713,7 +711,7 @@ __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
     const int2 task = __ldcg(a.tasks + slot);
     const int i = task.x, y = task.y;
     const int4* tw = reinterpret_cast<const int4*>(a.tails + i);
-    const int4 w0 = __ldcg(tw), w1 = __ldcg(tw + 1), w2 = __ldcg(tw + 2);
+    const int4 w0 = __ldcg(tw), w1 = __ldcg(tw + 1);
     wk.kind = w0.x;
     wk.seq = i;
     wk.slot = 0;
@@ -722,10 +720,8 @@ __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
     wk.c0 = y * a.tpt;
     wk.c1 = min(wk.c0 + a.tpt, a.nt);
     wk.c2 = __int_as_float(w1.x);
-    wk.mc0 = __int_as_float(w1.y);
-    wk.inv0 = __int_as_float(w1.z);
-    wk.mc1 = __int_as_float(w1.w);
-    wk.inv1 = __int_as_float(w2.x);
+    wk.nz0 = __int_as_float(w1.y);
+    wk.nz1 = __int_as_float(w1.z);
     wk.row0 = a.p + static_cast<int64_t>(w0.z) * a.ldp_bytes;
     wk.row1 = a.q + static_cast<int64_t>(w0.w) * a.ldq_bytes;
 }
@@ -875,10 +871,8 @@ __device__ bool issue_work(const VerifyArgs& a, SmemV& sm, const Work& wk, int c
         d.skip1 = pb.skip;
         d.tail1 = pb.tail;
         d.c2 = wk.c2;
-        d.mc0 = wk.mc0;
-        d.inv0 = wk.inv0;
-        d.mc1 = wk.mc1;
-        d.inv1 = wk.inv1;
+        d.nz0 = wk.nz0;
+        d.nz1 = wk.nz1;
         const int bytes = pa.bytes + pb.bytes;
         if (bytes > 0) {
             mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(bytes));
@@ -1105,99 +1099,186 @@ __device__ __forceinline__ void main_stage(const VerifyArgs& a, SmemV& sm, int s
     }
 }
 
-// A tail stage: each consumer warp reduces its own contiguous slice of the
-// sub-chunk (about 1/8 of it), so the selection can later narrow a draw down
-// to one slice.
 // Residual weights of two ids from packed p and q logits: accumulates the
 // residual sum and the p sum (bit-identical to resid_w per id).
-__device__ __forceinline__ void resid_pair(float xp0, float xp1, float xq0, float xq1, uint64_t C2, uint64_t NMC0,
-                                           uint64_t INV0, uint64_t NMC1, uint64_t INV1, uint64_t& sw, uint64_t& sp) {
+__device__ __forceinline__ void resid_pair(float xp0, float xp1, float xq0, float xq1, uint64_t C2, uint64_t NZ0,
+                                           uint64_t NZ1, uint64_t& sw, uint64_t& sp) {
     float a0, a1, b0, b1;
-    unpack_f2(fma_f2(pack_f2(xp0, xp1), C2, NMC0), a0, a1);
-    unpack_f2(fma_f2(pack_f2(xq0, xq1), C2, NMC1), b0, b1);
-    const uint64_t pv = mul_f2(pack_f2(ex2_approx(a0), ex2_approx(a1)), INV0);
-    const uint64_t qv = mul_f2(pack_f2(ex2_approx(b0), ex2_approx(b1)), INV1);
+    unpack_f2(fma_f2(pack_f2(xp0, xp1), C2, NZ0), a0, a1);
+    unpack_f2(fma_f2(pack_f2(xq0, xq1), C2, NZ1), b0, b1);
+    const uint64_t pv = pack_f2(ex2_approx(a0), ex2_approx(a1));
+    const uint64_t qv = pack_f2(ex2_approx(b0), ex2_approx(b1));
     float d0, d1;
     unpack_f2(fma_f2(qv, pack_f2(-1.0f, -1.0f), pv), d0, d1);  // pv - qv, one rounding
     sw = add_f2(sw, pack_f2(fmaxf(0.0f, d0), fmaxf(0.0f, d1)));
     sp = add_f2(sp, pv);
 }
 
+// Residual weights of one 16-byte vector of p logits and the matching vector
+// of q logits.
+template <int E>
+__device__ __forceinline__ void resid_vec(const uint4& A, const uint4& B, uint64_t C2, uint64_t NZ0, uint64_t NZ1,
+                                          uint64_t& sw, uint64_t& sp) {
+    if constexpr (E == 2) {
+        resid_pair(bf16lo(A.x), bf16hi(A.x), bf16lo(B.x), bf16hi(B.x), C2, NZ0, NZ1, sw, sp);
+        resid_pair(bf16lo(A.y), bf16hi(A.y), bf16lo(B.y), bf16hi(B.y), C2, NZ0, NZ1, sw, sp);
+        resid_pair(bf16lo(A.z), bf16hi(A.z), bf16lo(B.z), bf16hi(B.z), C2, NZ0, NZ1, sw, sp);
+        resid_pair(bf16lo(A.w), bf16hi(A.w), bf16lo(B.w), bf16hi(B.w), C2, NZ0, NZ1, sw, sp);
+    } else {
+        resid_pair(__uint_as_float(A.x), __uint_as_float(A.y), __uint_as_float(B.x), __uint_as_float(B.y), C2, NZ0,
+                   NZ1, sw, sp);
+        resid_pair(__uint_as_float(A.z), __uint_as_float(A.w), __uint_as_float(B.z), __uint_as_float(B.w), C2, NZ0,
+                   NZ1, sw, sp);
+    }
+}
+
+// Element j (0 .. 16/E - 1) of a 16-byte vector, as float.
+template <int E>
+__device__ __forceinline__ float vec_elem(const uint4& v, int j) {
+    const uint32_t w = j < (8 / E) ? (j < (4 / E) ? v.x : v.y) : (j < (12 / E) ? v.z : v.w);
+    if constexpr (E == 2) return (j & 1) ? bf16hi(w) : bf16lo(w);
+    else return __uint_as_float(w);
+}
+
+// Largest element of a 16-byte vector.
+template <int E>
+__device__ __forceinline__ float vec_max(const uint4& v) {
+    if constexpr (E == 2) {
+        const uint32_t m = hmax2_bf16(hmax2_bf16(v.x, v.y), hmax2_bf16(v.z, v.w));
+        return fmaxf(bf16lo(m), bf16hi(m));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+}
+
+// Sum of exp2(x c2 - mc) over a 16-byte vector, added to a packed accumulator.
+template <int E>
+__device__ __forceinline__ void soft_vec(const uint4& v, uint64_t C2, uint64_t NMC, uint64_t& acc) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; j += (E == 2 ? 1 : 2)) {
+        float y0, y1;
+        if constexpr (E == 2)
+            unpack_f2(fma_f2(pack_f2(bf16lo(w[j]), bf16hi(w[j])), C2, NMC), y0, y1);
+        else
+            unpack_f2(fma_f2(pack_f2(__uint_as_float(w[j]), __uint_as_float(w[j + 1])), C2, NMC), y0, y1);
+        acc = add_f2(acc, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+    }
+}
+
 // A tail stage: each consumer warp reduces its own contiguous slice of the
 // sub-chunk (about 1/8 of it), so the selection can later narrow a draw down
-// to one slice.
+// to one slice.  A slice holds at most 64 vectors: every lane loads its (at
+// most two) vectors of each row up front, then reduces them from registers.
 template <typename Elem>
 __device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int warp,
                                            int lane, long long& nrec) {
     constexpr int E = sizeof(Elem);
     constexpr int kVec = 16 / E;
+    constexpr uint32_t kNeg = E == 2 ? 0xff80ff80u : 0xff800000u;  // -inf pattern
     const unsigned char* s0 = sm.stage[stage];
     const unsigned char* s1 = s0 + kHalf;
     int wb, we;
     tail_slice<E>(d.n, warp, wb, we);
+    const bool vec0 = d.skip0 == 0 && d.nsm0 == d.n;  // piece whole and aligned in shared memory
+    const bool vec = vec0 && (d.kind != kTailRes || (d.skip1 == 0 && d.nsm1 == d.n));
+    // The lane's vectors v, v + 32 of the slice, -inf where past its end.
+    const int vb = wb / kVec, ve = we / kVec;
+    const int v0 = vb + lane, v1 = v0 + 32;
+    const uint4 neg = make_uint4(kNeg, kNeg, kNeg, kNeg);
+    uint4 A0 = neg, A1 = neg, B0 = neg, B1 = neg;
+    if (vec) {
+        const uint4* p4 = reinterpret_cast<const uint4*>(s0);
+        if (v0 < ve) A0 = p4[v0];
+        if (v1 < ve) A1 = p4[v1];
+        if (d.kind == kTailRes) {
+            const uint4* q4 = reinterpret_cast<const uint4*>(s1);
+            if (v0 < ve) B0 = q4[v0];
+            if (v1 < ve) B1 = q4[v1];
+        }
+    }
     float2 part;
     if (d.kind == kTailRes) {
-        uint64_t sw = 0, sp = 0;
-        int e_scalar = wb;
-        if (d.skip0 == 0 && d.skip1 == 0 && d.nsm0 == d.n && d.nsm1 == d.n) {
-            // Both pieces whole and aligned in shared memory: 16-byte vectors.
-            const uint4* p4 = reinterpret_cast<const uint4*>(s0);
-            const uint4* q4 = reinterpret_cast<const uint4*>(s1);
-            const int vb = wb / kVec, ve = we / kVec;
-            const uint64_t C2 = pack_f2(d.c2, d.c2);
-            const uint64_t NMC0 = pack_f2(-d.mc0, -d.mc0), INV0 = pack_f2(d.inv0, d.inv0);
-            const uint64_t NMC1 = pack_f2(-d.mc1, -d.mc1), INV1 = pack_f2(d.inv1, d.inv1);
-            for (int v = vb + lane; v < ve; v += 32) {
-                const uint4 A = p4[v], B = q4[v];
-                if constexpr (E == 2) {
-                    resid_pair(bf16lo(A.x), bf16hi(A.x), bf16lo(B.x), bf16hi(B.x), C2, NMC0, INV0, NMC1, INV1, sw, sp);
-                    resid_pair(bf16lo(A.y), bf16hi(A.y), bf16lo(B.y), bf16hi(B.y), C2, NMC0, INV0, NMC1, INV1, sw, sp);
-                    resid_pair(bf16lo(A.z), bf16hi(A.z), bf16lo(B.z), bf16hi(B.z), C2, NMC0, INV0, NMC1, INV1, sw, sp);
-                    resid_pair(bf16lo(A.w), bf16hi(A.w), bf16lo(B.w), bf16hi(B.w), C2, NMC0, INV0, NMC1, INV1, sw, sp);
-                } else {
-                    resid_pair(__uint_as_float(A.x), __uint_as_float(A.y), __uint_as_float(B.x), __uint_as_float(B.y),
-                               C2, NMC0, INV0, NMC1, INV1, sw, sp);
-                    resid_pair(__uint_as_float(A.z), __uint_as_float(A.w), __uint_as_float(B.z), __uint_as_float(B.w),
-                               C2, NMC0, INV0, NMC1, INV1, sw, sp);
-                }
-            }
-            e_scalar = ve * kVec;
-        }
         float sws = 0.0f, sps = 0.0f;
-        for (int e = e_scalar + lane; e < we; e += 32) {
-            const float xp = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
-            const float xq = piece_elem<Elem>(s1, d.nsm1, d.skip1, d.tail1, e);
-            float pv;
-            sws += resid_w(xp, xq, d.c2, d.mc0, d.inv0, d.mc1, d.inv1, pv);
-            sps += pv;
+        if (vec) {
+            const uint64_t C2 = pack_f2(d.c2, d.c2);
+            const uint64_t NZ0 = pack_f2(-d.nz0, -d.nz0), NZ1 = pack_f2(-d.nz1, -d.nz1);
+            uint64_t sw0 = 0, sp0 = 0, sw1 = 0, sp1 = 0;
+            resid_vec<E>(A0, B0, C2, NZ0, NZ1, sw0, sp0);
+            resid_vec<E>(A1, B1, C2, NZ0, NZ1, sw1, sp1);
+            float w0, w1, w2, w3, p0, p1, p2, p3;
+            unpack_f2(sw0, w0, w1);
+            unpack_f2(sw1, w2, w3);
+            unpack_f2(sp0, p0, p1);
+            unpack_f2(sp1, p2, p3);
+            sws = (w0 + w1) + (w2 + w3);
+            sps = (p0 + p1) + (p2 + p3);
+        } else {
+            for (int e = wb + lane; e < we; e += 32) {
+                const float xp = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
+                const float xq = piece_elem<Elem>(s1, d.nsm1, d.skip1, d.tail1, e);
+                float pv;
+                sws += resid_w(xp, xq, d.c2, d.nz0, d.nz1, pv);
+                sps += pv;
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        float w0, w1, p0, p1;
-        unpack_f2(sw, w0, w1);
-        unpack_f2(sp, p0, p1);
-        part = make_float2(warp_sum((w0 + w1) + sws), warp_sum((p0 + p1) + sps));
+        part = make_float2(warp_sum(sws), warp_sum(sps));
     } else if (d.kind == kTailSoft) {
-        float mt = -INFINITY;
-        for (int e = wb + lane; e < we; e += 32) mt = fmaxf(mt, piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e));
-        const float mct = mt * d.c2;
-        float st = 0.0f;
-        if (mt != -INFINITY)
-            for (int e = wb + lane; e < we; e += 32)
-                st += soft_w(piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e), d.c2, mct);
+        float mt = -INFINITY, st = 0.0f;
+        if (vec) {
+            mt = fmaxf(vec_max<E>(A0), vec_max<E>(A1));
+            if (mt != -INFINITY) {
+                const float mct = mt * d.c2;
+                const uint64_t C2 = pack_f2(d.c2, d.c2), NMC = pack_f2(-mct, -mct);
+                uint64_t acc0 = 0, acc1 = 0;
+                soft_vec<E>(A0, C2, NMC, acc0);
+                soft_vec<E>(A1, C2, NMC, acc1);
+                float a0, a1, a2, a3;
+                unpack_f2(acc0, a0, a1);
+                unpack_f2(acc1, a2, a3);
+                st = (a0 + a1) + (a2 + a3);
+            }
+        } else {
+            for (int e = wb + lane; e < we; e += 32) mt = fmaxf(mt, piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e));
+            if (mt != -INFINITY)
+                for (int e = wb + lane; e < we; e += 32)
+                    st += soft_w(piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e), d.c2, mt * d.c2);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        float M = mt == -INFINITY ? -INFINITY : mct, S = st;
+        float M = mt == -INFINITY ? -INFINITY : mt * d.c2, S = st;
         warp_merge_mc(M, S);
         part = make_float2(M, S);
-    } else {  // kTailArg
+    } else {  // kTailArg: the lane's first maximum in id order
         float mt = -INFINITY;
         int it = INT_MAX;
-        for (int e = wb + lane; e < we; e += 32) {
-            const float x = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
-            if (x > mt) {
-                mt = x;
-                it = d.e0 + e;
+        if (vec) {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float x = vec_elem<E>(A0, j);
+                if (x > mt) {
+                    mt = x;
+                    it = d.e0 + v0 * kVec + j;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float x = vec_elem<E>(A1, j);
+                if (x > mt) {
+                    mt = x;
+                    it = d.e0 + v1 * kVec + j;
+                }
+            }
+        } else {
+            for (int e = wb + lane; e < we; e += 32) {
+                const float x = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
+                if (x > mt) {
+                    mt = x;
+                    it = d.e0 + e;
+                }
             }
         }
         __syncwarp();
