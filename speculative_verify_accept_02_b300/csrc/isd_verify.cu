@@ -21,7 +21,7 @@
 //
 // Warp roles of a CTA:
 //   scheduler   (one thread) takes work: the next main item from the global
-//               counter into a 4-entry work ring, a published tail task into
+//               counter into a 2-entry work ring, a published tail task into
 //               a priority slot; it absorbs every global memory round trip;
 //   issuer      (one thread) streams the scheduled sub-chunks into a 4-stage
 //               shared-memory ring with 1-D bulk copies, serving the priority
@@ -39,6 +39,7 @@
 // The grid exits once every sequence is final; its last CTA re-zeroes the
 // control block for the next call.  Every wait is bounded by the global timer.
 #include <climits>
+#include <type_traits>
 
 #include "isd_device.cuh"
 #include "isd_internal.h"
@@ -56,7 +57,7 @@ constexpr int kFinishers = 2;
 constexpr int kThreadsV = kCT + 32 * (3 + kFinishers);  // + issuer, bookkeeper, scheduler, finishers
 constexpr int kStagesV = 4;
 constexpr int kJobs = 16;                 // job ring between bookkeeper and finisher
-constexpr int kWork = 4;                  // work ring between scheduler and issuer
+constexpr int kWork = 2;                  // work ring between scheduler and issuer
 constexpr int kRecs = 8;                  // record ring between consumers and bookkeeper
 constexpr int kVecPT = kStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
 constexpr int kHalf = kStageBytes / 2;          // tail stages: [p piece | q piece]
@@ -64,6 +65,7 @@ constexpr int kSmemSeqs = 512;                  // batches up to this size keep 
 constexpr int kSliceMax = 512;                  // ids in one tail slice (tail sub-chunk / 8 warps)
 static_assert(kHalf / 2 <= kSliceMax * kCW, "a tail sub-chunk of bf16 ids splits into slices of at most kSliceMax");
 static_assert(kVecPT * 16 * kCT == kStageBytes, "stage split");
+static_assert(kHalf / kCW <= kSliceMax * 2, "a slice fits its staging buffer");
 static_assert(kHalf / kCW <= 64 * 16, "a tail slice is at most two 16-byte vectors per lane");
 
 enum : int { kEnd = 0, kMain = 1 };  // descriptor / record kinds besides the TailMode values
@@ -122,7 +124,8 @@ struct SmemV {
     uint64_t job_full[kJobs];
     uint64_t job_empty[kJobs];
     Job job[kJobs];
-    float2 tsel[kFinishers][kMaxTailChunks * kCW];  // each finisher's copy of one sequence's slice partials
+    alignas(16) float2 tsel[kFinishers][kMaxTailChunks * kCW];  // each finisher's copy of one sequence's slice partials
+    alignas(16) unsigned char sslice[kFinishers][2][kSliceMax * 2];  // each finisher's chosen slice of p and q
     int job_take;
     Desc desc[kStagesV];
     Work work[kWork];
@@ -140,6 +143,14 @@ __device__ __forceinline__ float load_elem(const void* p) {
         return __uint_as_float(static_cast<uint32_t>(*static_cast<const uint16_t*>(p)) << 16);
     else
         return *static_cast<const float*>(p);
+}
+
+// Element j (0 .. 16/E - 1) of a 16-byte vector, as float.
+template <int E>
+__device__ __forceinline__ float vec_elem(const uint4& v, int j) {
+    const uint32_t w = j < (8 / E) ? (j < (4 / E) ? v.x : v.y) : (j < (12 / E) ? v.z : v.w);
+    if constexpr (E == 2) return (j & 1) ? bf16hi(w) : bf16lo(w);
+    else return __uint_as_float(w);
 }
 
 // Element e of a staged piece: shared memory first, then the unaligned tail.
@@ -392,9 +403,11 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
     const int4* tw = reinterpret_cast<const int4*>(a.tails + i);
     int4 tv = make_int4(0, 0, 0, 0);
     if (lane < 3) tv = __ldcg(tw + lane);
-    const int U = a.nt * kCW;
-    const float2* tp = a.tpart + static_cast<size_t>(i) * U;
-    for (int u = lane; u < U; u += 32) sm.tsel[fi][u] = __ldcg(tp + u);
+    const int U = a.nt * kCW;  // even: 16-byte pairs of partials
+    const float4* tp = reinterpret_cast<const float4*>(a.tpart + static_cast<size_t>(i) * U);
+    float4* ts = reinterpret_cast<float4*>(sm.tsel[fi]);
+    for (int u = lane; u < U / 2; u += 32) cp_async16(ts + u, tp + u);
+    cp_async_wait_all();
     SeqTail t;
     t.mode = __shfl_sync(0xffffffffu, tv.x, 0);
     t.a = __shfl_sync(0xffffffffu, tv.y, 0);
@@ -418,50 +431,65 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
         }
         return;
     }
-    // Slice weights in one scale, the target u * total, and its slice.
-    float MC = -INFINITY;
-    if (t.mode == kTailSoft)
-        for (int u = lane; u < U; u += 32) MC = fmaxf(MC, sm.tsel[fi][u].x);
-    MC = warp_max(MC);
-    bool fallback = false;
-    if (t.mode == kTailRes) {
-        float W = 0.0f;
-        for (int u = lane; u < U; u += 32) W += sm.tsel[fi][u].x;
-        fallback = !(warp_sum(W) > 0.0f);  // residual rounded to zero: draw from p_j
+    // Slice weights in one scale, the target u * total, and its slice.  Lane
+    // l owns the consecutive slices [l * ub, (l + 1) * ub): the lanes reduce
+    // their blocks locally and meet in one scan, so the pass costs a handful
+    // of shuffles instead of a few per 32 slices.
+    const int ub = (U + 31) / 32;
+    const int u_lo = min(U, lane * ub), u_hi = min(U, u_lo + ub);
+    float MC = -INFINITY, W = 0.0f;
+    for (int u = u_lo; u < u_hi; ++u) {
+        const float x = sm.tsel[fi][u].x;
+        MC = fmaxf(MC, x);
+        W += x;
     }
+    bool fallback = false;
+    if (t.mode == kTailSoft) MC = warp_max(MC);
+    else fallback = !(warp_sum(W) > 0.0f);  // residual rounded to zero: draw from p_j
     auto slice_w = [&](int u) -> float {
-        if (u >= U) return 0.0f;
         const float2 v = sm.tsel[fi][u];
         if (t.mode == kTailSoft) return v.x == -INFINITY ? 0.0f : v.y * ex2_approx(v.x - MC);
         return fallback ? v.y : v.x;
     };
     const float rnd = t.mode == kTailSoft ? decision_uniform(a.seed, a.offset, i, s.len + 1, kTagBonus)
                                           : decision_uniform(a.seed, a.offset, i, t.a + 1, kTagCorrect);
-    float total = 0.0f;
-    for (int u0 = 0; u0 < U; u0 += 32) total += warp_sum(slice_w(u0 + lane));
-    const float target = rnd * total;
-    int chosen = -1, last_pos = -1;
-    float tloc = INFINITY, carry = 0.0f;
-    for (int u0 = 0; u0 < U && chosen < 0; u0 += 32) {
-        const float w = slice_w(u0 + lane);
-        float incl = w;
+    float own = 0.0f;
+    int lpos = -1;  // the lane's last slice with positive weight
+    for (int u = u_lo; u < u_hi; ++u) {
+        const float w = slice_w(u);
+        own += w;
+        if (w > 0.0f) lpos = u;
+    }
+    float incl = own;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const float target = rnd * __shfl_sync(0xffffffffu, incl, 31);
+    const unsigned hit = __ballot_sync(0xffffffffu, u_hi > u_lo && incl > target);
+    int chosen = -1;
+    float tloc = INFINITY;
+    if (hit) {
+        const int owner = __ffs(hit) - 1;
+        if (lane == owner) {  // in-order scan of the owner's block
+            float cum = incl - own;
+            for (int u = u_lo; u < u_hi; ++u) {
+                const float w = slice_w(u);
+                if (cum + w > target) {
+                    chosen = u;
+                    tloc = target - cum;
+                    break;
+                }
+                cum += w;
+            }
+            if (chosen < 0) chosen = lpos;  // rounding inside the block: its last positive slice
         }
-        incl += carry;
-        const unsigned hit = __ballot_sync(0xffffffffu, u0 + lane < U && incl > target);
-        const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
-        if (pos) last_pos = u0 + 31 - __clz(pos);
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            chosen = u0 + l;
-            tloc = target - (__shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, w, l));
-        }
-        carry = __shfl_sync(0xffffffffu, incl, 31);
+        chosen = __shfl_sync(0xffffffffu, chosen, owner);
+        tloc = __shfl_sync(0xffffffffu, tloc, owner);
     }
     if (chosen < 0) {  // rounding left the target past the last weight
+        const int last_pos = warp_max_int(lpos);
         chosen = last_pos >= 0 ? last_pos : 0;
         tloc = INFINITY;
     }
@@ -474,46 +502,90 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
     const int len = se - sb;
     const char* prow = a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
     const char* qrow = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes;
-    const int q = (len + 31) / 32;  // at most kSliceMax / 32 ids per lane
+    constexpr int kVec = 16 / E;
+    constexpr int kPer = 2 * kVec;  // ids per lane: at most two 16-byte vectors
+    static_assert(kPer * 32 * E == kSliceMax * 2, "a slice fills at most two vectors per lane");
+    const int q = ((len + 31) / 32 + kVec - 1) / kVec * kVec;  // whole vectors per lane
     const int b = lane * q;
     const int cnt = max(0, min(q, len - b));
-    float wv[kSliceMax / 32];
+    // Stage the slice's logits in shared memory with every load in flight at
+    // once: 16-byte copies where both rows allow them, then the elements
+    // left (all of them for rows that are not 16-byte aligned).
+    const bool res = t.mode != kTailSoft;
+    unsigned char* sp = sm.sslice[fi][0];
+    unsigned char* sq = sm.sslice[fi][1];
+    const char* gp = prow + static_cast<size_t>(lo) * E;
+    const char* gq = qrow + static_cast<size_t>(lo) * E;
+    const bool v16 = (reinterpret_cast<uintptr_t>(gp) & 15u) == 0 && (!res || (reinterpret_cast<uintptr_t>(gq) & 15u) == 0);
+    const int nv16 = v16 ? (len * E) >> 4 : 0;
+    for (int v = lane; v < nv16; v += 32) {
+        cp_async16(sp + 16 * v, gp + 16 * v);
+        if (res) cp_async16(sq + 16 * v, gq + 16 * v);
+    }
+    using Raw = typename std::conditional<E == 2, uint16_t, uint32_t>::type;
+    for (int e0 = nv16 * (16 / E); e0 < len; e0 += 4 * 32) {
+        Raw rp[4], rq[4];
 #pragma unroll
-    for (int k = 0; k < kSliceMax / 32; ++k) {
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + lane + 32 * j;
+            rp[j] = e < len ? reinterpret_cast<const Raw*>(gp)[e] : Raw(0);
+            rq[j] = (res && e < len) ? reinterpret_cast<const Raw*>(gq)[e] : Raw(0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + lane + 32 * j;
+            if (e < len) {
+                reinterpret_cast<Raw*>(sp)[e] = rp[j];
+                if (res) reinterpret_cast<Raw*>(sq)[e] = rq[j];
+            }
+        }
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    const uint4* sp4 = reinterpret_cast<const uint4*>(sp) + b / kVec;
+    const uint4* sq4 = reinterpret_cast<const uint4*>(sq) + b / kVec;
+    uint4 P[2], Q[2];
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+        P[v] = v * kVec < cnt ? sp4[v] : make_uint4(0, 0, 0, 0);
+        Q[v] = (res && v * kVec < cnt) ? sq4[v] : make_uint4(0, 0, 0, 0);
+    }
+    float wv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
         wv[k] = 0.0f;
         if (k < cnt) {
-            const size_t e = static_cast<size_t>(lo + b + k);
-            const float xp = load_elem<Elem>(prow + e * E);
-            if (t.mode == kTailSoft) {
+            const float xp = vec_elem<E>(P[k / kVec], k % kVec);
+            if (!res) {
                 wv[k] = soft_w(xp, t.c2, MC);
             } else {
                 float pv;
-                const float rw = resid_w(xp, load_elem<Elem>(qrow + e * E), t.c2, t.nz0, t.nz1, pv);
+                const float rw = resid_w(xp, vec_elem<E>(Q[k / kVec], k % kVec), t.c2, t.nz0, t.nz1, pv);
                 wv[k] = fallback ? pv : rw;
             }
         }
     }
-    float own = 0.0f;
+    float own2 = 0.0f;
     int lp = -1;
 #pragma unroll
-    for (int k = 0; k < kSliceMax / 32; ++k) {
-        own += wv[k];
+    for (int k = 0; k < kPer; ++k) {
+        own2 += wv[k];
         if (wv[k] > 0.0f) lp = b + k;
     }
-    float incl = own;
+    float incl2 = own2;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        const float y = __shfl_up_sync(0xffffffffu, incl2, o);
+        if (lane >= o) incl2 += y;
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && incl > tloc);
+    const unsigned hit2 = __ballot_sync(0xffffffffu, cnt > 0 && incl2 > tloc);
     int found = -1;
-    if (hit) {
-        const int owner = __ffs(hit) - 1;
+    if (hit2) {
+        const int owner = __ffs(hit2) - 1;
         if (lane == owner) {
-            float cum = incl - own;
+            float cum = incl2 - own2;
 #pragma unroll
-            for (int k = 0; k < kSliceMax / 32; ++k) {
+            for (int k = 0; k < kPer; ++k) {
                 cum += wv[k];
                 if (found < 0 && k < cnt && cum > tloc) found = b + k;
             }
@@ -1132,14 +1204,6 @@ __device__ __forceinline__ void resid_vec(const uint4& A, const uint4& B, uint64
     }
 }
 
-// Element j (0 .. 16/E - 1) of a 16-byte vector, as float.
-template <int E>
-__device__ __forceinline__ float vec_elem(const uint4& v, int j) {
-    const uint32_t w = j < (8 / E) ? (j < (4 / E) ? v.x : v.y) : (j < (12 / E) ? v.z : v.w);
-    if constexpr (E == 2) return (j & 1) ? bf16hi(w) : bf16lo(w);
-    else return __uint_as_float(w);
-}
-
 // Largest element of a 16-byte vector.
 template <int E>
 __device__ __forceinline__ float vec_max(const uint4& v) {
@@ -1409,6 +1473,8 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
         }
     }
 }
+
+static_assert(sizeof(SmemV) + 128 <= 113 * 1024, "two CTAs per SM");
 
 template <typename Elem>
 cudaError_t launch_verify_t(const VerifyArgs& a, int grid, cudaStream_t stream) {
