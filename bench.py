@@ -365,7 +365,7 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} hbm_gbs", "avg_launch_us": verify_avg_s * 1e6},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,  # verify_kernel + propose_kernel per step
         "clocks": sampler.summary(),
         "wall_s_timed": t_wall,
     }

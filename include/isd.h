@@ -58,10 +58,10 @@
  *           *_workspace_bytes() reports, 256-byte aligned, ZERO-FILLED
  *           before its first use; every call leaves it reusable for the next
  *           call of the same entry point.  Calls that share a workspace must
- *           be ordered (same stream or events).  Internal waits are bounded:
- *           if one ever gives up (a hardware fault, not an input error), the
- *           affected outputs read accept_len = -2 / valid = 0 and the
- *           workspace must be zero-filled again.
+ *           be ordered (same stream or events).  isd_verify's internal
+ *           waits are bounded: if one ever gives up (a hardware fault, not an
+ *           input error), every accept_len reads -2 and the workspace must be
+ *           zero-filled again.  isd_propose has no internal waits.
  * Errors.   Host-side checks return a status and launch nothing.  A CUDA
  *           launch error returns ISD_ERR_CUDA (the sticky error is left for
  *           the caller to inspect).
@@ -86,7 +86,8 @@ typedef enum {
     ISD_OK = 0,
     ISD_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld < vocab, bad dtype */
     ISD_ERR_UNSUPPORTED = 2,   /* logits base not 16-byte aligned; isd_verify: vocab above
-                                  523,264 (bf16) or 261,632 (fp32) */
+                                  523,264 (bf16) or 261,632 (fp32); isd_propose: vocab above
+                                  1,047,552 (bf16) or 523,776 (fp32) */
     ISD_ERR_WORKSPACE = 3,     /* workspace too small or not 256-byte aligned */
     ISD_ERR_CUDA = 4           /* a CUDA call failed (launch or device query) */
 } isd_status;

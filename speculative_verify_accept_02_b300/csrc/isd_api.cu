@@ -80,16 +80,16 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl) {
     return l;
 }
 
-// Workspace of isd_propose: [err word | chunk partials of the qnew rows]
+// Workspace of isd_propose: [per-row chunk counters | chunk partials of the qnew rows]
 struct ProposeLayout {
-    size_t err, part, bytes;
+    size_t row_count, part, bytes;
 };
 
 ProposeLayout propose_layout(int total, const Chunking& ck) {
     ProposeLayout l;
     size_t off = 0;
-    l.err = off;
-    off = align_up(off + sizeof(int));
+    l.row_count = off;
+    off = align_up(off + sizeof(int) * static_cast<size_t>(total));
     l.part = off;
     off = align_up(off + sizeof(float2) * static_cast<size_t>(total) * ck.nchunks);
     l.bytes = off;
@@ -108,7 +108,6 @@ isd_status resident_grid(long long n_items, int ctas_per_sm, int* grid) {
     return ISD_OK;
 }
 
-isd_status stats_grid(long long n_items, int* grid) { return resident_grid(n_items, isd::kStatsCtasPerSm, grid); }
 
 }  // namespace
 
@@ -202,40 +201,9 @@ isd_status isd_propose(const void* qnew_logits, int64_t ld, isd_dtype dtype, int
     const ProposeLayout lay = propose_layout(total_positions, ck);
     if (workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
         return ISD_ERR_WORKSPACE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (ck.nchunks > isd::kMaxProposeChunks) return ISD_ERR_UNSUPPORTED;
     char* ws = static_cast<char*>(workspace);
-    int* err = reinterpret_cast<int*>(ws + lay.err);
-    float2* part = reinterpret_cast<float2*>(ws + lay.part);
-
-    const long long n_items = static_cast<long long>(total_positions) * ck.nchunks;
-    if (n_items > 0) {
-        isd::StatsArgs sa{};
-        sa.rows0 = static_cast<const char*>(qnew_logits);
-        sa.ld0_bytes = ld * esz;
-        sa.rows1 = nullptr;
-        sa.ld1_bytes = 0;
-        sa.tokens = nullptr;
-        sa.seq_offsets = seq_offsets;
-        sa.temperature = temperature;
-        sa.accept_len = accept_len_or_null;
-        sa.num_seqs = num_seqs;
-        sa.total = total_positions;
-        sa.vocab = vocab;
-        sa.chunk = ck.chunk;
-        sa.nchunks = ck.nchunks;
-        sa.two_rows = 0;
-        sa.n_items = n_items;
-        sa.part = part;
-        sa.zx = nullptr;
-        sa.zero_ptr = nullptr;
-        sa.zero_count = 0;
-        sa.err = err;
-        int grid = 1;
-        const isd_status gs = stats_grid(n_items, &grid);
-        if (gs != ISD_OK) return gs;
-        if (isd::launch_stats(sa, esz, grid, st) != cudaSuccess) return ISD_ERR_CUDA;
-    }
-    isd::ProposeSampleArgs pa{};
+    isd::ProposeArgs pa{};
     pa.rows = static_cast<const char*>(qnew_logits);
     pa.ld_bytes = ld * esz;
     pa.seq_offsets = seq_offsets;
@@ -248,11 +216,15 @@ isd_status isd_propose(const void* qnew_logits, int64_t ld, isd_dtype dtype, int
     pa.nchunks = ck.nchunks;
     pa.seed = seed;
     pa.offset = offset;
-    pa.part = part;
-    pa.err = err;
+    pa.part = reinterpret_cast<float2*>(ws + lay.part);
+    pa.row_count = reinterpret_cast<int*>(ws + lay.row_count);
     pa.proposals = proposals;
     pa.valid = valid;
-    if (isd::launch_propose_sample(pa, esz, st) != cudaSuccess) return ISD_ERR_CUDA;
+    int grid = 1;
+    const long long n_items = static_cast<long long>(total_positions) * ck.nchunks;
+    const isd_status gs = resident_grid(n_items > num_seqs ? n_items : num_seqs, isd::kProposeCtasPerSm, &grid);
+    if (gs != ISD_OK) return gs;
+    if (isd::launch_propose(pa, esz, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ISD_ERR_CUDA;
     return ISD_OK;
 }
 

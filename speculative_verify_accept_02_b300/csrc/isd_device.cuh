@@ -345,4 +345,56 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
+// ---------------------------------------------------------------------------
+// Streaming reductions shared by the verify and propose kernels
+// ---------------------------------------------------------------------------
+// Tempered softmax weight relative to a reference mc = max * c2.
+__device__ __forceinline__ float soft_w(float x, float c2, float mc) { return ex2_approx(__fmaf_rn(x, c2, -mc)); }
+
+// Softmax partials in the mc domain: (mc, s) holds sum exp2(x c2 - mc).
+__device__ __forceinline__ void merge_mc(float& M, float& S, float m, float s) {
+    if (m == -INFINITY) return;
+    if (m > M) {
+        S = (M == -INFINITY) ? s : S * ex2_approx(M - m) + s;
+        M = m;
+    } else {
+        S += s * ex2_approx(m - M);
+    }
+}
+
+// Element j (0 .. 16/E - 1) of a 16-byte vector, as float.
+template <int E>
+__device__ __forceinline__ float vec_elem(const uint4& v, int j) {
+    const uint32_t w = j < (8 / E) ? (j < (4 / E) ? v.x : v.y) : (j < (12 / E) ? v.z : v.w);
+    if constexpr (E == 2) return (j & 1) ? bf16hi(w) : bf16lo(w);
+    else return __uint_as_float(w);
+}
+
+// Largest element of a 16-byte vector.
+template <int E>
+__device__ __forceinline__ float vec_max(const uint4& v) {
+    if constexpr (E == 2) {
+        const uint32_t m = hmax2_bf16(hmax2_bf16(v.x, v.y), hmax2_bf16(v.z, v.w));
+        return fmaxf(bf16lo(m), bf16hi(m));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+}
+
+// Sum of exp2(x c2 - mc) over a 16-byte vector, added to a packed accumulator.
+template <int E>
+__device__ __forceinline__ void soft_vec(const uint4& v, uint64_t C2, uint64_t NMC, uint64_t& acc) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; j += (E == 2 ? 1 : 2)) {
+        float y0, y1;
+        if constexpr (E == 2)
+            unpack_f2(fma_f2(pack_f2(bf16lo(w[j]), bf16hi(w[j])), C2, NMC), y0, y1);
+        else
+            unpack_f2(fma_f2(pack_f2(__uint_as_float(w[j]), __uint_as_float(w[j + 1])), C2, NMC), y0, y1);
+        acc = add_f2(acc, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+    }
+}
+
 }  // namespace isd

@@ -31,38 +31,13 @@ inline Chunking make_chunking(int vocab, int elem_bytes) {
     return c;
 }
 
-// Per-(row, chunk) streaming pass: softmax partials (max, sum of exp2) for
-// T > 0 rows, (max, lowest argmax id) for T = 0 rows, and the logit of the
-// proposed token of each verified row.
-struct StatsArgs {
-    const char* rows0;          // verify: anchor p; propose: qnew
-    int64_t ld0_bytes;
-    const char* rows1;          // verify: proposal q; propose: unused
-    int64_t ld1_bytes;
-    const int32_t* tokens;      // verify: x_k (gathered); propose: null
-    const int32_t* seq_offsets;
-    const float* temperature;
-    const int32_t* accept_len;  // propose: skip sequences with a_i != L_i; else null
-    int num_seqs;
-    int total;
-    int vocab;
-    int chunk;
-    int nchunks;
-    int two_rows;               // 1: verify (slot 2r = p row, 2r+1 = q row); 0: propose
-    long long n_items;          // slots * nchunks
-    float2* part;               // [slots * nchunks]
-    float* zx;                  // [slots] gathered logit (verify)
-    int* zero_ptr;              // counters of the following kernel, zeroed here
-    int zero_count;
-    int* err;                   // error word (bounded waits)
-};
-
-struct ProposeSampleArgs {
+// The propose kernel: every (qnew row, chunk) of the batch.
+struct ProposeArgs {
     const char* rows;
     int64_t ld_bytes;
     const int32_t* seq_offsets;
     const float* temperature;
-    const int32_t* accept_len;
+    const int32_t* accept_len;  // null: every valid sequence is drawn
     int num_seqs;
     int total;
     int vocab;
@@ -70,11 +45,18 @@ struct ProposeSampleArgs {
     int nchunks;
     uint64_t seed;
     uint64_t offset;
-    const float2* part;
-    const int* err;
+    float2* part;               // [total * nchunks] chunk partials
+    int* row_count;             // [total] chunks of each row reduced (zero between calls)
     int32_t* proposals;
     uint8_t* valid;
 };
+
+// Most chunks per qnew row the propose kernel supports (vocabularies up to
+// 1,047,552 bf16 or 523,776 fp32 ids).
+constexpr int kMaxProposeChunks = 128;
+
+// Resident CTAs of the propose kernel per SM.
+constexpr int kProposeCtasPerSm = 2;
 
 // ---------------------------------------------------------------------------
 // Persistent verify kernel
@@ -157,12 +139,8 @@ constexpr int kVerifyCtasPerSm = 2;
 cudaError_t launch_verify(const VerifyArgs& a, int elem_bytes, int grid, cudaStream_t stream);
 
 // Launchers (return the launch's cudaError_t).
-cudaError_t launch_stats(const StatsArgs& a, int elem_bytes, int grid, cudaStream_t stream);
-cudaError_t launch_propose_sample(const ProposeSampleArgs& a, int elem_bytes, cudaStream_t stream);
+cudaError_t launch_propose(const ProposeArgs& a, int elem_bytes, int grid, cudaStream_t stream);
 cudaError_t launch_alpha(const float* ratio, const int32_t* seq_offsets, int num_seqs, int total,
                          float* alpha_per_seq, float* alpha_mean, cudaStream_t stream);
-
-// Resident CTAs of the streaming kernel per SM.
-constexpr int kStatsCtasPerSm = 2;
 
 }  // namespace isd

@@ -145,23 +145,12 @@ __device__ __forceinline__ float load_elem(const void* p) {
         return *static_cast<const float*>(p);
 }
 
-// Element j (0 .. 16/E - 1) of a 16-byte vector, as float.
-template <int E>
-__device__ __forceinline__ float vec_elem(const uint4& v, int j) {
-    const uint32_t w = j < (8 / E) ? (j < (4 / E) ? v.x : v.y) : (j < (12 / E) ? v.z : v.w);
-    if constexpr (E == 2) return (j & 1) ? bf16hi(w) : bf16lo(w);
-    else return __uint_as_float(w);
-}
-
 // Element e of a staged piece: shared memory first, then the unaligned tail.
 template <typename Elem>
 __device__ __forceinline__ float piece_elem(const unsigned char* st, int nsm, int skip, const char* tail, int e) {
     return e < nsm ? load_elem<Elem>(st + static_cast<size_t>(e + skip) * sizeof(Elem))
                    : load_elem<Elem>(tail + static_cast<size_t>(e - nsm) * sizeof(Elem));
 }
-
-// Tempered softmax weight relative to a reference mc = max * c2.
-__device__ __forceinline__ float soft_w(float x, float c2, float mc) { return ex2_approx(__fmaf_rn(x, c2, -mc)); }
 
 // Residual weight max(0, p - q) of one id, and p itself.
 // nz0, nz1: log2 of the normalisers of p and q in the exp2 domain, so that
@@ -172,17 +161,8 @@ __device__ __forceinline__ float resid_w(float xp, float xq, float c2, float nz0
     return fmaxf(0.0f, __fsub_rn(pv, qv));
 }
 
-// Softmax partials in the mc domain: (mc, s) holds sum exp2(x c2 - mc).
-__device__ __forceinline__ void merge_mc(float& M, float& S, float m, float s) {
-    if (m == -INFINITY) return;
-    if (m > M) {
-        S = (M == -INFINITY) ? s : S * ex2_approx(M - m) + s;
-        M = m;
-    } else {
-        S += s * ex2_approx(m - M);
-    }
-}
-
+// Softmax partials in the mc domain: (mc, s) holds sum exp2(x c2 - mc);
+// merge_mc (isd_device.cuh) merges two of them.
 __device__ __forceinline__ void warp_merge_mc(float& M, float& S) {
     const float W = warp_max(M);
     S = (M == -INFINITY) ? 0.0f : S * ex2_approx(M - W);
@@ -1201,33 +1181,6 @@ __device__ __forceinline__ void resid_vec(const uint4& A, const uint4& B, uint64
                    NZ1, sw, sp);
         resid_pair(__uint_as_float(A.z), __uint_as_float(A.w), __uint_as_float(B.z), __uint_as_float(B.w), C2, NZ0,
                    NZ1, sw, sp);
-    }
-}
-
-// Largest element of a 16-byte vector.
-template <int E>
-__device__ __forceinline__ float vec_max(const uint4& v) {
-    if constexpr (E == 2) {
-        const uint32_t m = hmax2_bf16(hmax2_bf16(v.x, v.y), hmax2_bf16(v.z, v.w));
-        return fmaxf(bf16lo(m), bf16hi(m));
-    } else {
-        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
-                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
-    }
-}
-
-// Sum of exp2(x c2 - mc) over a 16-byte vector, added to a packed accumulator.
-template <int E>
-__device__ __forceinline__ void soft_vec(const uint4& v, uint64_t C2, uint64_t NMC, uint64_t& acc) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; j += (E == 2 ? 1 : 2)) {
-        float y0, y1;
-        if constexpr (E == 2)
-            unpack_f2(fma_f2(pack_f2(bf16lo(w[j]), bf16hi(w[j])), C2, NMC), y0, y1);
-        else
-            unpack_f2(fma_f2(pack_f2(__uint_as_float(w[j]), __uint_as_float(w[j + 1])), C2, NMC), y0, y1);
-        acc = add_f2(acc, pack_f2(ex2_approx(y0), ex2_approx(y1)));
     }
 }
 
