@@ -31,6 +31,7 @@ struct VerifyPlan {
 
 constexpr int kSubChunksPerSegment = 8;  // one main item: 8 x 16 KB
 constexpr int kTailSubChunksPerTask = 2;
+constexpr double kL2KeepBytes = 40.0 * (1 << 20);  // of the 126 MB L2
 
 VerifyPlan verify_plan(int vocab, int esz) {
     VerifyPlan pl;
@@ -163,6 +164,9 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
     va.tpt = pl.tpt;
     va.ntask = pl.ntask;
     va.n_main = 2LL * total_positions * pl.nseg;
+    // Rows of the first position of every sequence, both p and q, kept in L2
+    // while they fit in about a third of it.
+    va.keep_first = 2.0 * num_seqs * vocab * esz <= kL2KeepBytes ? 1 : 0;
     va.seed = seed;
     va.offset = offset;
     va.ctl = reinterpret_cast<isd::VerifyCtl*>(ws + lay.ctl);

@@ -77,8 +77,7 @@ struct VerifyCtl {
 // Tail kinds: which row(s) the work after a decision reads.
 enum TailMode : int {
     kTailRes = 2,   // T > 0, rejection: residual max(0, p_j - q_j) over row pair j
-    kTailSoft = 3,  // T > 0, all accepted: softmax of the final anchor p_{L+1}
-    kTailArg = 4    // T = 0, all accepted: argmax of p_{L+1}
+    kTailSoft = 3   // T > 0, all accepted: softmax of the final anchor p_{L+1}
 };
 
 // What a sequence's tail needs, written by its decision (48 bytes).
@@ -112,6 +111,7 @@ struct VerifyArgs {
     int tpt;          // tail sub-chunks per tail task
     int ntask;        // tail tasks per sequence
     long long n_main; // 2 * total * nseg main items
+    int keep_first;   // 1: first-position rows of T > 0 sequences are kept in L2 for their tails
     uint64_t seed;
     uint64_t offset;
     VerifyCtl* ctl;

@@ -100,6 +100,7 @@ struct Rec {
 struct Work {
     int kind;
     int seq, slot, seg, expect, c0, c1;
+    int keep;  // load under the L2 evict_last policy (rows likely re-read by a tail)
     float c2, nz0, nz1;
     const char* row0;
     const char* row1;
@@ -339,9 +340,24 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         a.accept_len[i] = na;
         a.alpha[i] = total / static_cast<float>(L);
     }
-    if (T == 0.0f && na < L) {  // greedy correction: argmax of p_j, already known
+    if (T == 0.0f) {
+        // Greedy: the correction is the argmax of p_j, already known; the
+        // bonus is the argmax of p_{L+1}, streamed in the last position's q
+        // slot.
+        int tok = amax_j;
+        if (na == L) {
+            const float2* pb = a.part + static_cast<size_t>(2 * (s.start + L - 1) + 1) * a.nseg;
+            float M = -INFINITY;
+            int I = INT_MAX;
+            for (int g = lane; g < a.nseg; g += 32) {
+                const float2 v = __ldcg(pb + g);
+                merge_argmax(M, I, v.x, __float_as_int(v.y));
+            }
+            warp_merge_arg(M, I);
+            tok = I;
+        }
         if (lane == 0) {
-            a.out_tokens[s.start + i + na] = amax_j;
+            a.out_tokens[s.start + i + na] = tok;
             a.seq_count[i] = 0;
             finalize(a);
         }
@@ -350,7 +366,7 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
     int base = 0;
     if (lane == 0) {
         SeqTail t = {};
-        t.mode = na < L ? kTailRes : (T > 0.0f ? kTailSoft : kTailArg);
+        t.mode = na < L ? kTailRes : kTailSoft;
         t.a = na;
         t.prow = s.start + i + na;  // p_j, or p_{L+1} when na == L
         t.qrow = s.start + na;
@@ -399,18 +415,6 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
     __syncwarp();
     const SeqInfo s = seq_lookup(a, sm, i);
     const int out_slot = s.start + i + t.a;
-    if (t.mode == kTailArg) {
-        float M = -INFINITY;
-        int I = INT_MAX;
-        for (int u = lane; u < U; u += 32) merge_argmax(M, I, sm.tsel[fi][u].x, __float_as_int(sm.tsel[fi][u].y));
-        warp_merge_arg(M, I);
-        if (lane == 0) {
-            a.out_tokens[out_slot] = I;
-            a.tail_count[i] = 0;
-            finalize(a);
-        }
-        return;
-    }
     // Slice weights in one scale, the target u * total, and its slice.  Lane
     // l owns the consecutive slices [l * ub, (l + 1) * ub): the lanes reduce
     // their blocks locally and meet in one scan, so the pass costs a handful
@@ -743,16 +747,25 @@ __device__ bool main_work(const VerifyArgs& a, const SmemV& sm, long long w, Seq
         }
     }
     if (!sc.ok) return false;
-    if (kind == 1 && sc.T == 0.0f) return false;  // greedy verification never reads q
+    // Greedy verification reads no q rows; the last position's q slot streams
+    // the final anchor row p_{L+1} instead, whose argmax is the bonus token.
+    const bool greedy = !(sc.T > 0.0f);
+    const bool bonus = greedy && kind == 1;
+    if (bonus && r != sc.start + sc.len - 1) return false;
     wk.kind = kMain;
     wk.seq = sc.i;
     wk.slot = slot;
     wk.seg = seg;
-    wk.expect = (sc.T > 0.0f ? 2 : 1) * sc.len * a.nseg;
+    wk.expect = (greedy ? sc.len + 1 : 2 * sc.len) * a.nseg;
+    // A rejection is likeliest at the first position: its rows stay in L2
+    // for the residual tail when the batch can afford it.
+    wk.keep = a.keep_first && !greedy && r == sc.start;
     wk.c0 = seg * a.spseg;
     wk.c1 = min(wk.c0 + a.spseg, a.nck);
     wk.c2 = sc.T > 0.0f ? inv_temp_log2e(sc.T) : 0.0f;
-    wk.row0 = kind ? a.q + static_cast<int64_t>(r) * a.ldq_bytes : a.p + static_cast<int64_t>(r + sc.i) * a.ldp_bytes;
+    wk.row0 = bonus  ? a.p + static_cast<int64_t>(r + sc.i + 1) * a.ldp_bytes
+              : kind ? a.q + static_cast<int64_t>(r) * a.ldq_bytes
+                     : a.p + static_cast<int64_t>(r + sc.i) * a.ldp_bytes;
     wk.row1 = nullptr;
     return true;
 }
@@ -769,6 +782,7 @@ __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
     wk.slot = 0;
     wk.seg = 0;
     wk.expect = 0;
+    wk.keep = 0;
     wk.c0 = y * a.tpt;
     wk.c1 = min(wk.c0 + a.tpt, a.nt);
     wk.c2 = __int_as_float(w1.x);
@@ -894,7 +908,8 @@ __device__ __forceinline__ int acquire_stage(SmemV& sm, long long n, int* err) {
 
 // Stream sub-chunks [c0, c1) of one unit of work into the stage ring.
 template <typename Elem>
-__device__ bool issue_work(const VerifyArgs& a, SmemV& sm, const Work& wk, int c0, int c1, long long& n) {
+__device__ bool issue_work(const VerifyArgs& a, SmemV& sm, const Work& wk, int c0, int c1, long long& n,
+                           uint64_t pol_first, uint64_t pol_last) {
     constexpr int E = sizeof(Elem);
     const bool main = wk.kind == kMain;
     const int ck = main ? a.ck : a.ckt;
@@ -928,12 +943,13 @@ __device__ bool issue_work(const VerifyArgs& a, SmemV& sm, const Work& wk, int c
         const int bytes = pa.bytes + pb.bytes;
         if (bytes > 0) {
             mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(bytes));
+            const uint64_t pol = wk.keep ? pol_last : pol_first;
             if (pa.bytes > 0)
-                bulk_copy_g2s(sm.stage[stage], reinterpret_cast<const void*>(pa.lo),
-                              static_cast<uint32_t>(pa.bytes), &sm.full[stage]);
+                bulk_copy_g2s_hint(sm.stage[stage], reinterpret_cast<const void*>(pa.lo),
+                                   static_cast<uint32_t>(pa.bytes), &sm.full[stage], pol);
             if (pb.bytes > 0)
-                bulk_copy_g2s(sm.stage[stage] + kHalf, reinterpret_cast<const void*>(pb.lo),
-                              static_cast<uint32_t>(pb.bytes), &sm.full[stage]);
+                bulk_copy_g2s_hint(sm.stage[stage] + kHalf, reinterpret_cast<const void*>(pb.lo),
+                                   static_cast<uint32_t>(pb.bytes), &sm.full[stage], pol);
         } else {
             mbar_arrive(&sm.full[stage]);
         }
@@ -946,6 +962,7 @@ template <typename Elem>
 __device__ void issuer(const VerifyArgs& a, SmemV& sm) {
     long long n = 0, kp = 0;
     bool ok = true;
+    const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
     // Tail work waiting in the priority slot goes first, between any two
     // stages; returns -1 on a timeout, 1 if it issued work, 0 otherwise.
     auto priority = [&]() -> int {
@@ -953,7 +970,7 @@ __device__ void issuer(const VerifyArgs& a, SmemV& sm) {
         const Work pw = sm.prio;
         mbar_arrive(&sm.prio_empty);
         ++kp;
-        return issue_work<Elem>(a, sm, pw, pw.c0, pw.c1, n) ? 1 : -1;
+        return issue_work<Elem>(a, sm, pw, pw.c0, pw.c1, n, pol_first, pol_last) ? 1 : -1;
     };
     for (long long k = 0; ok; ++k) {
         const int ws = static_cast<int>(k % kWork);
@@ -976,7 +993,7 @@ __device__ void issuer(const VerifyArgs& a, SmemV& sm) {
         if (wk.kind == kEnd) break;
         for (int c = wk.c0; c < wk.c1 && ok; ++c) {
             ok = priority() >= 0;
-            if (ok) ok = issue_work<Elem>(a, sm, wk, c, c + 1, n);
+            if (ok) ok = issue_work<Elem>(a, sm, wk, c, c + 1, n, pol_first, pol_last);
         }
     }
     const int stage = acquire_stage(sm, n, &a.ctl->err);
@@ -1243,7 +1260,7 @@ __device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int s
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
         part = make_float2(warp_sum(sws), warp_sum(sps));
-    } else if (d.kind == kTailSoft) {
+    } else {  // kTailSoft
         float mt = -INFINITY, st = 0.0f;
         if (vec) {
             mt = fmaxf(vec_max<E>(A0), vec_max<E>(A1));
@@ -1269,39 +1286,6 @@ __device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int s
         float M = mt == -INFINITY ? -INFINITY : mt * d.c2, S = st;
         warp_merge_mc(M, S);
         part = make_float2(M, S);
-    } else {  // kTailArg: the lane's first maximum in id order
-        float mt = -INFINITY;
-        int it = INT_MAX;
-        if (vec) {
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float x = vec_elem<E>(A0, j);
-                if (x > mt) {
-                    mt = x;
-                    it = d.e0 + v0 * kVec + j;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float x = vec_elem<E>(A1, j);
-                if (x > mt) {
-                    mt = x;
-                    it = d.e0 + v1 * kVec + j;
-                }
-            }
-        } else {
-            for (int e = wb + lane; e < we; e += 32) {
-                const float x = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
-                if (x > mt) {
-                    mt = x;
-                    it = d.e0 + e;
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        warp_merge_arg(mt, it);
-        part = make_float2(mt, __int_as_float(it));
     }
     push_record(a, sm, nrec, warp, lane, part, d.kind, d.flags, d.seq, d.slot, 0, 0);
 }
