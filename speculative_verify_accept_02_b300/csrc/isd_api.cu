@@ -68,7 +68,7 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl) {
     l.tails = off;
     off = align_up(off + sizeof(isd::SeqTail) * C);
     l.tasks = off;
-    off = align_up(off + sizeof(int2) * C * pl.ntask);
+    off = align_up(off + 2 * sizeof(int4) * C * pl.ntask);
     l.task_ready = off;
     off = align_up(off + sizeof(int) * C * pl.ntask);
     l.part = off;
@@ -173,7 +173,7 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
     va.seq_count = reinterpret_cast<int*>(ws + lay.seq_count);
     va.tail_count = reinterpret_cast<int*>(ws + lay.tail_count);
     va.tails = reinterpret_cast<isd::SeqTail*>(ws + lay.tails);
-    va.tasks = reinterpret_cast<int2*>(ws + lay.tasks);
+    va.tasks = reinterpret_cast<int4*>(ws + lay.tasks);
     va.task_ready = reinterpret_cast<int*>(ws + lay.task_ready);
     va.part = reinterpret_cast<float2*>(ws + lay.part);
     va.zx = reinterpret_cast<float*>(ws + lay.zx);

@@ -118,7 +118,8 @@ struct VerifyArgs {
     int* seq_count;   // [C] main items finished
     int* tail_count;  // [C] tail tasks finished
     SeqTail* tails;   // [C]
-    int2* tasks;      // [C * ntask] (sequence, task) in reservation order
+    int4* tasks;      // [C * ntask][2] task records in reservation order:
+                      // {sequence, task, mode, p row}, {q row, c2, nz0, nz1}
     int* task_ready;  // [C * ntask] 1 once the slot's task is published
     float2* part;     // [2 * total * nseg] per (row slot, segment) partials
     float* zx;        // [2 * total] logit of the proposed token, p and q rows

@@ -62,6 +62,7 @@ constexpr int kRecs = 8;                  // record ring between consumers and b
 constexpr int kVecPT = kStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
 constexpr int kHalf = kStageBytes / 2;          // tail stages: [p piece | q piece]
 constexpr int kSmemSeqs = 512;                  // batches up to this size keep offsets in shared memory
+constexpr int kSmemToks = 2048;                 // batches up to this many positions keep their tokens there
 constexpr int kSliceMax = 512;                  // ids in one tail slice (tail sub-chunk / 8 warps)
 static_assert(kHalf / 2 <= kSliceMax * kCW, "a tail sub-chunk of bf16 ids splits into slices of at most kSliceMax");
 static_assert(kVecPT * 16 * kCT == kStageBytes, "stage split");
@@ -136,6 +137,7 @@ struct SmemV {
     int batch_bad;
     int offs[kSmemSeqs + 1];
     float temp[kSmemSeqs];
+    int tok[kSmemToks];
 };
 
 template <typename Elem>
@@ -276,7 +278,7 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
     const float c2 = T > 0.0f ? inv_temp_log2e(T) : 0.0f;
     const int r = s.start + lane;
     const bool mine = lane < L;
-    const int x = mine ? __ldg(a.tokens + r) : 0;
+    const int x = mine ? (a.total <= kSmemToks ? sm.tok[r] : __ldg(a.tokens + r)) : 0;
     if (__any_sync(0xffffffffu, mine && (x < 0 || x >= a.vocab))) {
         write_invalid(a, i, s, lane, -1);
         if (lane == 0) {
@@ -330,7 +332,7 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
     const float total = warp_sum(ratio);
     if (mine) a.ratio[r] = ratio;
     for (int m = lane; m <= L; m += 32) {
-        if (m < na) a.out_tokens[s.start + i + m] = __ldg(a.tokens + s.start + m);
+        if (m < na) a.out_tokens[s.start + i + m] = x;  // m < na <= 32: m is this lane
         else if (m > na) a.out_tokens[s.start + i + m] = -1;
     }
     const int amax_j = __shfl_sync(0xffffffffu, amax, na & 31);
@@ -363,24 +365,36 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         }
         return;
     }
+    // Every task record carries what its producer needs, so that taking a
+    // task is one round trip.
+    const int mode = na < L ? kTailRes : kTailSoft;
+    const int prow = s.start + i + na;  // p_j, or p_{L+1} when na == L
+    const int qrow = s.start + na;
+    float nz0 = 0.0f, nz1 = 0.0f;
+    if (na < L) {
+        nz0 = __fadd_rn(mc0, log2f(sp0));
+        nz1 = __fadd_rn(mc1, log2f(sq0));
+    }
     int base = 0;
     if (lane == 0) {
         SeqTail t = {};
-        t.mode = na < L ? kTailRes : kTailSoft;
+        t.mode = mode;
         t.a = na;
-        t.prow = s.start + i + na;  // p_j, or p_{L+1} when na == L
-        t.qrow = s.start + na;
+        t.prow = prow;
+        t.qrow = qrow;
         t.c2 = c2;
-        if (na < L) {
-            t.nz0 = __fadd_rn(mc0, log2f(sp0));
-            t.nz1 = __fadd_rn(mc1, log2f(sq0));
-        }
+        t.nz0 = nz0;
+        t.nz1 = nz1;
         a.tails[i] = t;
         a.seq_count[i] = 0;
         base = atomicAdd(&a.ctl->tail_reserve, a.ntask);
     }
     base = __shfl_sync(0xffffffffu, base, 0);
-    for (int y = lane; y < a.ntask; y += 32) a.tasks[base + y] = make_int2(i, y);
+    for (int y = lane; y < a.ntask; y += 32) {
+        int4* tr = a.tasks + 2 * static_cast<size_t>(base + y);
+        tr[0] = make_int4(i, y, mode, prow);
+        tr[1] = make_int4(qrow, __float_as_int(c2), __float_as_int(nz0), __float_as_int(nz1));
+    }
     // Tail state and tasks are visible before any task is flagged ready.
     __threadfence();
     __syncwarp();
@@ -773,11 +787,9 @@ __device__ bool main_work(const VerifyArgs& a, const SmemV& sm, long long w, Seq
 // Tail task of a published queue slot as work for the issuer.
 __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
     st_volatile(a.task_ready + slot, 0);
-    const int2 task = __ldcg(a.tasks + slot);
-    const int i = task.x, y = task.y;
-    const int4* tw = reinterpret_cast<const int4*>(a.tails + i);
-    const int4 w0 = __ldcg(tw), w1 = __ldcg(tw + 1);
-    wk.kind = w0.x;
+    const int4 w0 = __ldcg(a.tasks + 2 * static_cast<size_t>(slot)), w1 = __ldcg(a.tasks + 2 * static_cast<size_t>(slot) + 1);
+    const int i = w0.x, y = w0.y;
+    wk.kind = w0.z;
     wk.seq = i;
     wk.slot = 0;
     wk.seg = 0;
@@ -785,11 +797,11 @@ __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
     wk.keep = 0;
     wk.c0 = y * a.tpt;
     wk.c1 = min(wk.c0 + a.tpt, a.nt);
-    wk.c2 = __int_as_float(w1.x);
-    wk.nz0 = __int_as_float(w1.y);
-    wk.nz1 = __int_as_float(w1.z);
-    wk.row0 = a.p + static_cast<int64_t>(w0.z) * a.ldp_bytes;
-    wk.row1 = a.q + static_cast<int64_t>(w0.w) * a.ldq_bytes;
+    wk.c2 = __int_as_float(w1.y);
+    wk.nz0 = __int_as_float(w1.z);
+    wk.nz1 = __int_as_float(w1.w);
+    wk.row0 = a.p + static_cast<int64_t>(w0.w) * a.ldp_bytes;
+    wk.row1 = a.q + static_cast<int64_t>(w1.x) * a.ldq_bytes;
 }
 
 __device__ void scheduler(const VerifyArgs& a, SmemV& sm, unsigned long long next) {
@@ -1369,6 +1381,8 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
             if (i == a.num_seqs - 1) sm.offs[i + 1] = end;
         }
     }
+    if (a.total <= kSmemToks)  // the decisions read the proposed tokens from here
+        for (int r = tid; r < a.total; r += kThreadsV) sm.tok[r] = __ldg(a.tokens + r);
     __syncthreads();
     if (nv) atomicAdd(&sm.n_valid, nv);
     bad = __syncthreads_or(bad);
