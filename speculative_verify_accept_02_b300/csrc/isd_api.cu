@@ -24,7 +24,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Workspace of isd_verify (persistent kernel):
 //   [control block | per-sequence counters | per-sequence tail state |
 //    tail-task queue and flags | per (row slot, segment) partials |
-//    gathered logits | per tail sub-chunk partials]
+//    per (tail sub-chunk, consumer warp) slice partials]
 struct VerifyPlan {
     int ck, nck, spseg, nseg, ckt, nt, tpt, ntask;
 };
@@ -52,7 +52,7 @@ VerifyPlan verify_plan(int vocab, int esz) {
 }
 
 struct VerifyLayout {
-    size_t ctl, seq_count, tail_count, tails, tasks, task_ready, part, zx, tpart, bytes;
+    size_t ctl, seq_count, tail_count, tails, tasks, task_ready, part, tpart, bytes;
 };
 
 VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl) {
@@ -73,8 +73,6 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl) {
     off = align_up(off + sizeof(int) * C * pl.ntask);
     l.part = off;
     off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * pl.nseg);
-    l.zx = off;
-    off = align_up(off + sizeof(float) * 2 * static_cast<size_t>(total));
     l.tpart = off;
     off = align_up(off + sizeof(float2) * C * pl.nt * 8);  // 8 consumer-warp slices per tail sub-chunk
     l.bytes = off;
@@ -176,7 +174,6 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
     va.tasks = reinterpret_cast<int4*>(ws + lay.tasks);
     va.task_ready = reinterpret_cast<int*>(ws + lay.task_ready);
     va.part = reinterpret_cast<float2*>(ws + lay.part);
-    va.zx = reinterpret_cast<float*>(ws + lay.zx);
     va.tpart = reinterpret_cast<float2*>(ws + lay.tpart);
     va.accept_len = accept_len;
     va.out_tokens = out_tokens;

@@ -122,7 +122,6 @@ struct VerifyArgs {
                       // {sequence, task, mode, p row}, {q row, c2, nz0, nz1}
     int* task_ready;  // [C * ntask] 1 once the slot's task is published
     float2* part;     // [2 * total * nseg] per (row slot, segment) partials
-    float* zx;        // [2 * total] logit of the proposed token, p and q rows
     float2* tpart;    // [C * nt * 8] per (tail sub-chunk, consumer warp) slice partials
     int32_t* accept_len;
     int32_t* out_tokens;

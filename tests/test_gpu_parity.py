@@ -61,6 +61,7 @@ SMALL = [
     ("tiny", dict(num_seqs=6, vocab=5)),
     ("tiny", dict(num_seqs=4, vocab=1)),
     ("tiny", dict(num_seqs=5, vocab=17, dtype=torch.bfloat16)),
+    ("ragged", dict(num_seqs=600, vocab=300)),                  # layout and tokens beyond shared memory
 ]
 
 
@@ -82,9 +83,10 @@ def test_small_parity(name, kw):
     assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 20), rep
 
 
-@pytest.mark.parametrize("name", ["c64", "ragged", "tiny"])
-def test_propose_without_skip(name):
-    batch = workloads.make(name, **({} if name == "tiny" else dict(num_seqs=6)))
+@pytest.mark.parametrize("name,kw", [("c64", dict(num_seqs=6)), ("ragged", dict(num_seqs=6)), ("tiny", {}),
+                                     ("ragged", dict(num_seqs=600, vocab=300))])
+def test_propose_without_skip(name, kw):
+    batch = workloads.make(name, **kw)
     h = host(batch)
     _, gp = gpu_step(batch, 5, 11, skip_rejected=False)
     op = oracle.propose(h["qnew"], batch.vocab, h["offs"], h["temp"], 5, 11)
@@ -204,3 +206,30 @@ def test_greedy_ties_lowest_id():
     ov = oracle.verify(workloads.host_logits(Pb), workloads.host_logits(Qb), V, tokens.numpy(),
                        offs.numpy(), temps.numpy(), 0, 0)
     assert np.array_equal(ov["out_tokens"], out.out_tokens.cpu().numpy())
+
+
+def test_all_accepted_largest_stride():
+    """q identical to p accepts every proposal (Summary §3.2), here at the
+    largest stride: the bonus token comes from the final anchor p_{L+1}, by a
+    softmax draw at T > 0 and as its argmax at T = 0."""
+    V, L = 4099, 32
+    temps = np.array([1.0, 0.0, 0.6, 0.0], np.float32)
+    C = len(temps)
+    offs = (np.arange(C + 1) * L).astype(np.int32)
+    total = C * L
+    g = torch.Generator().manual_seed(11)
+    P = torch.randn(total + C, V, generator=g).to(torch.bfloat16)
+    prow = [int(offs[i]) + i + k for i in range(C) for k in range(L)]
+    Q = P[prow].clone()
+    tokens = torch.argmax(P[prow].float(), dim=1).to(torch.int32)  # accepted at T = 0 too
+    d = "cuda"
+    for seed, offset in ((0, 0), (3, 9)):
+        out = isd_verify(P.to(d), Q.to(d), tokens.to(d), torch.from_numpy(offs).to(d),
+                         torch.from_numpy(temps).to(d), seed, offset, total=total)
+        torch.cuda.synchronize()
+        gv = dict(accept_len=out.accept_len.cpu().numpy(), out_tokens=out.out_tokens.cpu().numpy(),
+                  ratio=out.ratio.cpu().numpy(), alpha=out.alpha.cpu().numpy())
+        assert list(gv["accept_len"]) == [L] * C
+        ov = oracle.verify(workloads.host_logits(P), workloads.host_logits(Q), V, tokens.numpy(), offs, temps,
+                           seed, offset)
+        compare_verify(ov, gv, offs).check()
