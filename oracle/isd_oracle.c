@@ -143,6 +143,16 @@ ORACLE_API double oracle_ratio(const double* P, const double* Q, int V, double T
     return r < 1.0 ? r : 1.0;
 }
 
+/* The acceptance test of the relaxed-acceptance ablation (Table 4 of the
+ * pages' experiments: the ratio multiplied by 1 + tau): min(1, (1+tau) p(x)/q(x)).
+ * tau = 0 gives the strict ratio; at T = 0 the argmax indicator stands. */
+ORACLE_API double oracle_ratio_relaxed(const double* P, const double* Q, int V, double T, int x, double tau) {
+    if (T == 0.0) return x == oracle_argmax(P, V) ? 1.0 : 0.0;
+    const double log_px = oracle_log_softmax_at(P, V, T, x), log_qx = oracle_log_softmax_at(Q, V, T, x);
+    if (log_qx == -INFINITY) return 1.0;
+    return fmin(1.0, (1.0 + tau) * exp(log_px - log_qx));
+}
+
 /* Residual weights at a rejection (§3.2): w = max(0, p - q) with p, q the
  * temperature-T softmaxes; left unnormalised (sampling normalises).  If every
  * weight is zero (possible only by rounding) the weights fall back to p. */
@@ -210,7 +220,7 @@ ORACLE_API void oracle_verify_one(const double* P, const double* Q, int V, int L
                                   const int32_t* x, const double* u_accept, const double* u_correct,
                                   double u_bonus, int32_t* accept_len, int32_t* out_tokens,
                                   double* ratio, double* alpha, double* accept_margin,
-                                  double* token_margin) {
+                                  double* token_margin, double tau) {
     /* §2: ratios of every position, and their mean. */
     double sum = 0.0;
     for (int k = 1; k <= L; ++k) {
@@ -219,16 +229,21 @@ ORACLE_API void oracle_verify_one(const double* P, const double* Q, int V, int L
     }
     *alpha = sum / L;
 
-    /* §3.2: strict acceptance, the accepted prefix ends at the first rejection. */
+    /* §3.2: strict acceptance, the accepted prefix ends at the first rejection.
+     * With tau > 0 the test uses the relaxed ratio instead; the reported
+     * ratios and alpha stay the strict ones (§2). */
     int a = 0;
     for (int k = 1; k <= L; ++k) {
         int accepted;
+        double racc = ratio[k - 1];
+        if (tau != 0.0)
+            racc = oracle_ratio_relaxed(P + (size_t)(k - 1) * V, Q + (size_t)(k - 1) * V, V, T, x[k - 1], tau);
         if (T == 0.0) {
             accepted = ratio[k - 1] == 1.0;
             accept_margin[k - 1] = INFINITY;
         } else {
-            accepted = u_accept[k - 1] < ratio[k - 1];
-            accept_margin[k - 1] = fabs(u_accept[k - 1] - ratio[k - 1]);
+            accepted = u_accept[k - 1] < racc;
+            accept_margin[k - 1] = fabs(u_accept[k - 1] - racc);
         }
         if (!accepted) break;
         a = k;
@@ -327,7 +342,7 @@ ORACLE_API void oracle_verify(const void* p_logits, int64_t ld_p, const void* q_
                               int num_seqs, const float* temperature, uint64_t seed, uint64_t offset,
                               int32_t* accept_len, int32_t* out_tokens, double* ratio, double* alpha,
                               double* accept_margin, double* token_margin, const int32_t* seqs,
-                              int n_sel, int nthreads) {
+                              int n_sel, int nthreads, double tau) {
     set_threads(nthreads);
     int count = seqs ? n_sel : num_seqs;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -364,7 +379,7 @@ ORACLE_API void oracle_verify(const void* p_logits, int64_t ld_p, const void* q_
         double u_bonus = oracle_uniform(seed, offset, (uint64_t)i, (uint64_t)(L + 1), TAG_BONUS);
         oracle_verify_one(P, Q, V, L, (double)T, tokens + start, u_acc, u_cor, u_bonus,
                           &accept_len[i], out_tokens + start + i, ratio + start, &alpha[i],
-                          accept_margin + start, &token_margin[i]);
+                          accept_margin + start, &token_margin[i], tau);
         free(P);
         free(Q);
     }

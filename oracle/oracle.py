@@ -44,11 +44,13 @@ def _declare(L):
     L.oracle_icdf.restype = C.c_int
     L.oracle_verify_one.argtypes = [_dp, _dp, C.c_int, C.c_int, C.c_double, _ip, _dp, _dp,
                                     C.c_double, C.POINTER(C.c_int32), _ip, _dp,
-                                    C.POINTER(C.c_double), _dp, C.POINTER(C.c_double)]
+                                    C.POINTER(C.c_double), _dp, C.POINTER(C.c_double), C.c_double]
     L.oracle_verify_one.restype = None
+    L.oracle_ratio_relaxed.argtypes = [_dp, _dp, C.c_int, C.c_double, C.c_int, C.c_double]
+    L.oracle_ratio_relaxed.restype = C.c_double
     L.oracle_verify.argtypes = [C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_int,
                                 _ip, _ip, C.c_int, _fp, C.c_uint64, C.c_uint64,
-                                _ip, _ip, _dp, _dp, _dp, _dp, C.c_void_p, C.c_int, C.c_int]
+                                _ip, _ip, _dp, _dp, _dp, _dp, C.c_void_p, C.c_int, C.c_int, C.c_double]
     L.oracle_verify.restype = None
     L.oracle_propose.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int, _ip, C.c_int, _fp,
                                  C.c_uint64, C.c_uint64, C.c_void_p, _ip, _bp, _dp,
@@ -139,8 +141,14 @@ class Oracle:
         v = self.lib.oracle_icdf(ww, ww.size, float(u), C.byref(m))
         return v, m.value
 
-    def verify_one(self, P, Q, T, x, u_accept, u_correct, u_bonus):
-        """One sequence with explicit uniforms. P: (L+1, V), Q: (L, V)."""
+    def ratio_relaxed(self, P, Q, T, x, tau):
+        """min(1, (1 + tau) p(x)/q(x)) of one row pair (argmax indicator at T = 0)."""
+        P, Q = _d(P), _d(Q)
+        return self.lib.oracle_ratio_relaxed(P, Q, P.size, float(T), int(x), float(tau))
+
+    def verify_one(self, P, Q, T, x, u_accept, u_correct, u_bonus, tau=0.0):
+        """One sequence with explicit uniforms. P: (L+1, V), Q: (L, V).  tau:
+        the accept test uses min(1, (1 + tau) p/q) (relaxed acceptance)."""
         P, Q = _d(P), _d(Q)
         L, V = Q.shape
         assert P.shape == (L + 1, V)
@@ -153,13 +161,15 @@ class Oracle:
         tm = C.c_double()
         self.lib.oracle_verify_one(P, Q, V, L, float(T), x, _d(u_accept), _d(u_correct),
                                    float(u_bonus), C.byref(a), out, r, C.byref(alpha), am,
-                                   C.byref(tm))
+                                   C.byref(tm), float(tau))
         return dict(accept_len=a.value, out_tokens=out, ratio=r, alpha=alpha.value,
                     accept_margin=am, token_margin=tm.value)
 
     def verify(self, p_logits, q_logits, vocab, tokens, seq_offsets, temperature, seed, offset,
-               seqs=None, nthreads=0):
-        """All (or the selected) sequences of one verify step.
+               seqs=None, nthreads=0, tau=0.0):
+        """All (or the selected) sequences of one verify step.  tau > 0: the
+        accept test uses the relaxed ratio min(1, (1 + tau) p/q); the reported
+        ratios and alpha stay the strict ones.
 
         Returns a dict of accept_len [C], out_tokens [sum L + C], ratio [sum L],
         alpha [C], accept_margin [sum L], token_margin [C]; entries of unselected
@@ -180,7 +190,8 @@ class Oracle:
         self.lib.oracle_verify(pa.ctypes.data, ld_p, qa.ctypes.data, ld_q, code_p, int(vocab),
                                toks, offs, C_, temp, int(seed), int(offset), out["accept_len"],
                                out["out_tokens"], out["ratio"], out["alpha"],
-                               out["accept_margin"], out["token_margin"], sp, sn, int(nthreads))
+                               out["accept_margin"], out["token_margin"], sp, sn, int(nthreads),
+                               float(tau))
         return out
 
     def propose(self, qnew_logits, vocab, seq_offsets, temperature, seed, offset, accept_len=None,

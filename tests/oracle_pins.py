@@ -335,6 +335,50 @@ def pin_mc_verify_law(orc):
     assert _chi2_ok(np.bincount(first, minlength=V), pr[0])
 
 
+def pin_relaxed_law(orc):
+    """Relaxed acceptance (the pages' Table 4 ablation: the ratio multiplied by
+    1 + tau): many copies of one tiny sequence give (accept length, emitted
+    token) with the exact law when every accept test uses
+    min(1, (1 + tau) p/q) and the correction stays normalize(max(0, p - q));
+    the reported ratios stay min(1, p/q).  The first ratio is below 1 even
+    relaxed, the second is clipped to 1 by the relaxation."""
+    V, L, T, tau = 3, 2, 1.0, 0.5
+    pp = [np.array([0.5, 0.3, 0.2]), np.array([0.4, 0.2, 0.4]), np.array([0.1, 0.6, 0.3])]
+    qq = [np.array([0.2, 0.5, 0.3]), np.array([0.5, 0.1, 0.4])]
+    x = [1, 0]
+    C = 40000
+    P = np.tile(np.log(np.stack(pp)).astype(np.float32), (C, 1))
+    Q = np.tile(np.log(np.stack(qq)).astype(np.float32), (C, 1))
+    offs = (np.arange(C + 1) * L).astype(np.int32)
+    tokens = np.tile(np.array(x, np.int32), C)
+    pr = [sp_softmax(r) for r in np.log(np.stack(pp)).astype(np.float32).astype(np.float64)]
+    qr = [sp_softmax(r) for r in np.log(np.stack(qq)).astype(np.float32).astype(np.float64)]
+    s1, s2 = pr[0][1] / qr[0][1], pr[1][0] / qr[1][0]
+    r1, r2 = min(1, (1 + tau) * s1), min(1, (1 + tau) * s2)
+    assert r1 < 1 and r2 == 1 and s2 < 1
+    out = orc.verify(P, Q, V, tokens, offs, np.full(C, T, np.float32), 77, 2, tau=tau)
+    a = out["accept_len"]
+    last = out["out_tokens"].reshape(C, L + 1)[np.arange(C), a]
+    w1 = np.maximum(pr[0] - qr[0], 0); w1 /= w1.sum()
+    w2 = np.maximum(pr[1] - qr[1], 0); w2 /= w2.sum()
+    probs = np.concatenate([(1 - r1) * w1, r1 * (1 - r2) * w2, r1 * r2 * pr[2]])
+    counts = np.bincount(a * V + last, minlength=3 * V)
+    assert _chi2_ok(counts, probs), (counts, probs * C)
+    assert np.allclose(out["ratio"].reshape(C, L)[0], [s1, s2], rtol=1e-6)
+    # tau = 0 is the strict step, bit for bit.
+    strict = orc.verify(P[:200 * (L + 1)], Q[:200 * L], V, tokens[:200 * L], offs[:201],
+                        np.full(200, T, np.float32), 77, 2)
+    relaxed0 = orc.verify(P[:200 * (L + 1)], Q[:200 * L], V, tokens[:200 * L], offs[:201],
+                          np.full(200, T, np.float32), 77, 2, tau=0.0)
+    for k in ("accept_len", "out_tokens", "ratio", "alpha"):
+        assert np.array_equal(strict[k], relaxed0[k])
+    # The relaxed ratio of one row pair, and the argmax indicator at T = 0.
+    assert math.isclose(orc.ratio_relaxed(np.log(pp[0]), np.log(qq[0]), 1.0, 1, tau),
+                        (1 + tau) * pp[0][1] / qq[0][1], rel_tol=1e-12)
+    assert orc.ratio_relaxed(np.log(pp[0]), np.log(qq[0]), 0.0, 0, 9.0) == 1.0
+    assert orc.ratio_relaxed(np.log(pp[0]), np.log(qq[0]), 0.0, 1, 9.0) == 0.0
+
+
 def pin_mc_propose_law(orc):
     """Proposals follow softmax(qnew/T) (inverse CDF with the PROPOSE
     uniforms); T = 0 gives the lowest-id argmax; accept_len < L gives no
@@ -446,5 +490,5 @@ ALL_PINS = [
     pin_philox_numpy, pin_uniform_layout, pin_softmax_library, pin_temperature_ratio,
     pin_tv_identity, pin_residual_known, pin_icdf_grid, pin_handworked, pin_greedy_planted,
     pin_p_equals_q, pin_lossless_enumeration, pin_mc_verify_law, pin_mc_propose_law,
-    pin_mc_step_independence, pin_alpha_mean, pin_bf16_decoding, pin_invalid_inputs,
+    pin_mc_step_independence, pin_alpha_mean, pin_bf16_decoding, pin_invalid_inputs, pin_relaxed_law,
 ]

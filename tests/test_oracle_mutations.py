@@ -23,8 +23,11 @@ MUTATIONS = {
     "residual fallback dropped": ("if (total == 0.0)\n", "if (0)\n"),
     "icdf boundary": ("if (c > t) { chosen = v; break; }", "if (c >= t) { chosen = v; break; }"),
     "icdf unscaled target": ("double t = u * S;", "double t = u;"),
-    "accept test reversed": ("accepted = u_accept[k - 1] < ratio[k - 1];",
-                             "accepted = u_accept[k - 1] > ratio[k - 1];"),
+    "accept test reversed": ("accepted = u_accept[k - 1] < racc;",
+                             "accepted = u_accept[k - 1] > racc;"),
+    "relaxation divides": ("fmin(1.0, (1.0 + tau) * exp(log_px - log_qx))",
+                           "fmin(1.0, exp(log_px - log_qx) / (1.0 + tau))"),
+    "relaxed ratio reported": ("        if (tau != 0.0)\n            racc", "        if (tau != 0.0)\n            ratio[k - 1] = racc"),
     "prefix not stopped": ("if (!accepted) break;", "if (!accepted) continue;"),
     "greedy accepts all": ("accepted = ratio[k - 1] == 1.0;", "accepted = 1;"),
     "alpha denominator": ("*alpha = sum / L;", "*alpha = sum / (L + 1);"),
