@@ -136,6 +136,24 @@ ISD_API isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_
                               int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * isd_verify_relaxed — isd_verify with the relaxed acceptance of the pages'
+ * ablation (experiments, Table 4: the acceptance ratio multiplied by 1 + tau).
+ * Each accept test becomes u_k < min(1, (1 + tau) p_k(x_k) / q_k(x_k)); the
+ * correction is still drawn from normalize(max(0, p_j - q_j)), and ratio and
+ * alpha still report the strict min(1, p_k(x_k)/q_k(x_k)).  Relaxation gives
+ * up exact preservation of the anchor distribution.  tau = 0 is isd_verify;
+ * T = 0 (greedy) is unaffected.  tau must be finite and >= 0
+ * (ISD_ERR_INVALID_ARG otherwise).  Every other argument as isd_verify; the
+ * two share a workspace size.
+ */
+ISD_API isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                                      isd_dtype dtype, int vocab, const int32_t* tokens,
+                                      const int32_t* seq_offsets, int num_seqs, int total_positions,
+                                      const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                                      int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace isd_propose needs for this batch shape. */
 ISD_API size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype);
 

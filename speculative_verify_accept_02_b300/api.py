@@ -86,7 +86,9 @@ class ProposeOut:
 def isd_verify(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, seq_offsets: torch.Tensor,
                temperature: torch.Tensor, seed: int = 0, offset: int = 0, *, vocab: Optional[int] = None,
                total: Optional[int] = None, out: Optional[VerifyOut] = None,
-               ws: Optional[torch.Tensor] = None, stream=None) -> VerifyOut:
+               ws: Optional[torch.Tensor] = None, stream=None, tau: float = 0.0) -> VerifyOut:
+    """isd_verify; tau > 0 calls isd_verify_relaxed (accept tests use
+    min(1, (1 + tau) p/q))."""
     device = p.device
     C = seq_offsets.numel() - 1
     total = _total(seq_offsets, total)
@@ -103,12 +105,16 @@ def isd_verify(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, seq_offse
     need = isd_verify_workspace_bytes(C, total, V, p.dtype)
     if ws is None:
         ws = workspace(need, device)
-    status = _lib.load().isd_verify(
-        pp, ldp, qp, ldq, _dtype_code(p), V, _int32(tokens, "tokens"), _int32(seq_offsets, "seq_offsets"),
-        C, total, _f32(temperature, "temperature"), int(seed), int(offset),
-        out.accept_len.data_ptr(), out.out_tokens.data_ptr(), out.ratio.data_ptr(), out.alpha.data_ptr(),
-        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
-    _lib.check("isd_verify", status)
+    head = (pp, ldp, qp, ldq, _dtype_code(p), V, _int32(tokens, "tokens"), _int32(seq_offsets, "seq_offsets"),
+            C, total, _f32(temperature, "temperature"), int(seed), int(offset))
+    tail = (out.accept_len.data_ptr(), out.out_tokens.data_ptr(), out.ratio.data_ptr(), out.alpha.data_ptr(),
+            ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
+    if tau == 0.0:
+        status = _lib.load().isd_verify(*head, *tail)
+        _lib.check("isd_verify", status)
+    else:
+        status = _lib.load().isd_verify_relaxed(*head, float(tau), *tail)
+        _lib.check("isd_verify_relaxed", status)
     return out
 
 

@@ -2,6 +2,7 @@
 // workspace layout, kernel launches.  No allocation, no synchronisation.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "../../include/isd.h"
@@ -122,13 +123,18 @@ size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab,
     return propose_layout(total_positions, isd::make_chunking(vocab, elem_bytes_of(dtype))).bytes;
 }
 
-isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
-                      isd_dtype dtype, int vocab, const int32_t* tokens,
-                      const int32_t* seq_offsets, int num_seqs, int total_positions,
-                      const float* temperature, uint64_t seed, uint64_t offset,
-                      int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+isd_status verify_impl(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                       isd_dtype dtype, int vocab, const int32_t* tokens,
+                       const int32_t* seq_offsets, int num_seqs, int total_positions,
+                       const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                       int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                       void* workspace, size_t workspace_bytes, void* stream) {
     if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return ISD_ERR_INVALID_ARG;
+    if (!(tau >= 0.0f) || !std::isfinite(tau)) return ISD_ERR_INVALID_ARG;
     if (num_seqs == 0) return ISD_OK;
     if (!p_logits || !q_logits || !tokens || !seq_offsets || !temperature || !accept_len ||
         !out_tokens || !ratio || !alpha || !workspace)
@@ -166,6 +172,7 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
     // while they fit in about a third of it.
     va.keep_first = 2.0 * num_seqs * vocab * esz <= kL2KeepBytes ? 1 : 0;
     va.seed = seed;
+    va.relax_log2 = tau > 0.0f ? std::log2(1.0f + tau) : 0.0f;
     va.offset = offset;
     va.ctl = reinterpret_cast<isd::VerifyCtl*>(ws + lay.ctl);
     va.seq_count = reinterpret_cast<int*>(ws + lay.seq_count);
@@ -184,6 +191,32 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
     if (gs != ISD_OK) return gs;
     if (isd::launch_verify(va, esz, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ISD_ERR_CUDA;
     return ISD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                      isd_dtype dtype, int vocab, const int32_t* tokens,
+                      const int32_t* seq_offsets, int num_seqs, int total_positions,
+                      const float* temperature, uint64_t seed, uint64_t offset,
+                      int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                       total_positions, temperature, seed, offset, 0.0f, accept_len, out_tokens, ratio, alpha,
+                       workspace, workspace_bytes, stream);
+}
+
+isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                              isd_dtype dtype, int vocab, const int32_t* tokens,
+                              const int32_t* seq_offsets, int num_seqs, int total_positions,
+                              const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                              int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                       total_positions, temperature, seed, offset, tau, accept_len, out_tokens, ratio, alpha,
+                       workspace, workspace_bytes, stream);
 }
 
 isd_status isd_propose(const void* qnew_logits, int64_t ld, isd_dtype dtype, int vocab,

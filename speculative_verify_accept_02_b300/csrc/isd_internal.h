@@ -114,6 +114,7 @@ struct VerifyArgs {
     int keep_first;   // 1: first-position rows of T > 0 sequences are kept in L2 for their tails
     uint64_t seed;
     uint64_t offset;
+    float relax_log2; // log2(1 + tau) of relaxed acceptance, 0 for strict
     VerifyCtl* ctl;
     int* seq_count;   // [C] main items finished
     int* tail_count;  // [C] tail tasks finished

@@ -287,7 +287,7 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         }
         return;
     }
-    float ratio = 0.0f, Mp = -INFINITY, Sp = 0.0f, Mq = -INFINITY, Sq = 0.0f;
+    float ratio = 0.0f, racc = 0.0f, Mp = -INFINITY, Sp = 0.0f, Mq = -INFINITY, Sq = 0.0f;
     int amax = INT_MAX;
     if (mine) {
         const float2* pp = a.part + static_cast<size_t>(2 * r) * a.nseg;
@@ -321,12 +321,16 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
             const float lp = __fmaf_rn(zp, c2, -Mp) - log2f(Sp);
             const float lq = __fmaf_rn(zq, c2, -Mq) - log2f(Sq);
             ratio = lq == -INFINITY ? 1.0f : fminf(1.0f, exp2f(lp - lq));
+            // Relaxed acceptance tests min(1, (1 + tau) p/q); the reported
+            // ratio stays the strict one.
+            racc = (lq == -INFINITY || a.relax_log2 == 0.0f) ? ratio : fminf(1.0f, exp2f(lp - lq + a.relax_log2));
         } else {
             ratio = x == amax ? 1.0f : 0.0f;
+            racc = ratio;
         }
     }
     bool acc = false;
-    if (mine) acc = T > 0.0f ? decision_uniform(a.seed, a.offset, i, lane + 1, kTagAccept) < ratio : ratio == 1.0f;
+    if (mine) acc = T > 0.0f ? decision_uniform(a.seed, a.offset, i, lane + 1, kTagAccept) < racc : ratio == 1.0f;
     const unsigned bits = __ballot_sync(0xffffffffu, acc);
     const int na = min(bits == 0xffffffffu ? 32 : __ffs(~bits) - 1, L);
     const float total = warp_sum(ratio);

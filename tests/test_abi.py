@@ -25,7 +25,7 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     names = declared_symbols()
-    for n in ("isd_verify", "isd_propose", "isd_alpha", "isd_verify_workspace_bytes",
+    for n in ("isd_verify", "isd_verify_relaxed", "isd_propose", "isd_alpha", "isd_verify_workspace_bytes",
               "isd_propose_workspace_bytes", "isd_status_string"):
         assert n in names
 
@@ -85,6 +85,23 @@ def test_verify_host_checks(lib):
     assert _verify(lib, q=FAKE + 8) == _lib.ISD_ERR_UNSUPPORTED
     assert _verify(lib, wsb=16) == _lib.ISD_ERR_WORKSPACE
     assert _verify(lib, ws=FAKE + 16) == _lib.ISD_ERR_WORKSPACE
+
+
+def _verify_relaxed(lib, tau, **kw):
+    args = dict(p=FAKE, ldp=1024, q=FAKE, ldq=1024, dtype=0, vocab=1024, tokens=FAKE, offs=FAKE,
+                C=2, total=4, temp=FAKE, seed=0, offset=0, tau=tau, acc=FAKE, out=FAKE, ratio=FAKE,
+                alpha=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return lib.isd_verify_relaxed(*args.values())
+
+
+def test_verify_relaxed_host_checks(lib):
+    """tau must be finite and >= 0; the other checks are isd_verify's."""
+    for bad in (-0.5, float("nan"), float("inf")):
+        assert _verify_relaxed(lib, bad) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify_relaxed(lib, 0.5, C=0) == _lib.ISD_OK
+    assert _verify_relaxed(lib, 0.5, p=FAKE + 2) == _lib.ISD_ERR_UNSUPPORTED
+    assert _verify_relaxed(lib, 0.5, wsb=16) == _lib.ISD_ERR_WORKSPACE
 
 
 def test_propose_and_alpha_host_checks(lib):

@@ -233,3 +233,29 @@ def test_all_accepted_largest_stride():
         ov = oracle.verify(workloads.host_logits(P), workloads.host_logits(Q), V, tokens.numpy(), offs, temps,
                            seed, offset)
         compare_verify(ov, gv, offs).check()
+
+
+@pytest.mark.parametrize("name,kw,tau", [("c64", dict(num_seqs=6), 0.5), ("highconc", dict(num_seqs=5), 1.0),
+                                          ("ragged", dict(num_seqs=12, vocab=3001), 0.25)])
+def test_relaxed_acceptance_parity(name, kw, tau):
+    """isd_verify_relaxed (the pages' relaxed-acceptance ablation, ratio x
+    (1 + tau)) against the oracle with the same tau; with the same uniforms a
+    relaxed accept length is never shorter than the strict one."""
+    batch = workloads.make(name, **kw)
+    h = host(batch)
+    b = batch.to("cuda")
+    rep = Report()
+    for seed, offset in ((0, 0), (7, 3)):
+        outs = {}
+        for t in (0.0, tau):
+            v = isd_verify(b.p, b.q, b.tokens, b.seq_offsets, b.temperature, seed, offset, vocab=b.vocab,
+                           total=b.total, tau=t)
+            torch.cuda.synchronize()
+            outs[t] = dict(accept_len=v.accept_len.cpu().numpy(), out_tokens=v.out_tokens.cpu().numpy(),
+                           ratio=v.ratio.cpu().numpy(), alpha=v.alpha.cpu().numpy())
+        ov = oracle.verify(h["p"], h["q"], batch.vocab, h["tokens"], h["offs"], h["temp"], seed, offset, tau=tau)
+        compare_verify(ov, outs[tau], h["offs"], report=rep)
+        assert np.all(outs[tau]["accept_len"] >= outs[0.0]["accept_len"])
+        assert np.array_equal(outs[tau]["ratio"], outs[0.0]["ratio"])
+    rep.check()
+    assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 20), rep
