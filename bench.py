@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--workload", default="c64", choices=["c64", "greedy", "highconc", "ragged"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--separate", action="store_true",
+                    help="time isd_verify then isd_propose (two launches) instead of isd_verify_propose")
     return ap.parse_args()
 
 
@@ -239,7 +241,9 @@ def run_ours(args):
     import torch.distributed as dist
 
     from speculative_verify_accept_02_b300 import (_lib, build, isd_propose, isd_propose_workspace_bytes,
-                                                   isd_verify, isd_verify_workspace_bytes, workloads)
+                                                   isd_verify, isd_verify_propose,
+                                                   isd_verify_propose_workspace_bytes, isd_verify_workspace_bytes,
+                                                   workloads)
     from speculative_verify_accept_02_b300.api import ProposeOut, VerifyOut, workspace
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -264,6 +268,8 @@ def run_ours(args):
     pout = ProposeOut(torch.empty(total, dtype=i32, device=dev), torch.empty(C, dtype=torch.uint8, device=dev))
     vws = workspace(isd_verify_workspace_bytes(C, total, V, batch.dtype), dev)
     pws = workspace(isd_propose_workspace_bytes(C, total, V, batch.dtype), dev)
+    fws = workspace(isd_verify_propose_workspace_bytes(C, total, V, batch.dtype), dev)
+    fused = not args.separate
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -275,11 +281,20 @@ def run_ours(args):
         isd_propose(b["qnew"], b["seq_offsets"], b["temperature"], batch.seed, batch.offset,
                     accept_len=vout.accept_len, vocab=V, total=total, out=pout, ws=pws, stream=stream)
 
+    def step(b):
+        """One step: the fused call (one launch), or the two calls."""
+        if fused:
+            isd_verify_propose(b["p"], b["q"], b["tokens"], b["qnew"], b["seq_offsets"], b["temperature"],
+                               batch.seed, batch.offset, vocab=V, total=total, out=vout, pout=pout, ws=fws,
+                               stream=stream)
+        else:
+            verify(b)
+            propose(b)
+
     names = ("p", "q", "qnew", "tokens", "seq_offsets", "temperature")
     resident = {n: getattr(batch, n) for n in names}
     for _ in range(max(3, args.warmup)):
-        verify(resident)
-        propose(resident)
+        step(resident)
     torch.cuda.synchronize(dev)
     vbytes, pbytes = algorithmic_bytes(batch, vout.accept_len.cpu().tolist(), pout.valid.cpu().tolist())
 
@@ -296,9 +311,13 @@ def run_ours(args):
         for k in range(K):
             flush.zero_()
             ev[k][0].record(stream)
-            verify(resident)
-            ev[k][1].record(stream)
-            propose(resident)
+            if fused:
+                step(resident)
+                ev[k][1].record(stream)
+            else:
+                verify(resident)
+                ev[k][1].record(stream)
+                propose(resident)
             ev[k][2].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
@@ -315,7 +334,10 @@ def run_ours(args):
     logit_gbs = (vbytes + pbytes) * world * K / (total_ms / 1e3) / 1e9
     peak, peak_kind = load_peaks()
     verify_avg_s = verify_ms / K / 1e3
-    achieved = vbytes / verify_avg_s / 1e9
+    # The roofline kernel is the verify kernel; fused, it also streams the
+    # qnew rows it draws proposals from.
+    kernel_bytes = vbytes + (pbytes if fused else 0)
+    achieved = kernel_bytes / verify_avg_s / 1e9
 
     # End to end through the public API: every step copies its inputs from
     # pinned host memory, runs, and reads every result back.
@@ -331,8 +353,7 @@ def run_ours(args):
         e2e_ev[k][0].record(stream)
         for n in names:
             dev_in[n].copy_(host_in[n], non_blocking=True)
-        verify(dev_in)
-        propose(dev_in)
+        step(dev_in)
         for hbuf, dbuf in zip(host_out, results):
             hbuf.copy_(dbuf, non_blocking=True)
         e2e_ev[k][1].record(stream)
@@ -357,15 +378,17 @@ def run_ours(args):
         "dtype": "f32", "data": "synthetic",
         "config": workload_config(batch, {
             "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write between timed steps",
-            "parallelism": f"replicas x{world}", "step": "isd_verify + isd_propose"}),
+            "parallelism": f"replicas x{world}", "step": "isd_verify_propose (one launch)" if fused else "isd_verify + isd_propose"}),
         "logit_gbs": logit_gbs, "hbm_frac": logit_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
-                     "kernel": "verify_kernel (isd_verify: one persistent launch)", "algorithmic_bytes": vbytes,
+                     "kernel": ("verify_kernel (isd_verify_propose: one persistent launch)" if fused
+                                else "verify_kernel (isd_verify: one persistent launch)"),
+                     "algorithmic_bytes": kernel_bytes,
                      "peak_source": f"{peak_kind} hbm_gbs", "avg_launch_us": verify_avg_s * 1e6},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * K,  # verify_kernel + propose_kernel per step
+        "gpu_launches": (1 if fused else 2) * K,  # verify_kernel (+ propose_kernel) per step
         "clocks": sampler.summary(),
         "wall_s_timed": t_wall,
     }

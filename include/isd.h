@@ -154,6 +154,35 @@ ISD_API isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const 
                                       int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of workspace isd_verify_propose needs for this batch shape. */
+ISD_API size_t isd_verify_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype);
+
+/*
+ * isd_verify_propose — one launch that does isd_verify_relaxed (tau = 0:
+ * isd_verify) and then isd_propose with this call's accept lengths: the
+ * fused step of Summary §3.2, where one forward verifies the pending
+ * proposals and its mask positions propose the next stride.  Proposals are
+ * drawn only for sequences that accept their whole stride (valid[i] = 1);
+ * the others get valid[i] = 0 and proposals -1, as isd_propose with
+ * accept_len_or_null does.  Every output equals that of the two separate
+ * calls on the same arguments (same uniforms); the proposal draws run inside
+ * the verify kernel, right after the decision that keeps them.
+ *
+ * Arguments: those of isd_verify_relaxed, then
+ * qnew_logits, ld_qnew  [total, ld_qnew] this forward's mask-position logits
+ *                       (layout of q), same dtype as p, 16-byte aligned base
+ * proposals [total] int32 out, valid [C] uint8 out
+ * workspace of at least isd_verify_propose_workspace_bytes() (the rules of
+ * every workspace), not shared with isd_verify calls in flight.
+ */
+ISD_API isd_status isd_verify_propose(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                                      isd_dtype dtype, int vocab, const int32_t* tokens,
+                                      const int32_t* seq_offsets, int num_seqs, int total_positions,
+                                      const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                                      int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                                      const void* qnew_logits, int64_t ld_qnew, int32_t* proposals,
+                                      uint8_t* valid, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace isd_propose needs for this batch shape. */
 ISD_API size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype);
 

@@ -5,4 +5,5 @@ marshals torch CUDA tensors into its C ABI.  ``workloads`` makes seeded
 synthetic inputs.
 """
 from .api import (ProposeOut, VerifyOut, isd_alpha, isd_propose, isd_propose_workspace_bytes,  # noqa: F401
-                  isd_verify, isd_verify_workspace_bytes, workspace)
+                  isd_verify, isd_verify_propose, isd_verify_propose_workspace_bytes, isd_verify_workspace_bytes,
+                  workspace)

@@ -118,6 +118,47 @@ def isd_verify(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, seq_offse
     return out
 
 
+def isd_verify_propose_workspace_bytes(num_seqs: int, total: int, vocab: int, dtype: torch.dtype) -> int:
+    return int(_lib.load().isd_verify_propose_workspace_bytes(num_seqs, total, vocab, _DTYPES[dtype]))
+
+
+def isd_verify_propose(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, qnew: torch.Tensor,
+                       seq_offsets: torch.Tensor, temperature: torch.Tensor, seed: int = 0, offset: int = 0, *,
+                       vocab: Optional[int] = None, total: Optional[int] = None, tau: float = 0.0,
+                       out: Optional[VerifyOut] = None, pout: Optional[ProposeOut] = None,
+                       ws: Optional[torch.Tensor] = None, stream=None):
+    """isd_verify_propose: verify and the next stride's proposals in one
+    launch.  Returns (VerifyOut, ProposeOut)."""
+    device = p.device
+    C = seq_offsets.numel() - 1
+    total = _total(seq_offsets, total)
+    V = p.shape[1] if vocab is None else int(vocab)
+    if p.dtype != q.dtype or qnew.dtype != p.dtype:
+        raise TypeError("p, q and qnew must share a dtype")
+    pp, ldp = _rows(p, "p")
+    qp, ldq = _rows(q, "q")
+    np_, ldn = _rows(qnew, "qnew")
+    if out is None:
+        out = VerifyOut(torch.empty(C, dtype=torch.int32, device=device),
+                        torch.empty(total + C, dtype=torch.int32, device=device),
+                        torch.empty(total, dtype=torch.float32, device=device),
+                        torch.empty(C, dtype=torch.float32, device=device))
+    if pout is None:
+        pout = ProposeOut(torch.empty(total, dtype=torch.int32, device=device),
+                          torch.empty(C, dtype=torch.uint8, device=device))
+    need = isd_verify_propose_workspace_bytes(C, total, V, p.dtype)
+    if ws is None:
+        ws = workspace(need, device)
+    status = _lib.load().isd_verify_propose(
+        pp, ldp, qp, ldq, _dtype_code(p), V, _int32(tokens, "tokens"), _int32(seq_offsets, "seq_offsets"),
+        C, total, _f32(temperature, "temperature"), int(seed), int(offset), float(tau),
+        out.accept_len.data_ptr(), out.out_tokens.data_ptr(), out.ratio.data_ptr(), out.alpha.data_ptr(),
+        np_, ldn, pout.proposals.data_ptr(), pout.valid.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
+    _lib.check("isd_verify_propose", status)
+    return out, pout
+
+
 def isd_propose(qnew: torch.Tensor, seq_offsets: torch.Tensor, temperature: torch.Tensor,
                 seed: int = 0, offset: int = 0, accept_len: Optional[torch.Tensor] = None, *,
                 vocab: Optional[int] = None, total: Optional[int] = None,

@@ -53,29 +53,34 @@ VerifyPlan verify_plan(int vocab, int esz) {
 }
 
 struct VerifyLayout {
-    size_t ctl, seq_count, tail_count, tails, tasks, task_ready, part, tpart, bytes;
+    size_t ctl, seq_count, seq_pending, tail_count, tails, tasks, task_ready, part, tpart, bytes;
 };
 
-VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl) {
+// Tails: one per sequence (its correction or bonus), plus one per qnew row
+// when the call also draws the next proposals.
+VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl, bool fused) {
     VerifyLayout l;
     const size_t C = static_cast<size_t>(num_seqs);
+    const size_t NT = C + (fused ? static_cast<size_t>(total) : 0);
     size_t off = 0;
     l.ctl = off;
     off = align_up(off + sizeof(isd::VerifyCtl));
     l.seq_count = off;
     off = align_up(off + sizeof(int) * C);
-    l.tail_count = off;
+    l.seq_pending = off;
     off = align_up(off + sizeof(int) * C);
+    l.tail_count = off;
+    off = align_up(off + sizeof(int) * NT);
     l.tails = off;
-    off = align_up(off + sizeof(isd::SeqTail) * C);
+    off = align_up(off + sizeof(isd::SeqTail) * NT);
     l.tasks = off;
-    off = align_up(off + 2 * sizeof(int4) * C * pl.ntask);
+    off = align_up(off + 2 * sizeof(int4) * NT * pl.ntask);
     l.task_ready = off;
-    off = align_up(off + sizeof(int) * C * pl.ntask);
+    off = align_up(off + sizeof(int) * NT * pl.ntask);
     l.part = off;
     off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * pl.nseg);
     l.tpart = off;
-    off = align_up(off + sizeof(float2) * C * pl.nt * 8);  // 8 consumer-warp slices per tail sub-chunk
+    off = align_up(off + sizeof(float2) * NT * pl.nt * 8);  // 8 consumer-warp slices per tail sub-chunk
     l.bytes = off;
     return l;
 }
@@ -115,7 +120,12 @@ extern "C" {
 
 size_t isd_verify_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
     if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return 0;
-    return verify_layout(num_seqs, total_positions, verify_plan(vocab, elem_bytes_of(dtype))).bytes;
+    return verify_layout(num_seqs, total_positions, verify_plan(vocab, elem_bytes_of(dtype)), false).bytes;
+}
+
+size_t isd_verify_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
+    if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return 0;
+    return verify_layout(num_seqs, total_positions, verify_plan(vocab, elem_bytes_of(dtype)), true).bytes;
 }
 
 size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
@@ -132,7 +142,9 @@ isd_status verify_impl(const void* p_logits, int64_t ld_p, const void* q_logits,
                        const int32_t* seq_offsets, int num_seqs, int total_positions,
                        const float* temperature, uint64_t seed, uint64_t offset, float tau,
                        int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                       const void* qnew_logits, int64_t ld_qnew, int32_t* proposals, uint8_t* valid,
                        void* workspace, size_t workspace_bytes, void* stream) {
+    const bool fused = qnew_logits != nullptr || proposals != nullptr || valid != nullptr;
     if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return ISD_ERR_INVALID_ARG;
     if (!(tau >= 0.0f) || !std::isfinite(tau)) return ISD_ERR_INVALID_ARG;
     if (num_seqs == 0) return ISD_OK;
@@ -140,11 +152,13 @@ isd_status verify_impl(const void* p_logits, int64_t ld_p, const void* q_logits,
         !out_tokens || !ratio || !alpha || !workspace)
         return ISD_ERR_INVALID_ARG;
     if (ld_p < vocab || ld_q < vocab) return ISD_ERR_INVALID_ARG;
-    if (!aligned16(p_logits) || !aligned16(q_logits)) return ISD_ERR_UNSUPPORTED;
+    if (fused && (!qnew_logits || !proposals || !valid || ld_qnew < vocab)) return ISD_ERR_INVALID_ARG;
+    if (!aligned16(p_logits) || !aligned16(q_logits) || (fused && !aligned16(qnew_logits)))
+        return ISD_ERR_UNSUPPORTED;
     const int esz = elem_bytes_of(dtype);
     const VerifyPlan pl = verify_plan(vocab, esz);
     if (pl.nt > isd::kMaxTailChunks) return ISD_ERR_UNSUPPORTED;
-    const VerifyLayout lay = verify_layout(num_seqs, total_positions, pl);
+    const VerifyLayout lay = verify_layout(num_seqs, total_positions, pl, fused);
     if (workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
         return ISD_ERR_WORKSPACE;
     char* ws = static_cast<char*>(workspace);
@@ -176,6 +190,13 @@ isd_status verify_impl(const void* p_logits, int64_t ld_p, const void* q_logits,
     va.offset = offset;
     va.ctl = reinterpret_cast<isd::VerifyCtl*>(ws + lay.ctl);
     va.seq_count = reinterpret_cast<int*>(ws + lay.seq_count);
+    va.seq_pending = reinterpret_cast<int*>(ws + lay.seq_pending);
+    va.n_tail = num_seqs + (fused ? total_positions : 0);
+    va.fused = fused ? 1 : 0;
+    va.qnew = static_cast<const char*>(qnew_logits);
+    va.ldqnew_bytes = ld_qnew * esz;
+    va.proposals = proposals;
+    va.valid = valid;
     va.tail_count = reinterpret_cast<int*>(ws + lay.tail_count);
     va.tails = reinterpret_cast<isd::SeqTail*>(ws + lay.tails);
     va.tasks = reinterpret_cast<int4*>(ws + lay.tasks);
@@ -205,7 +226,7 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
                       void* workspace, size_t workspace_bytes, void* stream) {
     return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
                        total_positions, temperature, seed, offset, 0.0f, accept_len, out_tokens, ratio, alpha,
-                       workspace, workspace_bytes, stream);
+                       nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
 }
 
 isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
@@ -216,7 +237,20 @@ isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_
                               void* workspace, size_t workspace_bytes, void* stream) {
     return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
                        total_positions, temperature, seed, offset, tau, accept_len, out_tokens, ratio, alpha,
-                       workspace, workspace_bytes, stream);
+                       nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+isd_status isd_verify_propose(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                              isd_dtype dtype, int vocab, const int32_t* tokens,
+                              const int32_t* seq_offsets, int num_seqs, int total_positions,
+                              const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                              int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                              const void* qnew_logits, int64_t ld_qnew, int32_t* proposals, uint8_t* valid,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    if (!qnew_logits || !proposals || !valid) return ISD_ERR_INVALID_ARG;
+    return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                       total_positions, temperature, seed, offset, tau, accept_len, out_tokens, ratio, alpha,
+                       qnew_logits, ld_qnew, proposals, valid, workspace, workspace_bytes, stream);
 }
 
 isd_status isd_propose(const void* qnew_logits, int64_t ld, isd_dtype dtype, int vocab,

@@ -77,18 +77,28 @@ struct VerifyCtl {
 // Tail kinds: which row(s) the work after a decision reads.
 enum TailMode : int {
     kTailRes = 2,   // T > 0, rejection: residual max(0, p_j - q_j) over row pair j
-    kTailSoft = 3   // T > 0, all accepted: softmax of the final anchor p_{L+1}
+    kTailSoft = 3,  // T > 0: softmax draw from one row (bonus from p_{L+1}, or a proposal)
+    kTailArg = 4    // T = 0: argmax of one row (a proposal)
 };
+// Flag on a tail mode: its row is a qnew row (a proposal draw of the fused
+// verify-and-propose call), not a p row.
+constexpr int kTailQnew = 8;
 
 // What a sequence's tail needs, written by its decision (48 bytes).
+// What a tail (one draw after a decision) needs: written by the decision,
+// read by the tail's producers and its selection (48 bytes).
 struct alignas(16) SeqTail {
-    int mode;
-    int a;            // accept length
-    int prow, qrow;   // tail rows in p and in q
+    int mode;         // TailMode, with kTailQnew for a proposal row
+    int a;            // accept length of the sequence
+    int prow, qrow;   // rows: p_j (or p_{L+1}, or the qnew row) and q_j
     float c2;         // log2(e) / T
     float nz0;        // p_j: log2 of its normaliser, p_j(v) = exp2(x_v c2 - nz0)
     float nz1;        // q_j: the same
-    float pad[5];
+    int seq;          // the sequence
+    int pos;          // position of the draw's uniform (1-based)
+    int tag;          // the uniform's purpose (CORRECT, BONUS or PROPOSE)
+    int dest;         // >= 0: out_tokens slot; < 0: proposals slot -1 - dest
+    int pad;
 };
 
 struct VerifyArgs {
@@ -117,13 +127,24 @@ struct VerifyArgs {
     float relax_log2; // log2(1 + tau) of relaxed acceptance, 0 for strict
     VerifyCtl* ctl;
     int* seq_count;   // [C] main items finished
-    int* tail_count;  // [C] tail tasks finished
-    SeqTail* tails;   // [C]
-    int4* tasks;      // [C * ntask][2] task records in reservation order:
-                      // {sequence, task, mode, p row}, {q row, c2, nz0, nz1}
-    int* task_ready;  // [C * ntask] 1 once the slot's task is published
+    // Tails are indexed by tail id: sequence i's correction or bonus is tail
+    // i; with `fused`, the proposal draw of qnew row r is tail C + r.
+    int n_tail;       // C, or C + total when fused
+    int* tail_count;  // [n_tail] tail tasks finished
+    SeqTail* tails;   // [n_tail]
+    int4* tasks;      // [n_tail * ntask][2] task records in reservation order:
+                      // {tail id, task, mode, row}, {q row, c2, nz0, nz1}
+    int* task_ready;  // [n_tail * ntask] 1 once the slot's task is published
     float2* part;     // [2 * total * nseg] per (row slot, segment) partials
-    float2* tpart;    // [C * nt * 8] per (tail sub-chunk, consumer warp) slice partials
+    float2* tpart;    // [n_tail * nt * 8] per (tail sub-chunk, consumer warp) slice partials
+    int* seq_pending; // [C] draws of the sequence still to finish
+    // The fused call (isd_verify_propose): the next stride's proposals of the
+    // sequences that accept their whole stride, drawn from qnew rows.
+    int fused;
+    const char* qnew;
+    int64_t ldqnew_bytes;
+    int32_t* proposals;
+    uint8_t* valid;
     int32_t* accept_len;
     int32_t* out_tokens;
     float* ratio;

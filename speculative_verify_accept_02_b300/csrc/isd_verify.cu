@@ -213,10 +213,13 @@ __device__ void write_invalid(const VerifyArgs& a, int i, const SeqInfo& s, int 
     if (s.in_range) {
         for (int m = lane; m <= s.len; m += 32) a.out_tokens[s.start + i + m] = -1;
         for (int k = lane; k < s.len; k += 32) a.ratio[s.start + k] = NAN;
+        if (a.fused)
+            for (int k = lane; k < s.len; k += 32) a.proposals[s.start + k] = -1;
     }
     if (lane == 0) {
         a.accept_len[i] = code;
         a.alpha[i] = NAN;
+        if (a.fused) a.valid[i] = 0;
     }
 }
 
@@ -346,11 +349,20 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         a.accept_len[i] = na;
         a.alpha[i] = total / static_cast<float>(L);
     }
+    // The fused call draws the next stride's proposals of a sequence that
+    // accepts its whole stride (the others' would be discarded).
+    const bool props = a.fused && na == L;
+    if (a.fused) {
+        if (lane == 0) a.valid[i] = props ? 1 : 0;
+        if (!props)
+            for (int m = lane; m < L; m += 32) a.proposals[s.start + m] = -1;
+    }
+    int tok = -1;  // greedy: the token, known now
     if (T == 0.0f) {
         // Greedy: the correction is the argmax of p_j, already known; the
         // bonus is the argmax of p_{L+1}, streamed in the last position's q
         // slot.
-        int tok = amax_j;
+        tok = amax_j;
         if (na == L) {
             const float2* pb = a.part + static_cast<size_t>(2 * (s.start + L - 1) + 1) * a.nseg;
             float M = -INFINITY;
@@ -362,47 +374,77 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
             warp_merge_arg(M, I);
             tok = I;
         }
+        if (lane == 0) a.out_tokens[s.start + i + na] = tok;
+    }
+    // Tails: the correction or bonus draw (T > 0), then one per proposal row.
+    const int n_tok = T > 0.0f ? 1 : 0;
+    const int n_pub = n_tok + (props ? L : 0);
+    if (n_pub == 0) {
         if (lane == 0) {
-            a.out_tokens[s.start + i + na] = tok;
             a.seq_count[i] = 0;
             finalize(a);
         }
         return;
     }
-    // Every task record carries what its producer needs, so that taking a
-    // task is one round trip.
-    const int mode = na < L ? kTailRes : kTailSoft;
-    const int prow = s.start + i + na;  // p_j, or p_{L+1} when na == L
-    const int qrow = s.start + na;
+    const int mode_tok = na < L ? kTailRes : kTailSoft;
+    const int mode_prop = (T > 0.0f ? kTailSoft : kTailArg) | kTailQnew;
     float nz0 = 0.0f, nz1 = 0.0f;
     if (na < L) {
         nz0 = __fadd_rn(mc0, log2f(sp0));
         nz1 = __fadd_rn(mc1, log2f(sq0));
     }
+    // Tail record k of this decision (k < n_tok: the token; else proposal
+    // row k - n_tok): its tail id and what its producers and selection need.
+    auto tail_of = [&](int k, SeqTail& t) -> int {
+        t = SeqTail{};
+        t.seq = i;
+        t.a = na;
+        t.c2 = c2;
+        if (k < n_tok) {
+            t.mode = mode_tok;
+            t.prow = s.start + i + na;  // p_j, or p_{L+1} when na == L
+            t.qrow = s.start + na;
+            t.nz0 = nz0;
+            t.nz1 = nz1;
+            t.pos = na + 1;
+            t.tag = na < L ? kTagCorrect : kTagBonus;
+            t.dest = s.start + i + na;
+            return i;
+        }
+        const int row = s.start + (k - n_tok);  // qnew row of position m = k - n_tok + 1
+        t.mode = mode_prop;
+        t.prow = row;
+        t.pos = k - n_tok + 1;
+        t.tag = kTagPropose;
+        t.dest = -1 - row;
+        return a.num_seqs + row;
+    };
     int base = 0;
     if (lane == 0) {
-        SeqTail t = {};
-        t.mode = mode;
-        t.a = na;
-        t.prow = prow;
-        t.qrow = qrow;
-        t.c2 = c2;
-        t.nz0 = nz0;
-        t.nz1 = nz1;
-        a.tails[i] = t;
+        a.seq_pending[i] = n_pub;
         a.seq_count[i] = 0;
-        base = atomicAdd(&a.ctl->tail_reserve, a.ntask);
+        base = atomicAdd(&a.ctl->tail_reserve, n_pub * a.ntask);
     }
     base = __shfl_sync(0xffffffffu, base, 0);
-    for (int y = lane; y < a.ntask; y += 32) {
-        int4* tr = a.tasks + 2 * static_cast<size_t>(base + y);
-        tr[0] = make_int4(i, y, mode, prow);
-        tr[1] = make_int4(qrow, __float_as_int(c2), __float_as_int(nz0), __float_as_int(nz1));
+    for (int k = lane; k < n_pub; k += 32) {
+        SeqTail t;
+        const int id = tail_of(k, t);
+        a.tails[id] = t;
+    }
+    // Every task record carries what its producer needs, so that taking a
+    // task is one round trip.
+    for (int e = lane; e < n_pub * a.ntask; e += 32) {
+        const int k = e / a.ntask, y = e - k * a.ntask;
+        SeqTail t;
+        const int id = tail_of(k, t);
+        int4* tr = a.tasks + 2 * static_cast<size_t>(base + e);
+        tr[0] = make_int4(id, y, t.mode, t.prow);
+        tr[1] = make_int4(t.qrow, __float_as_int(t.c2), __float_as_int(t.nz0), __float_as_int(t.nz1));
     }
     // Tail state and tasks are visible before any task is flagged ready.
     __threadfence();
     __syncwarp();
-    for (int y = lane; y < a.ntask; y += 32) st_volatile(a.task_ready + base + y, 1);
+    for (int e = lane; e < n_pub * a.ntask; e += 32) st_volatile(a.task_ready + base + e, 1);
 }
 
 // Selection of sequence i's token from its tail partials (one warp).  The
@@ -423,16 +465,38 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
     for (int u = lane; u < U / 2; u += 32) cp_async16(ts + u, tp + u);
     cp_async_wait_all();
     SeqTail t;
-    t.mode = __shfl_sync(0xffffffffu, tv.x, 0);
+    const int mode_flags = __shfl_sync(0xffffffffu, tv.x, 0);
+    t.mode = mode_flags & ~kTailQnew;
     t.a = __shfl_sync(0xffffffffu, tv.y, 0);
     t.prow = __shfl_sync(0xffffffffu, tv.z, 0);
     t.qrow = __shfl_sync(0xffffffffu, tv.w, 0);
     t.c2 = __int_as_float(__shfl_sync(0xffffffffu, tv.x, 1));
     t.nz0 = __int_as_float(__shfl_sync(0xffffffffu, tv.y, 1));
     t.nz1 = __int_as_float(__shfl_sync(0xffffffffu, tv.z, 1));
+    t.seq = __shfl_sync(0xffffffffu, tv.w, 1);
+    t.pos = __shfl_sync(0xffffffffu, tv.x, 2);
+    t.tag = __shfl_sync(0xffffffffu, tv.y, 2);
+    t.dest = __shfl_sync(0xffffffffu, tv.z, 2);
     __syncwarp();
-    const SeqInfo s = seq_lookup(a, sm, i);
-    const int out_slot = s.start + i + t.a;
+    // The draw is written to its slot; the sequence is final with its last draw.
+    auto finish = [&](int token) {
+        if (lane == 0) {
+            if (t.dest >= 0)
+                a.out_tokens[t.dest] = token;
+            else
+                a.proposals[-1 - t.dest] = token;
+            a.tail_count[i] = 0;
+            if (atomicSub(a.seq_pending + t.seq, 1) == 1) finalize(a);
+        }
+    };
+    if (t.mode == kTailArg) {  // greedy proposal: merge the slice argmaxes
+        float M = -INFINITY;
+        int I = INT_MAX;
+        for (int u = lane; u < U; u += 32) merge_argmax(M, I, sm.tsel[fi][u].x, __float_as_int(sm.tsel[fi][u].y));
+        warp_merge_arg(M, I);
+        finish(I);
+        return;
+    }
     // Slice weights in one scale, the target u * total, and its slice.  Lane
     // l owns the consecutive slices [l * ub, (l + 1) * ub): the lanes reduce
     // their blocks locally and meet in one scan, so the pass costs a handful
@@ -453,8 +517,7 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
         if (t.mode == kTailSoft) return v.x == -INFINITY ? 0.0f : v.y * ex2_approx(v.x - MC);
         return fallback ? v.y : v.x;
     };
-    const float rnd = t.mode == kTailSoft ? decision_uniform(a.seed, a.offset, i, s.len + 1, kTagBonus)
-                                          : decision_uniform(a.seed, a.offset, i, t.a + 1, kTagCorrect);
+    const float rnd = decision_uniform(a.seed, a.offset, t.seq, t.pos, t.tag);
     float own = 0.0f;
     int lpos = -1;  // the lane's last slice with positive weight
     for (int u = u_lo; u < u_hi; ++u) {
@@ -502,7 +565,8 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
     tail_slice<E>(nc, w, sb, se);
     const int lo = c * a.ckt + sb;
     const int len = se - sb;
-    const char* prow = a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
+    const char* prow = (mode_flags & kTailQnew) ? a.qnew + static_cast<int64_t>(t.prow) * a.ldqnew_bytes
+                                                : a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
     const char* qrow = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes;
     constexpr int kVec = 16 / E;
     constexpr int kPer = 2 * kVec;  // ids per lane: at most two 16-byte vectors
@@ -596,12 +660,7 @@ __device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int l
         found = __shfl_sync(0xffffffffu, found, owner);
     }
     const int last = warp_max_int(lp);
-    if (lane == 0) {
-        const int v = found >= 0 ? found : (last >= 0 ? last : 0);
-        a.out_tokens[out_slot] = lo + v;
-        a.tail_count[i] = 0;
-        finalize(a);
-    }
+    finish(lo + (found >= 0 ? found : (last >= 0 ? last : 0)));
 }
 
 // Hand a decision or selection to the finisher warp (lane 0 of the bookkeeper).
@@ -793,7 +852,7 @@ __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
     st_volatile(a.task_ready + slot, 0);
     const int4 w0 = __ldcg(a.tasks + 2 * static_cast<size_t>(slot)), w1 = __ldcg(a.tasks + 2 * static_cast<size_t>(slot) + 1);
     const int i = w0.x, y = w0.y;
-    wk.kind = w0.z;
+    wk.kind = w0.z & ~kTailQnew;
     wk.seq = i;
     wk.slot = 0;
     wk.seg = 0;
@@ -804,7 +863,8 @@ __device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
     wk.c2 = __int_as_float(w1.y);
     wk.nz0 = __int_as_float(w1.z);
     wk.nz1 = __int_as_float(w1.w);
-    wk.row0 = a.p + static_cast<int64_t>(w0.w) * a.ldp_bytes;
+    wk.row0 = (w0.z & kTailQnew) ? a.qnew + static_cast<int64_t>(w0.w) * a.ldqnew_bytes
+                                 : a.p + static_cast<int64_t>(w0.w) * a.ldp_bytes;
     wk.row1 = a.q + static_cast<int64_t>(w1.x) * a.ldq_bytes;
 }
 
@@ -816,7 +876,7 @@ __device__ void scheduler(const VerifyArgs& a, SmemV& sm, unsigned long long nex
     // task to the issuer through a priority slot as soon as a decision
     // publishes it, ahead of the main items already queued.  Every global
     // round trip is issued one pass before its result is looked at.
-    const int cap = a.num_seqs * a.ntask;
+    const int cap = a.n_tail * a.ntask;
     bool tickets_left = cap > 0;
     int ticket = -1, claim = 0, flag = 0;
     bool claim_pending = false, claim_started = false;
@@ -1276,7 +1336,7 @@ __device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int s
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
         part = make_float2(warp_sum(sws), warp_sum(sps));
-    } else {  // kTailSoft
+    } else if (d.kind == kTailSoft) {
         float mt = -INFINITY, st = 0.0f;
         if (vec) {
             mt = fmaxf(vec_max<E>(A0), vec_max<E>(A1));
@@ -1302,6 +1362,39 @@ __device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int s
         float M = mt == -INFINITY ? -INFINITY : mt * d.c2, S = st;
         warp_merge_mc(M, S);
         part = make_float2(M, S);
+    } else {  // kTailArg: the lane's first maximum in id order
+        float mt = -INFINITY;
+        int it = INT_MAX;
+        if (vec) {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float x = vec_elem<E>(A0, j);
+                if (v0 < ve && x > mt) {
+                    mt = x;
+                    it = d.e0 + v0 * kVec + j;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float x = vec_elem<E>(A1, j);
+                if (v1 < ve && x > mt) {
+                    mt = x;
+                    it = d.e0 + v1 * kVec + j;
+                }
+            }
+        } else {
+            for (int e = wb + lane; e < we; e += 32) {
+                const float x = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
+                if (x > mt) {
+                    mt = x;
+                    it = d.e0 + e;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+        warp_merge_arg(mt, it);
+        part = make_float2(mt, __int_as_float(it));
     }
     push_record(a, sm, nrec, warp, lane, part, d.kind, d.flags, d.seq, d.slot, 0, 0);
 }
@@ -1419,7 +1512,10 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
         if (atomicAdd(&a.ctl->exited, 1) == static_cast<int>(gridDim.x) - 1) {
             __threadfence();
             if (ld_volatile(&a.ctl->err) != 0)
-                for (int i = 0; i < a.num_seqs; ++i) a.accept_len[i] = -2;
+                for (int i = 0; i < a.num_seqs; ++i) {
+                    a.accept_len[i] = -2;
+                    if (a.fused) a.valid[i] = 0;
+                }
             a.ctl->grab = 0;
             a.ctl->tail_reserve = 0;
             a.ctl->tail_claim = 0;

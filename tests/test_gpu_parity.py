@@ -259,3 +259,35 @@ def test_relaxed_acceptance_parity(name, kw, tau):
         assert np.array_equal(outs[tau]["ratio"], outs[0.0]["ratio"])
     rep.check()
     assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 20), rep
+
+
+FUSED = [("c64", dict(num_seqs=5)), ("greedy", dict(num_seqs=9)), ("highconc", dict(num_seqs=5)),
+         ("ragged", dict(num_seqs=16)), ("ragged", dict(num_seqs=24, vocab=1537, dtype=torch.float32)),
+         ("tiny", dict(num_seqs=6, vocab=5)), ("c64", dict(num_seqs=3, stride=32, vocab=4099))]
+
+
+@pytest.mark.parametrize("name,kw", FUSED, ids=[f"{n}-{i}" for i, (n, _) in enumerate(FUSED)])
+def test_fused_verify_propose_parity(name, kw):
+    """isd_verify_propose (the fused step of Summary §3.2) against the oracle's
+    verify and its propose with the same accept lengths."""
+    from speculative_verify_accept_02_b300 import isd_verify_propose
+    batch = workloads.make(name, **kw)
+    h = host(batch)
+    b = batch.to("cuda")
+    rep = Report()
+    for seed, offset in ((0, 0), (7, 3)):
+        v, pr = isd_verify_propose(b.p, b.q, b.tokens, b.qnew, b.seq_offsets, b.temperature, seed, offset,
+                                   vocab=b.vocab, total=b.total)
+        torch.cuda.synchronize()
+        gv = dict(accept_len=v.accept_len.cpu().numpy(), out_tokens=v.out_tokens.cpu().numpy(),
+                  ratio=v.ratio.cpu().numpy(), alpha=v.alpha.cpu().numpy())
+        gp = dict(proposals=pr.proposals.cpu().numpy(), valid=pr.valid.cpu().numpy())
+        ov = oracle.verify(h["p"], h["q"], batch.vocab, h["tokens"], h["offs"], h["temp"], seed, offset)
+        compare_verify(ov, gv, h["offs"], report=rep)
+        agree = [i for i in range(batch.num_seqs) if ov["accept_len"][i] == gv["accept_len"][i]]
+        op = oracle.propose(h["qnew"], batch.vocab, h["offs"], h["temp"], seed, offset,
+                            accept_len=gv["accept_len"])
+        compare_propose(op, gp, h["offs"], seqs=agree, report=rep)
+        assert np.array_equal(gp["valid"], (gv["accept_len"] == np.diff(h["offs"])).astype(np.uint8))
+    rep.check()
+    assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 20), rep
