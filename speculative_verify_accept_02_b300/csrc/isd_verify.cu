@@ -2,31 +2,36 @@
 // ("Introspective Diffusion Language Models | Summary", §2 acceptance rate,
 // §3.2 strict acceptance, residual correction and bonus token, §3.3 online
 // softmax over the vocabulary and a common acceptance path free of
-// correction work).
+// correction work), optionally with the next stride's proposal draws of the
+// fused step (§3.2: one forward verifies and proposes).
 //
 // Work is handed out dynamically, in sequence order, by a global counter:
-//   main item   one segment (four 16 KB sub-chunks) of one p_k or q_k row.
+//   main item   one segment (up to eight 16 KB sub-chunks) of one p_k or q_k
+//               row; greedy sequences stream their final anchor p_{L+1} in
+//               place of their (unread) last q row.
 //   decision    once a sequence's last item is done: ratio_k =
 //               min(1, p_k(x_k) / q_k(x_k)), alpha, the accept prefix
-//               (Philox uniforms, one warp ballot) and the emitted prefix.  A
-//               greedy rejection is complete here (argmax of p_j).
-//   tail task   otherwise the decision publishes tail tasks on a device queue:
-//               the residual max(0, p_j - q_j) of the one rejected row pair,
-//               or the final anchor row p_{L+1}.  Producers take queued tail
-//               tasks before new main items, so the rejected rows are re-read
-//               while they are still in L2.
-//   selection   once a sequence's last tail task is done: the token by
-//               inverse CDF, the sub-chunk from the tail partials, then an
-//               in-order scan of that one sub-chunk.
+//               (Philox uniforms, one warp ballot; relaxed acceptance tests
+//               min(1, (1 + tau) p/q)) and the emitted prefix.  A greedy
+//               correction or bonus is complete here (argmaxes of the
+//               partials).
+//   tail task   otherwise the decision publishes tails on a device queue: the
+//               residual max(0, p_j - q_j) of the one rejected row pair, or
+//               the final anchor row p_{L+1}; in the fused call also one per
+//               qnew row of a sequence that accepted its whole stride.
+//               Producers take queued tail tasks before new main items.
+//   selection   once a tail's last task is done: the draw by inverse CDF, a
+//               slice of about 500 ids from the tail partials, then an
+//               in-order scan of that one slice (an argmax merge at T = 0).
 //
 // Warp roles of a CTA:
 //   scheduler   (one thread) takes work: the next main item from the global
 //               counter into a 2-entry work ring, a published tail task into
 //               a priority slot; it absorbs every global memory round trip;
 //   issuer      (one thread) streams the scheduled sub-chunks into a 4-stage
-//               shared-memory ring with 1-D bulk copies, serving the priority
-//               slot between any two sub-chunks; it never waits on global
-//               memory;
+//               shared-memory ring with 1-D bulk copies under L2 eviction
+//               policies, serving the priority slot between any two
+//               sub-chunks; it never waits on global memory;
 //   consumers   (8 warps) fold each stage into per-thread online softmax
 //               partials (packed bf16 maxima, packed fp32 FMAs, one ex2 per
 //               logit) or an exact argmax; at the end of an item every warp
