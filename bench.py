@@ -18,6 +18,8 @@ this step) on a bounded sample of the same workload, on the host cores.
 import argparse
 import hashlib
 import json
+
+import numpy as np
 import os
 import statistics
 import subprocess
@@ -29,6 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified stride-positions/sec and logit GB/s (% of B300 HBM peak), C=64 V=151936"
 UNIT = "positions/s"
+REFERENCE_BUDGET_S = 120.0  # seconds for a whole --impl reference run
 FALLBACK_HBM_GBS = 6400.0
 L2_FLUSH_BYTES = 256 << 20
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
@@ -226,26 +229,63 @@ def time_oracle(batch, seconds):
     return positions * reps / el, oracle.threads(), reps, el, positions
 
 
+def _sample_batch(batch, seqs, kp):
+    """A sub-batch of the workload: sequences `seqs`, each cut to its first kp
+    positions (a shorter stride; its anchor rows p_1..p_{kp+1} are the
+    sequence's own)."""
+    import torch
+    from speculative_verify_accept_02_b300 import workloads
+    o = batch.seq_offsets.tolist()
+    prow, qrow, Ls = [], [], []
+    for i in seqs:
+        L = min(kp, o[i + 1] - o[i])
+        prow += [o[i] + i + k for k in range(L + 1)]
+        qrow += [o[i] + k for k in range(L)]
+        Ls.append(L)
+    offs = torch.tensor([0] + list(np.cumsum(Ls)), dtype=torch.int32)
+    sub = workloads.Batch(batch.name, batch.vocab, batch.ld, batch.dtype, offs, batch.temperature[seqs].clone(),
+                          batch.tokens[qrow].clone(), batch.p[prow].clone(), batch.q[qrow].clone(),
+                          batch.qnew[qrow].clone(), batch.seed, batch.offset, dict(batch.meta))
+    return sub, sum(Ls)
+
+
 def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return  # the oracle runs once, on rank 0
     import oracle
     from speculative_verify_accept_02_b300 import workloads
     batch = workloads.make(args.workload, device="cpu")
-    sample = list(range(0, batch.num_seqs, max(1, batch.num_seqs // 8)))[:8]
-    Ls = batch.strides()
-    positions = sum(Ls[i] for i in sample)
-    h = _host_inputs(batch)
+    # The sample per step is sized so that the whole run (warm-up and timed
+    # steps) takes about REFERENCE_BUDGET_S: up to 8 whole sequences, or one
+    # sequence cut to fewer positions when a whole one is already too slow.
+    one, _ = _sample_batch(batch, [0], 1 << 30)
+    h1 = _host_inputs(one)
+    t0 = time.perf_counter()
+    _oracle_step(h1, one, [0])
+    t_seq = time.perf_counter() - t0
+    t_step = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    L0 = batch.strides()[0]
+    if t_seq <= t_step:
+        ns = int(min(8, max(1, t_step // t_seq)))
+        seqs = list(range(0, batch.num_seqs, max(1, batch.num_seqs // ns)))[:ns]
+        kp = 1 << 30
+    else:
+        seqs = [0]
+        kp = max(1, int(L0 * t_step / t_seq))
+    sub, positions = _sample_batch(batch, seqs, kp)
+    h = _host_inputs(sub)
+    idx = list(range(len(seqs)))
     for _ in range(args.warmup):
-        _oracle_step(h, batch, sample)
+        _oracle_step(h, sub, idx)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_step(h, batch, sample)
+        _oracle_step(h, sub, idx)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
     value = positions / (ms / 1e3)
-    desc = f"{len(sample)} of {batch.num_seqs} sequences ({positions} positions) per step, verify+propose"
+    desc = (f"{len(seqs)} of {batch.num_seqs} sequences" + (f", cut to {kp} positions" if kp < L0 else "")
+            + f" ({positions} positions) per step, verify+propose")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
