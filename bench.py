@@ -300,6 +300,22 @@ def run_reference(args):
 # The CUDA path
 # ---------------------------------------------------------------------------
 
+def slowest_rank(ms, device, distributed):
+    """The job's time: the largest of the ranks' times (one all-reduce)."""
+    import torch
+    if not distributed:
+        return float(ms)
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(positions_per_rank, world, steps, ms):
+    """Whole-job positions per second: every replica verifies its own batch."""
+    return positions_per_rank * world * steps / (ms / 1e3)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -389,12 +405,9 @@ def run_ours(args):
         dist.barrier()
     step_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
     verify_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
-    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if distributed:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = slowest_rank(step_ms, dev, distributed)
     ms_per_step = total_ms / K
-    value = total * world * K / (total_ms / 1e3)
+    value = job_throughput(total, world, K, total_ms)
     logit_gbs = (vbytes + pbytes) * world * K / (total_ms / 1e3) / 1e9
     peak, peak_kind = load_peaks()
     verify_avg_s = verify_ms / K / 1e3
@@ -423,10 +436,7 @@ def run_ours(args):
         e2e_ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.e2e_steps
-    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if distributed:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = total * world / (float(te.item()) / 1e3)
+    e2e_value = job_throughput(total, world, 1, slowest_rank(e2e_ms, dev, distributed))
 
     if rank != 0:
         dist.destroy_process_group()
