@@ -142,9 +142,8 @@ isd_status verify_impl(const void* p_logits, int64_t ld_p, const void* q_logits,
                        const int32_t* seq_offsets, int num_seqs, int total_positions,
                        const float* temperature, uint64_t seed, uint64_t offset, float tau,
                        int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
-                       const void* qnew_logits, int64_t ld_qnew, int32_t* proposals, uint8_t* valid,
-                       void* workspace, size_t workspace_bytes, void* stream) {
-    const bool fused = qnew_logits != nullptr || proposals != nullptr || valid != nullptr;
+                       bool fused, const void* qnew_logits, int64_t ld_qnew, int32_t* proposals,
+                       uint8_t* valid, void* workspace, size_t workspace_bytes, void* stream) {
     if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return ISD_ERR_INVALID_ARG;
     if (!(tau >= 0.0f) || !std::isfinite(tau)) return ISD_ERR_INVALID_ARG;
     if (num_seqs == 0) return ISD_OK;
@@ -226,7 +225,7 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
                       void* workspace, size_t workspace_bytes, void* stream) {
     return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
                        total_positions, temperature, seed, offset, 0.0f, accept_len, out_tokens, ratio, alpha,
-                       nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
+                       false, nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
 }
 
 isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
@@ -237,7 +236,7 @@ isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_
                               void* workspace, size_t workspace_bytes, void* stream) {
     return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
                        total_positions, temperature, seed, offset, tau, accept_len, out_tokens, ratio, alpha,
-                       nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
+                       false, nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
 }
 
 isd_status isd_verify_propose(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
@@ -247,10 +246,9 @@ isd_status isd_verify_propose(const void* p_logits, int64_t ld_p, const void* q_
                               int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
                               const void* qnew_logits, int64_t ld_qnew, int32_t* proposals, uint8_t* valid,
                               void* workspace, size_t workspace_bytes, void* stream) {
-    if (!qnew_logits || !proposals || !valid) return ISD_ERR_INVALID_ARG;
     return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
                        total_positions, temperature, seed, offset, tau, accept_len, out_tokens, ratio, alpha,
-                       qnew_logits, ld_qnew, proposals, valid, workspace, workspace_bytes, stream);
+                       true, qnew_logits, ld_qnew, proposals, valid, workspace, workspace_bytes, stream);
 }
 
 isd_status isd_propose(const void* qnew_logits, int64_t ld, isd_dtype dtype, int vocab,

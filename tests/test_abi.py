@@ -25,7 +25,8 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     names = declared_symbols()
-    for n in ("isd_verify", "isd_verify_relaxed", "isd_propose", "isd_alpha", "isd_verify_workspace_bytes",
+    for n in ("isd_verify", "isd_verify_relaxed", "isd_verify_propose", "isd_propose", "isd_alpha",
+              "isd_verify_workspace_bytes", "isd_verify_propose_workspace_bytes",
               "isd_propose_workspace_bytes", "isd_status_string"):
         assert n in names
 
@@ -102,6 +103,30 @@ def test_verify_relaxed_host_checks(lib):
     assert _verify_relaxed(lib, 0.5, C=0) == _lib.ISD_OK
     assert _verify_relaxed(lib, 0.5, p=FAKE + 2) == _lib.ISD_ERR_UNSUPPORTED
     assert _verify_relaxed(lib, 0.5, wsb=16) == _lib.ISD_ERR_WORKSPACE
+
+
+def _verify_propose(lib, **kw):
+    args = dict(p=FAKE, ldp=1024, q=FAKE, ldq=1024, dtype=0, vocab=1024, tokens=FAKE, offs=FAKE,
+                C=2, total=4, temp=FAKE, seed=0, offset=0, tau=0.0, acc=FAKE, out=FAKE, ratio=FAKE,
+                alpha=FAKE, qnew=FAKE, ldn=1024, props=FAKE, valid=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return lib.isd_verify_propose(*args.values())
+
+
+def test_verify_propose_host_checks(lib):
+    """The fused call needs its qnew rows and proposal outputs, except for an
+    empty batch; qnew's base must be 16-byte aligned like p's and q's."""
+    assert _verify_propose(lib, C=0, qnew=None, props=None, valid=None) == _lib.ISD_OK
+    for k in ("qnew", "props", "valid"):
+        assert _verify_propose(lib, **{k: None}) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify_propose(lib, ldn=1000) == _lib.ISD_ERR_INVALID_ARG
+    assert _verify_propose(lib, qnew=FAKE + 4) == _lib.ISD_ERR_UNSUPPORTED
+    assert _verify_propose(lib, tau=-1.0) == _lib.ISD_ERR_INVALID_ARG
+    assert lib.isd_verify_propose_workspace_bytes(64, 512, 151936, 0) > lib.isd_verify_workspace_bytes(64, 512, 151936, 0)
+    # The fused call's workspace check uses its own, larger size.
+    small = lib.isd_verify_workspace_bytes(64, 512, 151936, 0)
+    assert _verify_propose(lib, C=64, total=512, vocab=151936, ldp=151936, ldq=151936, ldn=151936,
+                           wsb=small) == _lib.ISD_ERR_WORKSPACE
 
 
 def test_propose_and_alpha_host_checks(lib):

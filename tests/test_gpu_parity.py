@@ -291,3 +291,45 @@ def test_fused_verify_propose_parity(name, kw):
         assert np.array_equal(gp["valid"], (gv["accept_len"] == np.diff(h["offs"])).astype(np.uint8))
     rep.check()
     assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 20), rep
+
+
+def test_fused_invalid_sequences_and_relaxed():
+    """The fused call on a batch with invalid sequences (strides out of range,
+    bad temperatures, a token out of range): those get accept length -1,
+    valid 0 and proposals -1; the valid ones match the oracle, also relaxed."""
+    from speculative_verify_accept_02_b300 import isd_verify_propose
+    V = 300
+    Ls = [2, 0, 33, 2, 2, 2, 1, 3, 4]
+    temps = np.array([1.0, 1.0, 1.0, -0.5, np.nan, 1.0, 1e-40, 0.0, 0.7], np.float32)
+    C = len(Ls)
+    offs = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int32)
+    total = int(offs[-1])
+    g = torch.Generator().manual_seed(5)
+    P = torch.randn(total + C, V, generator=g).to(torch.bfloat16)
+    Q = P[[int(offs[i]) + i + k for i in range(C) for k in range(Ls[i])]].clone()  # q == p: all accept
+    Qn = torch.randn(total, V, generator=g).to(torch.bfloat16)
+    tokens = torch.empty(total, dtype=torch.int32)
+    for i in range(C):
+        for k in range(Ls[i]):
+            tokens[offs[i] + k] = int(torch.argmax(P[offs[i] + i + k].float()))  # accepted at T = 0 too
+    tokens[offs[5] + 1] = V
+    d = "cuda"
+    hp, hq, hn = workloads.host_logits(P), workloads.host_logits(Q), workloads.host_logits(Qn)
+    for tau in (0.0, 0.5):
+        v, pr = isd_verify_propose(P.to(d), Q.to(d), tokens.to(d), Qn.to(d), torch.from_numpy(offs).to(d),
+                                   torch.from_numpy(temps).to(d), 2, 9, total=total, tau=tau)
+        torch.cuda.synchronize()
+        gv = dict(accept_len=v.accept_len.cpu().numpy(), out_tokens=v.out_tokens.cpu().numpy(),
+                  ratio=v.ratio.cpu().numpy(), alpha=v.alpha.cpu().numpy())
+        gp = dict(proposals=pr.proposals.cpu().numpy(), valid=pr.valid.cpu().numpy())
+        assert list(gv["accept_len"][1:7]) == [-1] * 6
+        assert list(gp["valid"]) == [1, 0, 0, 0, 0, 0, 0, 1, 1]
+        assert np.all(gp["proposals"][offs[1]:offs[7]] == -1)
+        ov = oracle.verify(hp, hq, V, tokens.numpy(), offs, temps, 2, 9, tau=tau)
+        compare_verify(ov, gv, offs).check()
+        op = oracle.propose(hn, V, offs, temps, 2, 9, accept_len=gv["accept_len"])
+        compare_propose(op, gp, offs, seqs=[0, 7, 8]).check()
+    # Empty batch: nothing launched, nothing written.
+    e = torch.zeros(1, dtype=torch.int32, device=d)
+    r, rp = isd_verify_propose(P.to(d), Q.to(d), tokens.to(d), Qn.to(d), e, torch.zeros(0, device=d), total=0)
+    assert r.accept_len.numel() == 0 and rp.valid.numel() == 0
