@@ -129,6 +129,46 @@ ORACLE_API double oracle_log_softmax_at(const double* logits, int V, double T, i
     return logits[x] / T - zmax - log(total);
 }
 
+/* The sampling filters of the pages' evaluation setting (experiments, §4.1:
+ * temperature 1.0, top-k 50, top-p 0.95) on one row, T > 0: p = softmax(logits/T);
+ * keep the top_k ids of highest probability (lower id first among equal
+ * probabilities; top_k <= 0 keeps every id); of those, in the same order,
+ * keep the shortest prefix whose probability, renormalised over the top_k,
+ * adds up to at least top_p (top_p >= 1 keeps them all); out = the kept
+ * probabilities renormalised, 0 elsewhere. */
+typedef struct { double p; int id; } ranked_id;
+
+static int by_rank(const void* a, const void* b) {
+    const ranked_id* x = (const ranked_id*)a;
+    const ranked_id* y = (const ranked_id*)b;
+    if (x->p != y->p) return x->p > y->p ? -1 : 1;
+    return x->id - y->id;
+}
+
+ORACLE_API void oracle_filtered_probs(const double* logits, int V, double T, int top_k, double top_p,
+                                      double* out) {
+    oracle_softmax(logits, V, T, out);
+    ranked_id* r = (ranked_id*)malloc(sizeof(ranked_id) * (size_t)V);
+    for (int v = 0; v < V; ++v) { r[v].p = out[v]; r[v].id = v; }
+    qsort(r, (size_t)V, sizeof(ranked_id), by_rank);
+    int kept = (top_k > 0 && top_k < V) ? top_k : V;
+    double sk = 0.0;
+    for (int j = 0; j < kept; ++j) sk += r[j].p;
+    int n = kept;
+    if (top_p < 1.0) {
+        double cum = 0.0;
+        for (int j = 0; j < kept; ++j) {
+            cum += r[j].p / sk;
+            if (cum >= top_p) { n = j + 1; break; }
+        }
+    }
+    double total = 0.0;
+    for (int j = 0; j < n; ++j) total += r[j].p;
+    for (int v = 0; v < V; ++v) out[v] = 0.0;
+    for (int j = 0; j < n; ++j) out[r[j].id] = r[j].p / total;
+    free(r);
+}
+
 /* Acceptance ratio of a proposed token x (§2 and §3.2):
  *   T > 0: min(1, p(x)/q(x)) with p = softmax(P/T), q = softmax(Q/T);
  *          q(x) = 0 (log q(x) = -inf) gives 1.

@@ -9,6 +9,7 @@ Summary" — §2 (alpha), §3.2 (acceptance, residual correction, bonus token),
 §3.3 (argmax proposals with strict verification), §3.1 (next-token shift).
 """
 import ctypes as C
+import math
 
 import numpy as np
 
@@ -46,6 +47,8 @@ def _declare(L):
                                     C.c_double, C.POINTER(C.c_int32), _ip, _dp,
                                     C.POINTER(C.c_double), _dp, C.POINTER(C.c_double), C.c_double]
     L.oracle_verify_one.restype = None
+    L.oracle_filtered_probs.argtypes = [_dp, C.c_int, C.c_double, C.c_int, C.c_double, _dp]
+    L.oracle_filtered_probs.restype = None
     L.oracle_ratio_relaxed.argtypes = [_dp, _dp, C.c_int, C.c_double, C.c_int, C.c_double]
     L.oracle_ratio_relaxed.restype = C.c_double
     L.oracle_verify.argtypes = [C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_int,
@@ -83,6 +86,14 @@ def _logit_buffer(logits):
     if a.strides[1] != a.itemsize or a.strides[0] % a.itemsize:
         raise ValueError("rows must be contiguous")
     return a, code, a.strides[0] // a.itemsize
+
+
+def _decode(logits, vocab):
+    """Rows of a host logit buffer (bf16 bit patterns or float32) as float64."""
+    a = np.asarray(logits)
+    if a.dtype in (np.uint16, np.int16):
+        a = (a.view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return a[:, :vocab].astype(np.float64)
 
 
 def _sel(seqs):
@@ -140,6 +151,85 @@ class Oracle:
         m = C.c_double()
         v = self.lib.oracle_icdf(ww, ww.size, float(u), C.byref(m))
         return v, m.value
+
+    def filtered_probs(self, logits, T, top_k, top_p):
+        """softmax(logits/T) after the top-k, then top-p filter, renormalised
+        (the pages' evaluation sampling setting)."""
+        z = _d(logits)
+        out = np.empty(z.size, dtype=np.float64)
+        self.lib.oracle_filtered_probs(z, z.size, float(T), int(top_k), float(top_p), out)
+        return out
+
+    def verify_filtered(self, p_logits, q_logits, vocab, tokens, seq_offsets, temperature, seed, offset,
+                        top_k, top_p):
+        """The verify step with the sampling filters applied to both p and q
+        (p~, q~): ratio min(1, p~(x)/q~(x)) (1 where q~(x) = 0), strict
+        acceptance, correction from normalize(max(0, p~_j - q~_j)) (p~_j if that
+        is all zero), bonus from p~_{L+1}.  T = 0 sequences are unaffected by
+        the filters and follow verify().  Same outputs as verify(); margins
+        are not computed."""
+        offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+        C_ = offs.size - 1
+        total = int(offs[-1])
+        temp = np.ascontiguousarray(temperature, dtype=np.float32)
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        P, Q = _decode(p_logits, vocab), _decode(q_logits, vocab)
+        out = dict(accept_len=np.full(C_, -2, np.int32), out_tokens=np.full(total + C_, -2, np.int32),
+                   ratio=np.full(total, np.nan), alpha=np.full(C_, np.nan))
+        for i in range(C_):
+            s, L, T = int(offs[i]), int(offs[i + 1] - offs[i]), float(temp[i])
+            if T == 0.0 or not (1 <= L <= 32) or not math.isfinite(T) or T < 0 or (0 < T < 1.17549435e-38) \
+                    or np.any((toks[s:s + L] < 0) | (toks[s:s + L] >= vocab)):
+                one = self.verify(p_logits, q_logits, vocab, tokens, seq_offsets, temperature, seed, offset,
+                                  seqs=[i])
+                for k in out:
+                    if k == "accept_len" or k == "alpha":
+                        out[k][i] = one[k][i]
+                    elif k == "ratio":
+                        out[k][s:s + max(L, 0)] = one[k][s:s + max(L, 0)]
+                    else:
+                        out[k][s + i: s + i + max(L, 0) + 1] = one[k][s + i: s + i + max(L, 0) + 1]
+                continue
+            pt = [self.filtered_probs(P[s + i + k], T, top_k, top_p) for k in range(L + 1)]
+            qt = [self.filtered_probs(Q[s + k], T, top_k, top_p) for k in range(L)]
+            x = toks[s:s + L]
+            ratio = np.array([1.0 if qt[k][x[k]] == 0.0 else min(1.0, pt[k][x[k]] / qt[k][x[k]])
+                              for k in range(L)])
+            a = 0
+            while a < L and self.uniform(seed, offset, i, a + 1, TAG_ACCEPT) < ratio[a]:
+                a += 1
+            if a < L:
+                w = np.maximum(pt[a] - qt[a], 0.0)
+                if not w.sum() > 0.0:
+                    w = pt[a]
+                tok = self.icdf(w, self.uniform(seed, offset, i, a + 1, TAG_CORRECT))[0]
+            else:
+                tok = self.icdf(pt[L], self.uniform(seed, offset, i, L + 1, TAG_BONUS))[0]
+            out["accept_len"][i] = a
+            out["ratio"][s:s + L] = ratio
+            out["alpha"][i] = ratio.mean()
+            slots = out["out_tokens"][s + i: s + i + L + 1]
+            slots[:] = -1
+            slots[:a] = x[:a]
+            slots[a] = tok
+        return out
+
+    def propose_filtered(self, qnew_logits, vocab, seq_offsets, temperature, seed, offset, top_k, top_p,
+                         accept_len=None):
+        """Proposals drawn from the filtered softmax(qnew/T) (argmax at T = 0),
+        with propose()'s validity rules."""
+        base = self.propose(qnew_logits, vocab, seq_offsets, temperature, seed, offset, accept_len=accept_len)
+        offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+        temp = np.ascontiguousarray(temperature, dtype=np.float32)
+        Qn = _decode(qnew_logits, vocab)
+        for i in range(offs.size - 1):
+            if not base["valid"][i] or temp[i] == 0.0:
+                continue
+            for m in range(1, int(offs[i + 1] - offs[i]) + 1):
+                r = int(offs[i]) + m - 1
+                w = self.filtered_probs(Qn[r], float(temp[i]), top_k, top_p)
+                base["proposals"][r] = self.icdf(w, self.uniform(seed, offset, i, m, TAG_PROPOSE))[0]
+        return base
 
     def ratio_relaxed(self, P, Q, T, x, tau):
         """min(1, (1 + tau) p(x)/q(x)) of one row pair (argmax indicator at T = 0)."""

@@ -379,6 +379,83 @@ def pin_relaxed_law(orc):
     assert orc.ratio_relaxed(np.log(pp[0]), np.log(qq[0]), 0.0, 1, 9.0) == 0.0
 
 
+def pin_filter_known(orc):
+    """The sampling filters of the pages' evaluation setting (experiments,
+    §4.1: top-k, then top-p, renormalised) on hand-worked rows; no filter is
+    plain softmax; top-k 1 is the lowest-id argmax; the temperature applies
+    before the filters."""
+    pr = np.array([0.5, 0.3, 0.15, 0.05])
+    lg = np.log(pr)
+    cases = [((0, 0.75), [0.625, 0.375, 0, 0]), ((0, 0.45), [1, 0, 0, 0]),
+             ((3, 1.0), [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95, 0]), ((2, 0.9), [0.625, 0.375, 0, 0]),
+             ((0, 0.9), [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95, 0]),
+             ((3, 0.82), [0.625, 0.375, 0, 0])]  # top-p measured within the top 3
+    for (k, tp), want in cases:
+        assert np.allclose(orc.filtered_probs(lg, 1.0, k, tp), want, atol=1e-12), (k, tp)
+    # Equal probabilities: the lower ids are kept.
+    assert np.allclose(orc.filtered_probs(np.zeros(4), 1.0, 2, 1.0), [0.5, 0.5, 0, 0], atol=1e-12)
+    rng = np.random.default_rng(21)
+    z = rng.normal(0, 2, 50)
+    assert np.allclose(orc.filtered_probs(z, 0.7, 0, 1.0), sp_softmax(z / 0.7), atol=1e-14)
+    assert np.allclose(orc.filtered_probs(z, 0.7, 50, 1.0), sp_softmax(z / 0.7), atol=1e-14)
+    onehot = np.zeros(50)
+    onehot[int(np.argmax(z))] = 1.0
+    assert np.array_equal(orc.filtered_probs(z, 1.3, 1, 1.0), onehot)
+    # T = 2 turns p into sqrt(p) renormalised, before the top-2 filter.
+    sq = np.sqrt(pr)
+    assert np.allclose(orc.filtered_probs(lg, 2.0, 2, 1.0), [sq[0] / (sq[0] + sq[1]), sq[1] / (sq[0] + sq[1]), 0, 0],
+                       atol=1e-12)
+
+
+def pin_filtered_verify_law(orc):
+    """Verification on filtered distributions (both p and q filtered, then
+    §3.2's strict acceptance and residual correction): many copies of one
+    sequence give (accept length, emitted token) with the exact law built
+    from the hand-worked filtered rows, and the emitted first token follows
+    the filtered p (the lossless property carries over to any pair of
+    distributions).  With no filter it is the plain verify step."""
+    V, L, T = 4, 1, 1.0
+    p1 = np.array([0.5, 0.3, 0.15, 0.05])
+    q1 = np.array([0.1, 0.4, 0.3, 0.2])
+    p2 = np.array([0.1, 0.2, 0.3, 0.4])
+    k, tp = 3, 0.9
+    # Filtered by hand: p1 -> top-3 {0, 1, 2} renormalised, cumulative 0.526,
+    # 0.842, 1.0 -> all three; q1 -> top-3 {1, 2, 3}: 0.444, 0.778, 1.0 -> all
+    # three; p2 -> top-3 {3, 2, 1}: 0.444, 0.778, 1.0 -> all three.
+    pt = np.array([0.5, 0.3, 0.15, 0]) / 0.95
+    qt = np.array([0, 0.4, 0.3, 0.2]) / 0.9
+    bt = np.array([0, 0.2, 0.3, 0.4]) / 0.9
+    C = 20000
+    P = np.tile(np.log(np.stack([p1, p2])).astype(np.float32), (C, 1))
+    Q = np.tile(np.log(q1[None]).astype(np.float32), (C, 1))
+    offs = (np.arange(C + 1) * L).astype(np.int32)
+    rng = np.random.default_rng(31)
+    xs = rng.choice(V, size=C, p=qt).astype(np.int32)  # proposals from the filtered q
+    out = orc.verify_filtered(P, Q, V, xs, offs, np.full(C, T, np.float32), 5, 1, k, tp)
+    a = out["accept_len"]
+    tok = out["out_tokens"].reshape(C, L + 1)[np.arange(C), a]
+    first = out["out_tokens"].reshape(C, L + 1)[:, 0]
+    assert _chi2_ok(np.bincount(first, minlength=V), pt), np.bincount(first, minlength=V)
+    ratio = np.where(qt > 0, np.minimum(1.0, pt / np.where(qt > 0, qt, 1.0)), 1.0)
+    w = np.maximum(pt - qt, 0.0)
+    w /= w.sum()
+    law = np.concatenate([np.array([qt[x] * (1 - ratio[x]) for x in range(V)]).sum() * w,
+                          np.zeros(V)])
+    for x in range(V):  # accepted: token x itself in slot 0, then the bonus
+        law[V:] += qt[x] * ratio[x] * bt
+    counts = np.bincount(a * V + tok, minlength=2 * V)
+    assert _chi2_ok(counts, law), (counts, law * C)
+    # No filter: the plain step.
+    Pn = P[:400 * (L + 1)]
+    Qn = Q[:400 * L]
+    xn = xs[:400]
+    plain = orc.verify(Pn, Qn, V, xn, offs[:401], np.full(400, T, np.float32), 5, 1)
+    filt = orc.verify_filtered(Pn, Qn, V, xn, offs[:401], np.full(400, T, np.float32), 5, 1, 0, 1.0)
+    assert np.array_equal(plain["accept_len"], filt["accept_len"])
+    assert np.array_equal(plain["out_tokens"], filt["out_tokens"])
+    assert np.allclose(plain["ratio"], filt["ratio"], rtol=1e-12)
+
+
 def pin_mc_propose_law(orc):
     """Proposals follow softmax(qnew/T) (inverse CDF with the PROPOSE
     uniforms); T = 0 gives the lowest-id argmax; accept_len < L gives no
@@ -491,4 +568,5 @@ ALL_PINS = [
     pin_tv_identity, pin_residual_known, pin_icdf_grid, pin_handworked, pin_greedy_planted,
     pin_p_equals_q, pin_lossless_enumeration, pin_mc_verify_law, pin_mc_propose_law,
     pin_mc_step_independence, pin_alpha_mean, pin_bf16_decoding, pin_invalid_inputs, pin_relaxed_law,
+    pin_filter_known, pin_filtered_verify_law,
 ]

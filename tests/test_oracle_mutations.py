@@ -29,6 +29,11 @@ MUTATIONS = {
                            "fmin(1.0, exp(log_px - log_qx) / (1.0 + tau))"),
     "relaxed ratio reported": ("        if (tau != 0.0)\n            racc", "        if (tau != 0.0)\n            ratio[k - 1] = racc"),
     "prefix not stopped": ("if (!accepted) break;", "if (!accepted) continue;"),
+    "top-k keeps one more": ("int kept = (top_k > 0 && top_k < V) ? top_k : V;",
+                             "int kept = (top_k > 0 && top_k < V) ? top_k + 1 : V;"),
+    "filter ties to higher id": ("return x->id - y->id;", "return y->id - x->id;"),
+    "filtered not renormalised": ("out[r[j].id] = r[j].p / total;", "out[r[j].id] = r[j].p;"),
+    "top-p over the whole row": ("cum += r[j].p / sk;", "cum += r[j].p;"),
     "greedy accepts all": ("accepted = ratio[k - 1] == 1.0;", "accepted = 1;"),
     "alpha denominator": ("*alpha = sum / L;", "*alpha = sum / (L + 1);"),
     "bonus row": ("const double* Pb = P + (size_t)L * V;",
