@@ -1,0 +1,45 @@
+"""Host-side arithmetic of bench.py: the algorithmic bytes of a step (the
+roofline's numerator) and the code-only hash that keys profiled traffic."""
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from speculative_verify_accept_02_b300 import workloads  # noqa: E402
+
+
+def test_algorithmic_bytes_counts_rows_read():
+    """Per sequence: 2 L rows at T > 0 and L at T = 0 (greedy reads no q), the
+    final anchor row only when every proposal was accepted; the propose pass
+    adds L qnew rows for each sequence whose proposals are drawn."""
+    b = workloads.make("ragged", num_seqs=6, vocab=1000)
+    Ls = b.strides()
+    temps = b.temperature.tolist()
+    acc = [Ls[0], 0, Ls[2], 1, 0, Ls[5]]
+    valid = [1, 0, 1, 0, 0, 1]
+    row = 2 * 1000  # bf16
+    want_v = sum(row * ((2 * L if t > 0 else L) + (1 if a == L else 0)) for L, t, a in zip(Ls, temps, acc))
+    want_p = sum(row * L for L, ok in zip(Ls, valid) if ok)
+    assert bench.algorithmic_bytes(b, acc, valid) == (want_v, want_p)
+    f = workloads.make("tiny", num_seqs=2, vocab=100)  # fp32 rows: 4 bytes per id
+    v, p = bench.algorithmic_bytes(f, [0, 0], [0, 0])
+    assert v == 4 * 100 * sum(2 * L for L in f.strides()) and p == 0
+
+
+def test_c64_algorithmic_bytes_match_the_recorded_figure():
+    """c64 (C=64, L=8, V=151936 bf16, T=1) reads 1024 rows of 303,872 bytes,
+    plus one final anchor row per sequence that accepts all 8."""
+    b = workloads.make("c64", num_seqs=2, vocab=151936)  # the per-sequence arithmetic
+    v, _ = bench.algorithmic_bytes(b, [3, 8], [0, 1])
+    assert v == 303872 * (16 + 16 + 1)
+
+
+def test_source_hash_ignores_comments_only():
+    src = "int a = 1; // note\n/* block\n comment */ const char* s = \"x//y\";\nint b;\n"
+    assert bench._strip_comments(src) == bench._strip_comments(src.replace("note", "other"))
+    assert bench._strip_comments(src) != bench._strip_comments(src.replace("int b", "int c"))
+    assert '"x//y"' in bench._strip_comments(src)
