@@ -20,6 +20,10 @@
  *     (the greedy, temperature-0 rule: accept while x_k is the argmax of p_k).
  *   - §3.1 Introspective-Consistency Training: logits[i] predict token[i+1]
  *     (next-token shift), which fixes which logit row scores which token.
+ *   - §3.3 I-DLM Serving Stack, the stationary-batch loop: KV slots are
+ *     allocated with a batched scatter, and the entries of rejected
+ *     proposals and of mask positions are trimmed after verification
+ *     (oracle_kv_commit, at the end of this file).
  *
  * Where the pages are silent the plainest reading is taken (listed in the
  * design notes): inverse-CDF sampling in vocabulary order with counter-based
@@ -487,4 +491,126 @@ ORACLE_API void oracle_alpha(const float* ratio, const int32_t* seq_offsets, int
         total += alpha_per_seq[i];
     }
     *alpha_mean = num_seqs > 0 ? total / num_seqs : NAN;
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV-slot bookkeeping of the stationary-batch loop (§3.3: slots allocated   */
+/* with a batched scatter; rejected and masked entries trimmed).             */
+/* ------------------------------------------------------------------------ */
+
+enum { KV_ERR_STATE = 1, KV_ERR_ACCEPT = 2, KV_ERR_SLOT = 4, KV_ERR_POOL = 8, KV_ERR_CAPACITY = 16 };
+
+/* Per-sequence outcome of one commit; 0 or one KV_ERR_* bit set. */
+static int kv_plan(const int32_t* table_row, int64_t ld, int len, int L, int w, int a_in, int M,
+                   int pool_size, int* kept, int* next_pend, int* status) {
+    *status = 0;
+    if (len < 0 || L < 0 || w < 0 || (int64_t)len + w > ld || (w == 0 && L != 0) ||
+        (w > 0 && w != 1 + L + M)) {
+        *status = KV_ERR_STATE;
+        return 0;
+    }
+    if (w == 0) {               /* admitted, no forward in flight yet */
+        *kept = 0;
+        *next_pend = 0;
+    } else {
+        int a = L > 0 ? a_in : 0;   /* a proposal-only step verified nothing */
+        if (a < 0 || a > L) {
+            *status = KV_ERR_ACCEPT;
+            return 0;
+        }
+        *kept = 1 + a;                               /* x_last, then x_1..x_a */
+        *next_pend = (L == 0 || a == L) ? M : 0;     /* the masks' proposals stand */
+    }
+    for (int j = *kept; j < w; ++j) {
+        int32_t slot = table_row[len + j];
+        if (slot < 0 || slot >= pool_size) *status |= KV_ERR_SLOT;
+    }
+    if ((int64_t)len + *kept + 1 + *next_pend + M > ld) *status |= KV_ERR_CAPACITY;
+    return 1;
+}
+
+/*
+ * One commit of the stationary batch after a forward and its verification.
+ *
+ * Cache model: a pool of pool_size KV slots (one token each) and, per
+ * sequence i, a row table[i][0..ld) of slot ids by position.  Positions
+ * 0..seq_len[i]-1 are committed; the forward in flight wrote alloc[i]
+ * entries at positions seq_len[i] .. seq_len[i]+alloc[i]-1, in the order
+ *     x_last, the pend[i] pending proposals x_1..x_L, the M mask positions,
+ * where x_last is the newest emitted token (§3.2: one anchor token, the
+ * proposals under verification, then the mask positions that propose).
+ * The free slots are a stack free_slots[0..*free_top), top last.
+ *
+ * Per sequence, with a = accept_len[i] (read only when L = pend[i] > 0):
+ *   alloc = 0 (just admitted; pend must be 0): keeps nothing, and its next
+ *       forward is a proposal-only step;
+ *   alloc = 1 + L + M: keeps x_last and the accepted x_1..x_a (1 + a
+ *       entries; 1 when L = 0), trims the rejected proposals and every mask
+ *       entry (§3.3), and its next forward verifies the masks' M proposals
+ *       when every proposal passed or none were pending (L' = M), else is
+ *       proposal-only (L' = 0, §3.2);
+ *   the next forward's 1 + L' + M entries are allocated right after the
+ *       kept ones.
+ * Trimmed slots are pushed on the stack in (sequence, position) order and
+ * their table entries set to -1; then the batch takes the top sum(1+L'+M)
+ * entries of the stack as one block, sequence i receiving the block's
+ * entries from its exclusive prefix of the counts onward, in position
+ * order (so the slots just trimmed are the first reused).
+ *
+ * Returns 0 after updating table, seq_len, pend, alloc, free_slots and
+ * free_top.  Otherwise returns the OR of KV_ERR_* bits and changes nothing:
+ *   per sequence, the first of STATE (negative fields, alloc past the row,
+ *   alloc not 0 or 1+L+M, alloc 0 with L > 0) and ACCEPT (a outside [0, L]),
+ *   else SLOT (a trimmed entry outside [0, pool_size)) and CAPACITY (the
+ *   next allocation runs past the row);
+ *   then, only when no bit is set: STATE if *free_top lies outside
+ *   [0, pool_size] or the pushes would overrun the pool, else POOL if the
+ *   stack cannot supply the batch.
+ */
+ORACLE_API int oracle_kv_commit(int32_t* table, int64_t ld, int32_t* seq_len, int32_t* pend, int32_t* alloc,
+                                int32_t* free_slots, int32_t* free_top, int pool_size,
+                                const int32_t* accept_len, int num_seqs, int num_masks) {
+    int M = num_masks;
+    int status = 0;
+    int64_t pushed = 0, wanted = 0;
+    for (int i = 0; i < num_seqs; ++i) {
+        int kept, next_pend, st;
+        if (kv_plan(table + (int64_t)i * ld, ld, seq_len[i], pend[i], alloc[i], accept_len[i], M, pool_size,
+                    &kept, &next_pend, &st)) {
+            pushed += alloc[i] - kept;
+            wanted += 1 + next_pend + M;
+        }
+        status |= st;
+    }
+    if (status) return status;
+    int64_t top = *free_top;
+    if (top < 0 || top > pool_size || top + pushed > pool_size) return KV_ERR_STATE;
+    if (top + pushed < wanted) return KV_ERR_POOL;
+
+    /* trim: push the trimmed slots, clear their table entries */
+    for (int i = 0; i < num_seqs; ++i) {
+        int kept, next_pend, st;
+        kv_plan(table + (int64_t)i * ld, ld, seq_len[i], pend[i], alloc[i], accept_len[i], M, pool_size,
+                &kept, &next_pend, &st);
+        for (int j = kept; j < alloc[i]; ++j) {
+            int32_t* e = &table[(int64_t)i * ld + seq_len[i] + j];
+            free_slots[top++] = *e;
+            *e = -1;
+        }
+    }
+    /* batched scatter: the top `wanted` stack entries, in sequence order */
+    int64_t next = top - wanted;
+    *free_top = (int32_t)next;
+    for (int i = 0; i < num_seqs; ++i) {
+        int kept, next_pend, st;
+        kv_plan(table + (int64_t)i * ld, ld, seq_len[i], pend[i], alloc[i], accept_len[i], M, pool_size,
+                &kept, &next_pend, &st);
+        int n = 1 + next_pend + M;
+        int len = seq_len[i] + kept;
+        for (int j = 0; j < n; ++j) table[(int64_t)i * ld + len + j] = free_slots[next++];
+        seq_len[i] = len;
+        pend[i] = next_pend;
+        alloc[i] = n;
+    }
+    return 0;
 }

@@ -61,6 +61,8 @@ def _declare(L):
     L.oracle_propose.restype = None
     L.oracle_alpha.argtypes = [_fp, _ip, C.c_int, _dp, C.POINTER(C.c_double)]
     L.oracle_alpha.restype = None
+    L.oracle_kv_commit.argtypes = [_ip, C.c_int64, _ip, _ip, _ip, _ip, _ip, C.c_int, _ip, C.c_int, C.c_int]
+    L.oracle_kv_commit.restype = C.c_int
     L.oracle_max_threads.argtypes = [C.c_int]
     L.oracle_max_threads.restype = C.c_int
 
@@ -310,6 +312,25 @@ class Oracle:
         mean = C.c_double()
         self.lib.oracle_alpha(r, offs, C_, per, C.byref(mean))
         return per, mean.value
+
+    def kv_commit(self, state, accept_len, num_masks):
+        """One commit of the stationary batch's KV-slot bookkeeping (Summary
+        §3.3: batched slot scatter, trim of rejected and masked entries).
+
+        state: a KVState (speculative_verify_accept_02_b300.kv) or any object
+        with int32 numpy arrays table [C, ld], seq_len, pend, alloc [C],
+        free_slots [pool] and free_top [1]; updated in place on success.
+        Returns the status: 0, or the OR of the KV error bits (state
+        unchanged)."""
+        arrs = [state.table, state.seq_len, state.pend, state.alloc, state.free_slots, state.free_top]
+        for a in arrs:
+            if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+                raise TypeError("KV state arrays must be C-contiguous int32 numpy arrays")
+        C_, ld = state.table.shape
+        acc = np.ascontiguousarray(np.broadcast_to(np.asarray(accept_len, np.int32), (C_,)))
+        return self.lib.oracle_kv_commit(state.table, ld, state.seq_len, state.pend, state.alloc,
+                                         state.free_slots, state.free_top, state.free_slots.size, acc, C_,
+                                         int(num_masks))
 
     def threads(self, nthreads=0):
         """Number of threads the batched oracle calls use."""

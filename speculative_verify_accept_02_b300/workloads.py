@@ -1,8 +1,8 @@
 """Seeded synthetic inputs for the verify-and-propose step.
 
 This module only makes inputs; it holds none of the step's arithmetic (no
-ratios, no acceptance, no residuals).  Both the CUDA path and the fp64 oracle
-consume what it makes.  Random draws use torch's own generators (CPU or CUDA)
+ratios, no acceptance, no residuals, no KV-slot bookkeeping).  Both the CUDA
+path and the fp64 oracle consume what it makes.  Random draws use torch's own generators (CPU or CUDA)
 seeded per workload; proposed tokens are drawn with ``torch.multinomial`` /
 ``torch.argmax`` as a stand-in for the forward pass that produced them.
 
@@ -24,6 +24,7 @@ Layout (shared with the library, see include/isd.h):
 from dataclasses import dataclass, field
 from typing import Optional
 
+import numpy as np
 import torch
 
 VOCAB = 151936
@@ -225,3 +226,96 @@ def host_logits(t: torch.Tensor):
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError(t.dtype)
+
+
+# ---------------------------------------------------------------------------
+# KV-slot state of a stationary batch (inputs of isd_kv_commit)
+# ---------------------------------------------------------------------------
+
+KV_FIELDS = ("table", "seq_len", "pend", "alloc", "free_slots", "free_top")
+
+
+@dataclass
+class KVState:
+    """KV-slot state of a stationary batch, as int32 host arrays (layout of
+    isd_kv_commit in include/isd.h):
+
+    table      [C, ld]  slot id of each cached position, -1 where empty
+    seq_len    [C]      committed positions per sequence
+    pend       [C]      proposals the forward in flight verifies
+    alloc      [C]      entries the forward in flight writes (0: none yet)
+    free_slots [pool]   stack of free slots; free_slots[:free_top] are free
+    free_top   [1]
+    """
+    table: np.ndarray
+    seq_len: np.ndarray
+    pend: np.ndarray
+    alloc: np.ndarray
+    free_slots: np.ndarray
+    free_top: np.ndarray
+
+    @property
+    def num_seqs(self) -> int:
+        return self.table.shape[0]
+
+    @property
+    def ld(self) -> int:
+        return self.table.shape[1]
+
+    @property
+    def pool_size(self) -> int:
+        return self.free_slots.size
+
+    def copy(self) -> "KVState":
+        return KVState(*(getattr(self, f).copy() for f in KV_FIELDS))
+
+    def equal(self, other) -> bool:
+        return all(np.array_equal(getattr(self, f), getattr(other, f)) for f in KV_FIELDS)
+
+    def to_torch(self, device) -> dict:
+        return {f: torch.from_numpy(getattr(self, f).copy()).to(device) for f in KV_FIELDS}
+
+    @staticmethod
+    def from_torch(tensors: dict) -> "KVState":
+        return KVState(*(tensors[f].detach().cpu().numpy().astype(np.int32, copy=True) for f in KV_FIELDS))
+
+
+def make_kv_state(num_seqs: int, max_len: int, pool_size: int, committed, seed: int = 0) -> KVState:
+    """Admitted sequences with `committed[i]` cached positions each (the
+    prompt, already prefilled) on slots drawn from a seeded permutation of
+    the pool; the remaining slots form the free stack in that permuted order.
+    Nothing is in flight (pend = alloc = 0)."""
+    committed = np.broadcast_to(np.asarray(committed, np.int64), (num_seqs,))
+    if np.any(committed < 0) or np.any(committed > max_len) or committed.sum() > pool_size:
+        raise ValueError("committed lengths do not fit the rows or the pool")
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(pool_size).astype(np.int32)
+    table = np.full((num_seqs, max_len), -1, np.int32)
+    at = 0
+    for i in range(num_seqs):
+        n = int(committed[i])
+        table[i, :n] = perm[at:at + n]
+        at += n
+    free = np.full(pool_size, -1, np.int32)
+    rest = perm[at:]
+    free[:rest.size] = rest
+    return KVState(table, committed.astype(np.int32), np.zeros(num_seqs, np.int32),
+                   np.zeros(num_seqs, np.int32), free, np.array([rest.size], np.int32))
+
+
+def draw_accept_lengths(rng: np.random.Generator, pend: np.ndarray, alpha: float) -> np.ndarray:
+    """Stand-in for a verify call's accept lengths: each of the pend[i]
+    proposals passes with probability alpha until the first failure.
+    Entries of sequences with nothing pending hold arbitrary values (the
+    commit ignores them)."""
+    pend = np.asarray(pend)
+    a = np.zeros(pend.size, np.int32)
+    for i, L in enumerate(pend):
+        if L == 0:
+            a[i] = rng.integers(-100, 100)
+            continue
+        k = 0
+        while k < L and rng.random() < alpha:
+            k += 1
+        a[i] = k
+    return a

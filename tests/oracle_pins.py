@@ -563,10 +563,123 @@ def pin_invalid_inputs(orc):
     assert not math.isnan(out["alpha"][0])
 
 
+# ---------------------------------------------------------------------------
+# KV-slot bookkeeping of the stationary-batch loop (Summary §3.3)
+# ---------------------------------------------------------------------------
+
+def _kv_state(d):
+    from speculative_verify_accept_02_b300.workloads import KVState
+    a = lambda x: np.array(x, np.int32)
+    return KVState(a(d["table"]), a(d["seq_len"]), a(d["pend"]), a(d["alloc"]), a(d["free_slots"]),
+                   a([d["free_top"]]))
+
+
+def pin_kv_handworked(orc):
+    """Commits worked by hand (tests/golden/handworked_kv_commit.json): the
+    kept prefix, the trimmed slots pushed in order, the batch's block taken
+    from the stack top, and refusals that change nothing."""
+    with open(os.path.join(GOLDEN, "handworked_kv_commit.json")) as f:
+        g = json.load(f)
+    st = _kv_state(dict(g["initial"]))
+    for c in g["commits"]:
+        before = st.copy()
+        status = orc.kv_commit(st, c["accept_len"], g["num_masks"])
+        assert status == c["status"], (c["name"], status)
+        if c.get("unchanged"):
+            assert st.equal(before), c["name"]
+        else:
+            assert st.equal(_kv_state(c)), c["name"]
+    pc = g["pool_case"]
+    st = _kv_state(pc)
+    before = st.copy()
+    assert orc.kv_commit(st, pc["accept_len"], pc["num_masks"]) == pc["status"]
+    assert st.equal(before)
+
+
+def pin_kv_refusals_and_exact_fits(orc):
+    """Hand-derived edge cases: an inconsistent in-flight count (STATE = 1),
+    a trimmed entry that is not a pool slot (SLOT = 4), and allocations that
+    use the last free slot and the last table column (accepted)."""
+    from speculative_verify_accept_02_b300.workloads import KVState
+    a = lambda x: np.array(x, np.int32)
+    # After the admission of the worked example: seq 0 at positions 2..4, seq 1 at 1..3.
+    admitted = dict(table=[[0, 1, 14, 15, 16, -1, -1, -1, -1, -1], [2, 17, 18, 19, -1, -1, -1, -1, -1, -1]],
+                    seq_len=[2, 1], pend=[0, 0], alloc=[3, 3],
+                    free_slots=list(range(3, 20)) + [-1, -1, -1], free_top=11)
+    st = _kv_state(admitted)
+    st.alloc[0] = 4                      # not 1 + L + M = 3
+    before = st.copy()
+    assert orc.kv_commit(st, [0, 0], 2) == 1 and st.equal(before)
+    st = _kv_state(admitted)
+    st.table[1, 3] = 20                  # trimmed in this commit; the pool has slots 0..19
+    before = st.copy()
+    assert orc.kv_commit(st, [0, 0], 2) == 4 and st.equal(before)
+    st = _kv_state(admitted)
+    st.pend[1] = 1                       # then alloc 3 != 1 + 1 + 2
+    assert orc.kv_commit(st, [0, 0], 2) == 1
+    # Exact fits: one admitted sequence takes all 4 free slots and fills its row.
+    st = KVState(a([[7, 6, -1, -1, -1, -1]]), a([2]), a([0]), a([0]), a([3, 2, 1, 0, 5, 4, 6, 7]), a([4]))
+    assert orc.kv_commit(st, [0], 3) == 0
+    assert list(st.table[0]) == [7, 6, 3, 2, 1, 0] and int(st.free_top[0]) == 0
+    assert list(st.alloc) == [4] and list(st.pend) == [0] and list(st.seq_len) == [2]
+
+
+def pin_kv_cache_holds_token_stream(orc):
+    """A stationary batch run for many steps with random accept lengths: a
+    synthetic forward writes each query token's id into its slot (x_last,
+    the pending proposals, a mask id at the mask positions), verification is
+    simulated from §3.2 (accept a prefix, then a correction or bonus token;
+    the masks' proposals are verified next only after a full acceptance or a
+    proposal-only step).  After every commit the cache must hold exactly the
+    committed token stream minus its newest token (x_last), and every pool
+    slot must be either free or referenced once."""
+    from speculative_verify_accept_02_b300.workloads import draw_accept_lengths, make_kv_state
+    rng = np.random.default_rng(11)
+    C, M, steps, MASK = 5, 3, 40, -7
+    prompts = [list(rng.integers(0, 1000, int(n))) for n in rng.integers(1, 9, C)]
+    ld = 9 + steps * (M + 1) + 2 * M + 1
+    st = make_kv_state(C, ld, C * ld, [len(pr) - 1 for pr in prompts], seed=5)
+    content = np.full(C * ld, -1, np.int64)
+    for i, pr in enumerate(prompts):
+        content[st.table[i, :len(pr) - 1]] = pr[:-1]
+    stream = [list(pr) for pr in prompts]
+    pending = [[] for _ in range(C)]
+    accept = np.zeros(C, np.int32)
+    for step in range(steps):
+        assert orc.kv_commit(st, accept, M) == 0, step
+        used = []
+        for i in range(C):
+            n = int(st.seq_len[i])
+            assert n == len(stream[i]) - 1, (step, i)
+            assert list(content[st.table[i, :n]]) == stream[i][:-1], (step, i)
+            assert int(st.pend[i]) == len(pending[i]) and int(st.alloc[i]) == 1 + len(pending[i]) + M
+            live = n + int(st.alloc[i])
+            assert np.all(st.table[i, live:] == -1)
+            used += list(st.table[i, :live])
+        free = list(st.free_slots[:int(st.free_top[0])])
+        assert sorted(used + free) == list(range(st.pool_size)), step
+        # the forward writes its query tokens into the allocated slots
+        for i in range(C):
+            n, L = int(st.seq_len[i]), len(pending[i])
+            toks = [stream[i][-1]] + pending[i] + [MASK] * M
+            content[st.table[i, n:n + len(toks)]] = toks
+        accept = draw_accept_lengths(rng, st.pend, 0.7)
+        for i in range(C):
+            L = len(pending[i])
+            if L == 0:                                   # proposal-only step
+                stream[i].append(int(rng.integers(0, 1000)))
+                pending[i] = list(rng.integers(0, 1000, M))
+                continue
+            k = int(accept[i])
+            stream[i] += pending[i][:k] + [int(rng.integers(0, 1000))]
+            pending[i] = list(rng.integers(0, 1000, M)) if k == L else []
+
+
 ALL_PINS = [
     pin_philox_numpy, pin_uniform_layout, pin_softmax_library, pin_temperature_ratio,
     pin_tv_identity, pin_residual_known, pin_icdf_grid, pin_handworked, pin_greedy_planted,
     pin_p_equals_q, pin_lossless_enumeration, pin_mc_verify_law, pin_mc_propose_law,
     pin_mc_step_independence, pin_alpha_mean, pin_bf16_decoding, pin_invalid_inputs, pin_relaxed_law,
-    pin_filter_known, pin_filtered_verify_law,
+    pin_filter_known, pin_filtered_verify_law, pin_kv_handworked, pin_kv_refusals_and_exact_fits,
+    pin_kv_cache_holds_token_stream,
 ]

@@ -58,6 +58,16 @@ MUTATIONS = {
                      "return (double)(out[0] >> 41) * (1.0 / 16777216.0);"),
     "anchor rows not shifted": ("load_rows(p_logits, dtype, ld_p, (int64_t)start + i, L + 1, V, P);",
                                 "load_rows(p_logits, dtype, ld_p, (int64_t)start, L + 1, V, P);"),
+    "kv keeps no x_last": ("*kept = 1 + a;", "*kept = a;"),
+    "kv verifies after a rejection": ("*next_pend = (L == 0 || a == L) ? M : 0;", "*next_pend = M;"),
+    "kv reads accept of proposal-only": ("int a = L > 0 ? a_in : 0;", "int a = a_in;"),
+    "kv trimmed entry not cleared": ("            *e = -1;\n", ""),
+    "kv block from stack bottom": ("int64_t next = top - wanted;", "int64_t next = 0;"),
+    "kv pool check off by one": ("if (top + pushed < wanted) return KV_ERR_POOL;",
+                                 "if (top + pushed <= wanted) return KV_ERR_POOL;"),
+    "kv capacity off by one": ("+ 1 + *next_pend + M > ld)", "+ 1 + *next_pend + M >= ld)"),
+    "kv slot range": ("slot >= pool_size", "slot > pool_size"),
+    "kv allocation after the trimmed": ("int len = seq_len[i] + kept;", "int len = seq_len[i] + alloc[i];"),
     "bf16 decoding": ("uint32_t bits = (uint32_t)h << 16;", "uint32_t bits = (uint32_t)h << 15;"),
 }
 
