@@ -21,6 +21,7 @@ import json
 
 import numpy as np
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -111,13 +112,40 @@ def _strip_comments(src: str) -> str:
     return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources' code (comments and blank lines ignored)."""
-    h = hashlib.sha256()
+# The sources that build and launch the verify kernel: its translation unit,
+# the host file that sizes its grid, workspace and cache policy, and the
+# local headers they include.  Profiled DRAM counters stay valid while these
+# are unchanged.
+PROFILED_SOURCES = ("isd_verify.cu", "isd_api.cu")
+
+
+def profiled_source_files():
+    """PROFILED_SOURCES and the local headers they include, recursively."""
     csrc = os.path.join(ROOT, "speculative_verify_accept_02_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), encoding="utf-8") as f:
-            h.update(name.encode() + _strip_comments(f.read()).encode())
+    seen = []
+
+    def visit(path):
+        path = os.path.normpath(path)
+        if path in seen:
+            return
+        seen.append(path)
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+        for inc in re.findall(r'^[ \t]*#[ \t]*include[ \t]+"([^"]+)"', text, re.M):
+            visit(os.path.join(os.path.dirname(path), inc))
+
+    for name in PROFILED_SOURCES:
+        visit(os.path.join(csrc, name))
+    return sorted(seen)
+
+
+def kernel_source_hash():
+    """Hash of the code (comments and blank lines ignored) of the files that
+    build and launch the verify kernel."""
+    h = hashlib.sha256()
+    for path in profiled_source_files():
+        with open(path, encoding="utf-8") as f:
+            h.update(os.path.relpath(path, ROOT).encode() + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,9 +1,10 @@
-"""ISD verify-and-propose on one B300: Python binding of libisd (include/isd.h).
+"""ISD verify-and-propose on one B300: Python binding of libisd (include/isd.h,
+include/isd_kv.h).
 
 The computation runs in libisd.so (hand-written sm_103a CUDA); this package
 marshals torch CUDA tensors into its C ABI.  ``workloads`` makes seeded
 synthetic inputs.
 """
-from .api import (ProposeOut, VerifyOut, isd_alpha, isd_propose, isd_propose_workspace_bytes,  # noqa: F401
-                  isd_verify, isd_verify_propose, isd_verify_propose_workspace_bytes, isd_verify_workspace_bytes,
-                  workspace)
+from .api import (ProposeOut, VerifyOut, isd_alpha, isd_kv_commit, isd_propose,  # noqa: F401
+                  isd_propose_workspace_bytes, isd_verify, isd_verify_propose,
+                  isd_verify_propose_workspace_bytes, isd_verify_workspace_bytes, workspace)

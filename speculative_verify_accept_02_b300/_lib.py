@@ -1,4 +1,4 @@
-"""Loads libisd.so (the C ABI of include/isd.h) with ctypes.
+"""Loads libisd.so (the C ABI of include/isd.h and include/isd_kv.h) with ctypes.
 
 There is no fallback: if the library is missing or fails to load, every
 entry point raises.
@@ -12,7 +12,11 @@ LIBRARY = os.path.join(HERE, "libisd.so")
 ISD_OK, ISD_ERR_INVALID_ARG, ISD_ERR_UNSUPPORTED, ISD_ERR_WORKSPACE, ISD_ERR_CUDA = range(5)
 ISD_DTYPE_BF16, ISD_DTYPE_F32 = 0, 1
 
-# Every symbol include/isd.h declares, with (restype, argtypes).
+# KV commit status bits (ISD_KV_ERR_* of include/isd_kv.h).
+ISD_KV_ERR_STATE, ISD_KV_ERR_ACCEPT, ISD_KV_ERR_SLOT, ISD_KV_ERR_POOL, ISD_KV_ERR_CAPACITY = 1, 2, 4, 8, 16
+ISD_KV_MAX_SEQS = 1 << 24
+
+# Every symbol the headers under include/ declare, with (restype, argtypes).
 SIGNATURES = {
     "isd_verify_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "isd_verify": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_int,
@@ -36,6 +40,8 @@ SIGNATURES = {
     "isd_alpha": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                             C.c_void_p]),
     "isd_status_string": (C.c_char_p, [C.c_int]),
+    "isd_kv_commit": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "isd_verify_noalloc": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_int,
                                      C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_uint64,
                                      C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,

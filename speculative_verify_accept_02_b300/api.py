@@ -1,5 +1,5 @@
-"""Python binding of libisd: the entry points of include/isd.h over torch
-CUDA tensors.  Argument marshalling only — every step of the computation runs
+"""Python binding of libisd: the entry points of include/isd.h and
+include/isd_kv.h over torch CUDA tensors.  Argument marshalling only — every step of the computation runs
 in the library's kernels; torch supplies device memory and the stream.
 
 Tensors:
@@ -196,3 +196,38 @@ def isd_alpha(ratio: torch.Tensor, seq_offsets: torch.Tensor, *, total: Optional
                                    per.data_ptr(), mean.data_ptr(), _stream(device, stream))
     _lib.check("isd_alpha", status)
     return per, mean
+
+
+KV_FIELDS = ("table", "seq_len", "pend", "alloc", "free_slots", "free_top")
+
+
+def isd_kv_commit(state: dict, accept_len: torch.Tensor, num_masks: int, *,
+                  status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One KV-slot commit of the stationary batch (include/isd_kv.h).
+
+    state: int32 CUDA tensors under the keys table [C, ld] (row-major),
+    seq_len, pend, alloc [C], free_slots [pool], free_top [1]; updated in
+    place when the commit succeeds.  accept_len [C] int32: the step's accept
+    lengths by batch position (read where pend > 0).  Returns the status
+    tensor [1] int32 on the device (0 = committed, else the OR of the
+    ISD_KV_ERR_* bits and nothing changed); reading it is a device->host
+    sync the caller may defer."""
+    t = state["table"]
+    if t.dim() != 2:
+        raise ValueError("table must be 2-D [num_seqs, ld]")
+    ptrs = {k: _int32(state[k], k) for k in KV_FIELDS}
+    C, ld = t.shape
+    for k in ("seq_len", "pend", "alloc"):
+        if state[k].numel() != C:
+            raise ValueError(f"{k} must have one entry per sequence")
+    if state["free_top"].numel() != 1 or accept_len.numel() != C:
+        raise ValueError("free_top must hold one entry and accept_len one per sequence")
+    device = t.device
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=device)
+    rc = _lib.load().isd_kv_commit(ptrs["table"], ld, ptrs["seq_len"], ptrs["pend"], ptrs["alloc"],
+                                   ptrs["free_slots"], ptrs["free_top"], state["free_slots"].numel(),
+                                   _int32(accept_len, "accept_len"), C, int(num_masks),
+                                   _int32(status, "status"), _stream(device, stream))
+    _lib.check("isd_kv_commit", rc)
+    return status

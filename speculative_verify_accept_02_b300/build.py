@@ -11,14 +11,14 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libisd.so")
-SOURCES = ["isd_api.cu", "isd_verify.cu", "isd_propose.cu", "isd_alpha.cu", "isd_noalloc.cu"]
+SOURCES = ["isd_api.cu", "isd_verify.cu", "isd_propose.cu", "isd_alpha.cu", "isd_noalloc.cu", "isd_kv.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "isd.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
 

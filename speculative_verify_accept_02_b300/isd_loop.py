@@ -27,6 +27,13 @@ The loop itself is host orchestration: it gathers each step's rows, calls
 for every sequence that proposes, reads back the accept lengths and
 proposals, and advances per-sequence state.  The Philox offset advances by
 one per step.
+
+With ``kv_len`` set, the loop also keeps the batch's KV-slot state and runs
+``isd_kv_commit`` after every step (§3.3: the stationary-batch loop's batched
+slot scatter and trim of rejected and masked entries): each sequence starts
+with one prompt token (x_last) and nothing cached, so after every step its
+cache holds exactly the tokens it has emitted (all but the newest, plus the
+prompt token).
 """
 from dataclasses import dataclass, field
 from typing import List
@@ -87,10 +94,23 @@ class TableModel:
 
 
 class CudaBackend:
-    """The library's entry points (isd_verify, isd_propose) on CUDA tensors."""
+    """The library's entry points (isd_verify, isd_propose, isd_kv_commit)
+    on CUDA tensors."""
 
     def __init__(self, device="cuda"):
         self.device = torch.device(device)
+
+    def kv_state(self, state):
+        return state.to_torch(self.device)
+
+    def kv_commit(self, handle, accept, num_masks) -> int:
+        from .api import isd_kv_commit
+        acc = torch.as_tensor(np.asarray(accept, np.int32), device=self.device)
+        return int(isd_kv_commit(handle, acc, num_masks).item())
+
+    def kv_read(self, handle):
+        from .workloads import KVState
+        return KVState.from_torch(handle)
 
     def verify(self, p, q, tokens, offs, temp, seed, offset):
         from .api import isd_verify
@@ -140,7 +160,8 @@ class ISDLoop:
     (proposals, valid), over the library's layout (include/isd.h).
     """
 
-    def __init__(self, model: TableModel, num_seqs: int, stride: int, backend, seed: int = 0):
+    def __init__(self, model: TableModel, num_seqs: int, stride: int, backend, seed: int = 0,
+                 kv_len: int = 0):
         if not 2 <= stride <= 32:
             raise ValueError("stride n must lie in [2, 32] (n - 1 proposals, one anchor row more)")
         self.model, self.C, self.n, self.backend, self.seed = model, num_seqs, stride, backend, seed
@@ -149,6 +170,17 @@ class ISDLoop:
         self.tokens: List[List[int]] = [[] for _ in range(num_seqs)]
         self.stats = LoopStats(per_seq_tokens=[0] * num_seqs)
         self.offset = 0
+        self.kv = None
+        if kv_len:
+            # every row holds the cache of kv_len positions; the pool backs all rows
+            from .workloads import make_kv_state
+            self.kv = backend.kv_state(make_kv_state(num_seqs, kv_len, num_seqs * kv_len, 0, seed=seed))
+            self._kv_commit(np.zeros(num_seqs, np.int32))  # admission: the first forward's slots
+
+    def _kv_commit(self, accept):
+        status = self.backend.kv_commit(self.kv, accept, self.n - 1)
+        if status != 0:
+            raise RuntimeError(f"isd_kv_commit refused the step (status {status})")
 
     def _propose(self, jobs):
         """One isd_propose call for every proposing sequence of the step, so
@@ -177,6 +209,7 @@ class ISDLoop:
     def step(self):
         L = self.n - 1
         st = self.stats
+        kv_accept = np.zeros(self.C, np.int32)         # by batch position, read where proposals were pending
         ver = [i for i in range(self.C) if self.pending[i] is not None]
         jobs = [(i, int(self.pos[i]), True) for i in range(self.C) if self.pending[i] is None]
         if ver:  # fused steps: verify the pending proposals
@@ -193,6 +226,7 @@ class ISDLoop:
             assert np.all(acc >= 0), acc
             for j, i in enumerate(ver):
                 a = int(acc[j])
+                kv_accept[i] = a
                 emitted = out[j * (L + 1): j * (L + 1) + a + 1]
                 self.tokens[i].extend(int(x) for x in emitted)
                 st.tokens += a + 1
@@ -214,6 +248,8 @@ class ISDLoop:
                     self.pos[i] += 1
                     props = props[1:]
                 self.pending[i] = np.asarray(props, dtype=np.int32)
+        if self.kv is not None:
+            self._kv_commit(kv_accept)
         st.forwards += self.C
         st.steps += 1
         self.offset += 1

@@ -9,7 +9,7 @@ import pytest
 from speculative_verify_accept_02_b300 import _lib, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "isd.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))]
 
 
 @pytest.fixture(scope="module")
@@ -19,7 +19,7 @@ def lib():
 
 
 def declared_symbols():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"ISD_API\s+[\w\s\*]+?\b(isd_\w+)\s*\(", text)))
 
 
@@ -27,7 +27,7 @@ def test_header_declares_the_entry_points():
     names = declared_symbols()
     for n in ("isd_verify", "isd_verify_relaxed", "isd_verify_propose", "isd_propose", "isd_alpha",
               "isd_verify_workspace_bytes", "isd_verify_propose_workspace_bytes",
-              "isd_propose_workspace_bytes", "isd_status_string"):
+              "isd_propose_workspace_bytes", "isd_status_string", "isd_kv_commit"):
         assert n in names
 
 
@@ -142,6 +142,25 @@ def test_propose_and_alpha_host_checks(lib):
     assert lib.isd_alpha(FAKE, FAKE, 0, 0, FAKE, FAKE, None) == _lib.ISD_OK
     assert lib.isd_alpha(None, FAKE, 3, 4, FAKE, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
     assert lib.isd_alpha(FAKE, FAKE, -3, 4, FAKE, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
+
+
+def _kv_commit(lib, **kw):
+    args = dict(table=FAKE, ld=64, seq_len=FAKE, pend=FAKE, alloc=FAKE, free_slots=FAKE, free_top=FAKE,
+                pool=1024, accept=FAKE, C=4, M=7, status=FAKE, stream=None)
+    args.update(kw)
+    return lib.isd_kv_commit(*args.values())
+
+
+def test_kv_commit_host_checks(lib):
+    """Bad sizes and missing pointers are refused before any launch (a
+    valid call always launches: even an empty batch writes its status)."""
+    for kw in (dict(C=-1), dict(ld=0), dict(pool=-1), dict(M=-1), dict(M=32), dict(status=None),
+               dict(free_top=None), dict(free_slots=None), dict(table=None), dict(seq_len=None),
+               dict(pend=None), dict(alloc=None), dict(accept=None)):
+        assert _kv_commit(lib, **kw) == _lib.ISD_ERR_INVALID_ARG, kw
+    assert _kv_commit(lib, C=_lib.ISD_KV_MAX_SEQS + 1) == _lib.ISD_ERR_UNSUPPORTED
+    # Pool and batch pointers are only required when there is something behind them.
+    assert _kv_commit(lib, C=-1, table=None, seq_len=None) == _lib.ISD_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -43,3 +43,14 @@ def test_source_hash_ignores_comments_only():
     assert bench._strip_comments(src) == bench._strip_comments(src.replace("note", "other"))
     assert bench._strip_comments(src) != bench._strip_comments(src.replace("int b", "int c"))
     assert '"x//y"' in bench._strip_comments(src)
+
+
+def test_profiled_sources_are_the_verify_kernels():
+    """The traffic key covers the verify kernel's translation unit, the host
+    file that launches it and every local header they include, and nothing
+    else (another kernel's source may change without voiding the counters)."""
+    names = {os.path.relpath(p, ROOT) for p in bench.profiled_source_files()}
+    csrc = "speculative_verify_accept_02_b300/csrc/"
+    assert {csrc + "isd_verify.cu", csrc + "isd_api.cu", csrc + "isd_device.cuh", csrc + "isd_internal.h",
+            "include/isd.h"} <= names
+    assert csrc + "isd_kv.cu" not in names and csrc + "isd_propose.cu" not in names

@@ -28,6 +28,15 @@ class OracleBackend:
         op = oracle.propose(workloads.host_logits(qnew), V, offs, temp, seed, offset)
         return op["proposals"], op["valid"]
 
+    def kv_state(self, state):
+        return state.copy()
+
+    def kv_commit(self, handle, accept, num_masks):
+        return oracle.kv_commit(handle, accept, num_masks)
+
+    def kv_read(self, handle):
+        return handle.copy()
+
 
 def chain_tpf(n, p):
     """Tokens per forward from the stationary law of the two-state step chain:
@@ -104,3 +113,33 @@ def test_loop_on_cuda_extremes():
 def test_loop_on_cuda_tpf_law():
     assert torch.cuda.is_available(), "GPU test needs a CUDA device"
     _law(CudaBackend(), 4096, "cuda", C=64, S=200)
+
+
+def _kv_loop(backend, vocab, device):
+    """The loop with its KV-slot state (Summary §3.3): after every step each
+    sequence caches exactly as many entries as it has emitted tokens (the
+    prompt token plus all emitted but the newest), its next forward verifies
+    exactly its pending proposals, and every pool slot is free or cached
+    once."""
+    n, C, S = 4, 6, 25
+    loop = ISDLoop(TableModel(vocab, 0.6, entries=9, support=32, seed=4, device=device), C, n, backend,
+                   kv_len=2 + S * n + 2 * n)
+    for _ in range(S):
+        st = loop.step()
+        kv = backend.kv_read(loop.kv)
+        assert list(kv.seq_len) == st.per_seq_tokens
+        assert list(kv.pend) == [0 if p is None else len(p) for p in loop.pending]
+        assert list(kv.alloc) == [1 + int(p) + n - 1 for p in kv.pend]
+        live = [kv.table[i, :kv.seq_len[i] + kv.alloc[i]] for i in range(C)]
+        used = np.concatenate(live + [kv.free_slots[:kv.free_top[0]]])
+        assert np.array_equal(np.sort(used), np.arange(kv.pool_size))
+
+
+def test_loop_kv_on_oracle():
+    _kv_loop(OracleBackend(), 256, "cpu")
+
+
+@pytest.mark.gpu
+def test_loop_kv_on_cuda():
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    _kv_loop(CudaBackend(), 4096, "cuda")
