@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--separate", action="store_true",
                     help="time isd_verify then isd_propose (two launches) instead of isd_verify_propose")
+    ap.add_argument("--row", choices=["step", "kv"], default="step",
+                    help="kv: time the KV-slot commit of the stationary batch (isd_kv_commit) instead")
     return ap.parse_args()
 
 
@@ -499,10 +501,93 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+KV_NUM_SEQS, KV_MASKS = 64, 7
+
+
+def run_kv(args):
+    """Commits per second of isd_kv_commit on a stationary batch of C=64
+    sequences at stride 8 (M=7 masks), one launch per commit.  Each commit
+    takes a fresh accept length per sequence, uniform on 0..7 (read only
+    where proposals are pending); the state evolves as in a decode run.
+    The floor is the same kernel on an empty batch (launch and one pass of
+    its checks): the commit cannot be faster."""
+    import torch
+    from speculative_verify_accept_02_b300 import _lib, build, isd_kv_commit, workloads
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    _lib.load()
+    C, M = KV_NUM_SEQS, KV_MASKS
+    K, W, E = args.steps, max(3, args.warmup), args.e2e_steps
+    n = K + W + E
+    ld = n * (M + 1) + 2 * M + 2
+    state = workloads.make_kv_state(C, ld, C * ld, 0, seed=7).to_torch(dev)
+    rng = np.random.default_rng(7)
+    accept = torch.from_numpy(rng.integers(0, M + 1, (n, C)).astype(np.int32)).to(dev)
+    status = torch.empty(n, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for j in range(W):
+        isd_kv_commit(state, accept[j], M, status=status[j:j + 1], stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            isd_kv_commit(state, accept[W + k], M, status=status[W + k:W + k + 1], stream=stream)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+    us = 1e3 * sum(a.elapsed_time(b) for a, b in ev) / K
+    # e2e: the step's accept lengths come from the host, the status goes back
+    host_acc = accept[W + K:].cpu().pin_memory()
+    host_status = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    dev_acc = torch.empty(C, dtype=torch.int32, device=dev)
+    e2e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E)]
+    for k in range(E):
+        e2e[k][0].record(stream)
+        dev_acc.copy_(host_acc[k], non_blocking=True)
+        isd_kv_commit(state, dev_acc, M, status=status[W + K + k:W + K + k + 1], stream=stream)
+        host_status.copy_(status[W + K + k:W + K + k + 1], non_blocking=True)
+        e2e[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_us = 1e3 * sum(a.elapsed_time(b) for a, b in e2e) / max(1, E)
+    refused = int((status != 0).sum().item())
+    # floor: the same kernel on an empty batch
+    empty = workloads.make_kv_state(0, 1, 1, [], seed=0).to_torch(dev)
+    none = torch.empty(0, dtype=torch.int32, device=dev)
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        fev[k][0].record(stream)
+        isd_kv_commit(empty, none, M, status=status[:1], stream=stream)
+        fev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    floor_us = 1e3 * sum(a.elapsed_time(b) for a, b in fev) / K
+    line = {
+        "metric": f"KV-slot commits/sec (isd_kv_commit), C={C} stride {M + 1}", "value": 1e6 / us,
+        "unit": "commits/s", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": us / 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"stationary batch of {C} sequences, {M} masks, accept lengths uniform on 0..{M}",
+                   "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write between timed commits",
+                   "refused_commits": refused},
+        "floor": {"kind": "the same kernel on an empty batch", "us": floor_us, "frac": floor_us / us},
+        "e2e": {"value": 1e6 / e2e_us, "unit": "commits/s", "h2d_bytes_per_step": C * 4, "d2h_bytes_per_step": 4},
+        "gpu_launches": K,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.row == "kv":
+        run_kv(args)
     else:
         run_ours(args)
 
