@@ -139,7 +139,10 @@ ORACLE_API double oracle_log_softmax_at(const double* logits, int V, double T, i
  * probabilities; top_k <= 0 keeps every id); of those, in the same order,
  * keep the shortest prefix whose probability, renormalised over the top_k,
  * adds up to at least top_p (top_p >= 1 keeps them all); out = the kept
- * probabilities renormalised, 0 elsewhere. */
+ * probabilities renormalised, 0 elsewhere.  `cut_margin` (optional) receives
+ * how far the top-p cut is from moving: the smaller of (running share at the
+ * last kept id - top_p) and (top_p - running share one id earlier); +inf
+ * when top_p >= 1. */
 typedef struct { double p; int id; } ranked_id;
 
 static int by_rank(const void* a, const void* b) {
@@ -150,7 +153,7 @@ static int by_rank(const void* a, const void* b) {
 }
 
 ORACLE_API void oracle_filtered_probs(const double* logits, int V, double T, int top_k, double top_p,
-                                      double* out) {
+                                      double* out, double* cut_margin) {
     oracle_softmax(logits, V, T, out);
     ranked_id* r = (ranked_id*)malloc(sizeof(ranked_id) * (size_t)V);
     for (int v = 0; v < V; ++v) { r[v].p = out[v]; r[v].id = v; }
@@ -159,13 +162,18 @@ ORACLE_API void oracle_filtered_probs(const double* logits, int V, double T, int
     double sk = 0.0;
     for (int j = 0; j < kept; ++j) sk += r[j].p;
     int n = kept;
+    double margin = INFINITY;
     if (top_p < 1.0) {
-        double cum = 0.0;
+        double cum = 0.0, prev = 0.0;
         for (int j = 0; j < kept; ++j) {
+            prev = cum;
             cum += r[j].p / sk;
             if (cum >= top_p) { n = j + 1; break; }
         }
+        margin = cum - top_p;
+        if (n > 1 && top_p - prev < margin) margin = top_p - prev;
     }
+    if (cut_margin) *cut_margin = margin;
     double total = 0.0;
     for (int j = 0; j < n; ++j) total += r[j].p;
     for (int v = 0; v < V; ++v) out[v] = 0.0;

@@ -47,7 +47,8 @@ def _declare(L):
                                     C.c_double, C.POINTER(C.c_int32), _ip, _dp,
                                     C.POINTER(C.c_double), _dp, C.POINTER(C.c_double), C.c_double]
     L.oracle_verify_one.restype = None
-    L.oracle_filtered_probs.argtypes = [_dp, C.c_int, C.c_double, C.c_int, C.c_double, _dp]
+    L.oracle_filtered_probs.argtypes = [_dp, C.c_int, C.c_double, C.c_int, C.c_double, _dp,
+                                        C.POINTER(C.c_double)]
     L.oracle_filtered_probs.restype = None
     L.oracle_ratio_relaxed.argtypes = [_dp, _dp, C.c_int, C.c_double, C.c_int, C.c_double]
     L.oracle_ratio_relaxed.restype = C.c_double
@@ -154,13 +155,15 @@ class Oracle:
         v = self.lib.oracle_icdf(ww, ww.size, float(u), C.byref(m))
         return v, m.value
 
-    def filtered_probs(self, logits, T, top_k, top_p):
+    def filtered_probs(self, logits, T, top_k, top_p, with_margin=False):
         """softmax(logits/T) after the top-k, then top-p filter, renormalised
-        (the pages' evaluation sampling setting)."""
+        (the pages' evaluation sampling setting).  with_margin: also return
+        the distance of the top-p cut from moving."""
         z = _d(logits)
         out = np.empty(z.size, dtype=np.float64)
-        self.lib.oracle_filtered_probs(z, z.size, float(T), int(top_k), float(top_p), out)
-        return out
+        m = C.c_double()
+        self.lib.oracle_filtered_probs(z, z.size, float(T), int(top_k), float(top_p), out, C.byref(m))
+        return (out, m.value) if with_margin else out
 
     def verify_filtered(self, p_logits, q_logits, vocab, tokens, seq_offsets, temperature, seed, offset,
                         top_k, top_p):
@@ -168,8 +171,11 @@ class Oracle:
         (p~, q~): ratio min(1, p~(x)/q~(x)) (1 where q~(x) = 0), strict
         acceptance, correction from normalize(max(0, p~_j - q~_j)) (p~_j if that
         is all zero), bonus from p~_{L+1}.  T = 0 sequences are unaffected by
-        the filters and follow verify().  Same outputs as verify(); margins
-        are not computed."""
+        the filters and follow verify().  Same outputs as verify(), with the
+        margins of the decisions: accept_margin [sum L] (|u - ratio| of each
+        tested position, +inf for the rest), token_margin [C] (inverse-CDF
+        margin of the correction or bonus draw) and cut_margin [C] (the
+        smallest top-p cut margin of the sequence's rows)."""
         offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
         C_ = offs.size - 1
         total = int(offs[-1])
@@ -177,7 +183,9 @@ class Oracle:
         toks = np.ascontiguousarray(tokens, dtype=np.int32)
         P, Q = _decode(p_logits, vocab), _decode(q_logits, vocab)
         out = dict(accept_len=np.full(C_, -2, np.int32), out_tokens=np.full(total + C_, -2, np.int32),
-                   ratio=np.full(total, np.nan), alpha=np.full(C_, np.nan))
+                   ratio=np.full(total, np.nan), alpha=np.full(C_, np.nan),
+                   accept_margin=np.full(total, np.inf), token_margin=np.full(C_, np.inf),
+                   cut_margin=np.full(C_, np.inf))
         for i in range(C_):
             s, L, T = int(offs[i]), int(offs[i + 1] - offs[i]), float(temp[i])
             if T == 0.0 or not (1 <= L <= 32) or not math.isfinite(T) or T < 0 or (0 < T < 1.17549435e-38) \
@@ -185,28 +193,35 @@ class Oracle:
                 one = self.verify(p_logits, q_logits, vocab, tokens, seq_offsets, temperature, seed, offset,
                                   seqs=[i])
                 for k in out:
-                    if k == "accept_len" or k == "alpha":
+                    if k in ("accept_len", "alpha", "token_margin"):
                         out[k][i] = one[k][i]
-                    elif k == "ratio":
+                    elif k in ("ratio", "accept_margin"):
                         out[k][s:s + max(L, 0)] = one[k][s:s + max(L, 0)]
-                    else:
+                    elif k == "out_tokens":
                         out[k][s + i: s + i + max(L, 0) + 1] = one[k][s + i: s + i + max(L, 0) + 1]
                 continue
-            pt = [self.filtered_probs(P[s + i + k], T, top_k, top_p) for k in range(L + 1)]
-            qt = [self.filtered_probs(Q[s + k], T, top_k, top_p) for k in range(L)]
+            pm = [self.filtered_probs(P[s + i + k], T, top_k, top_p, with_margin=True) for k in range(L + 1)]
+            qm = [self.filtered_probs(Q[s + k], T, top_k, top_p, with_margin=True) for k in range(L)]
+            pt, qt = [m[0] for m in pm], [m[0] for m in qm]
+            out["cut_margin"][i] = min(m[1] for m in pm + qm)
             x = toks[s:s + L]
             ratio = np.array([1.0 if qt[k][x[k]] == 0.0 else min(1.0, pt[k][x[k]] / qt[k][x[k]])
                               for k in range(L)])
             a = 0
-            while a < L and self.uniform(seed, offset, i, a + 1, TAG_ACCEPT) < ratio[a]:
+            while a < L:
+                u = self.uniform(seed, offset, i, a + 1, TAG_ACCEPT)
+                out["accept_margin"][s + a] = abs(u - ratio[a])
+                if not u < ratio[a]:
+                    break
                 a += 1
             if a < L:
                 w = np.maximum(pt[a] - qt[a], 0.0)
                 if not w.sum() > 0.0:
                     w = pt[a]
-                tok = self.icdf(w, self.uniform(seed, offset, i, a + 1, TAG_CORRECT))[0]
+                tok, tm = self.icdf(w, self.uniform(seed, offset, i, a + 1, TAG_CORRECT))
             else:
-                tok = self.icdf(pt[L], self.uniform(seed, offset, i, L + 1, TAG_BONUS))[0]
+                tok, tm = self.icdf(pt[L], self.uniform(seed, offset, i, L + 1, TAG_BONUS))
+            out["token_margin"][i] = tm
             out["accept_len"][i] = a
             out["ratio"][s:s + L] = ratio
             out["alpha"][i] = ratio.mean()
@@ -219,7 +234,8 @@ class Oracle:
     def propose_filtered(self, qnew_logits, vocab, seq_offsets, temperature, seed, offset, top_k, top_p,
                          accept_len=None):
         """Proposals drawn from the filtered softmax(qnew/T) (argmax at T = 0),
-        with propose()'s validity rules."""
+        with propose()'s validity rules; margin [sum L] is the smaller of the
+        draw's inverse-CDF margin and its row's top-p cut margin."""
         base = self.propose(qnew_logits, vocab, seq_offsets, temperature, seed, offset, accept_len=accept_len)
         offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
         temp = np.ascontiguousarray(temperature, dtype=np.float32)
@@ -229,8 +245,9 @@ class Oracle:
                 continue
             for m in range(1, int(offs[i + 1] - offs[i]) + 1):
                 r = int(offs[i]) + m - 1
-                w = self.filtered_probs(Qn[r], float(temp[i]), top_k, top_p)
-                base["proposals"][r] = self.icdf(w, self.uniform(seed, offset, i, m, TAG_PROPOSE))[0]
+                w, cm = self.filtered_probs(Qn[r], float(temp[i]), top_k, top_p, with_margin=True)
+                base["proposals"][r], tm = self.icdf(w, self.uniform(seed, offset, i, m, TAG_PROPOSE))
+                base["margin"][r] = min(tm, cm)
         return base
 
     def ratio_relaxed(self, P, Q, T, x, tau):

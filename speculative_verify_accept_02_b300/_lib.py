@@ -1,4 +1,4 @@
-"""Loads libisd.so (the C ABI of include/isd.h and include/isd_kv.h) with ctypes.
+"""Loads libisd.so (the C ABI declared under include/) with ctypes.
 
 There is no fallback: if the library is missing or fails to load, every
 entry point raises.
@@ -15,6 +15,7 @@ ISD_DTYPE_BF16, ISD_DTYPE_F32 = 0, 1
 # KV commit status bits (ISD_KV_ERR_* of include/isd_kv.h).
 ISD_KV_ERR_STATE, ISD_KV_ERR_ACCEPT, ISD_KV_ERR_SLOT, ISD_KV_ERR_POOL, ISD_KV_ERR_CAPACITY = 1, 2, 4, 8, 16
 ISD_KV_MAX_SEQS = 1 << 24
+ISD_FILTER_MAX_TOP_K = 64
 
 # Every symbol the headers under include/ declare, with (restype, argtypes).
 SIGNATURES = {
@@ -40,6 +41,15 @@ SIGNATURES = {
     "isd_alpha": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                             C.c_void_p]),
     "isd_status_string": (C.c_char_p, [C.c_int]),
+    "isd_verify_filtered_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
+    "isd_verify_filtered": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_int,
+                                      C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_uint64,
+                                      C.c_uint64, C.c_int, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "isd_propose_filtered_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
+    "isd_propose_filtered": (C.c_int, [C.c_void_p, C.c_int64, C.c_int, C.c_int, C.c_void_p, C.c_int,
+                                       C.c_int, C.c_void_p, C.c_uint64, C.c_uint64, C.c_int, C.c_float,
+                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "isd_kv_commit": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "isd_verify_noalloc": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_int,

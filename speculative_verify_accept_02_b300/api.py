@@ -1,5 +1,5 @@
-"""Python binding of libisd: the entry points of include/isd.h and
-include/isd_kv.h over torch CUDA tensors.  Argument marshalling only — every step of the computation runs
+"""Python binding of libisd: the entry points declared under include/
+(isd.h, isd_filter.h, isd_kv.h) over torch CUDA tensors.  Argument marshalling only — every step of the computation runs
 in the library's kernels; torch supplies device memory and the stream.
 
 Tensors:
@@ -181,6 +181,71 @@ def isd_propose(qnew: torch.Tensor, seq_offsets: torch.Tensor, temperature: torc
         _f32(temperature, "temperature"), int(seed), int(offset), acc, out.proposals.data_ptr(),
         out.valid.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
     _lib.check("isd_propose", status)
+    return out
+
+
+def isd_verify_filtered_workspace_bytes(num_seqs: int, total: int, top_k: int) -> int:
+    return int(_lib.load().isd_verify_filtered_workspace_bytes(num_seqs, total, top_k))
+
+
+def isd_propose_filtered_workspace_bytes(num_seqs: int, total: int, top_k: int) -> int:
+    return int(_lib.load().isd_propose_filtered_workspace_bytes(num_seqs, total, top_k))
+
+
+def isd_verify_filtered(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, seq_offsets: torch.Tensor,
+                        temperature: torch.Tensor, seed: int = 0, offset: int = 0, *, top_k: int = 50,
+                        top_p: float = 0.95, vocab: Optional[int] = None, total: Optional[int] = None,
+                        out: Optional[VerifyOut] = None, ws: Optional[torch.Tensor] = None,
+                        stream=None) -> VerifyOut:
+    """isd_verify_filtered: isd_verify with p and q under the top-k, then
+    top-p filters (include/isd_filter.h)."""
+    device = p.device
+    C = seq_offsets.numel() - 1
+    total = _total(seq_offsets, total)
+    V = p.shape[1] if vocab is None else int(vocab)
+    if p.dtype != q.dtype:
+        raise TypeError("p and q must share a dtype")
+    pp, ldp = _rows(p, "p")
+    qp, ldq = _rows(q, "q")
+    if out is None:
+        out = VerifyOut(torch.empty(C, dtype=torch.int32, device=device),
+                        torch.empty(total + C, dtype=torch.int32, device=device),
+                        torch.empty(total, dtype=torch.float32, device=device),
+                        torch.empty(C, dtype=torch.float32, device=device))
+    if ws is None:
+        ws = workspace(isd_verify_filtered_workspace_bytes(C, total, top_k), device)
+    status = _lib.load().isd_verify_filtered(
+        pp, ldp, qp, ldq, _dtype_code(p), V, _int32(tokens, "tokens"), _int32(seq_offsets, "seq_offsets"),
+        C, total, _f32(temperature, "temperature"), int(seed), int(offset), int(top_k), float(top_p),
+        out.accept_len.data_ptr(), out.out_tokens.data_ptr(), out.ratio.data_ptr(), out.alpha.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
+    _lib.check("isd_verify_filtered", status)
+    return out
+
+
+def isd_propose_filtered(qnew: torch.Tensor, seq_offsets: torch.Tensor, temperature: torch.Tensor,
+                         seed: int = 0, offset: int = 0, accept_len: Optional[torch.Tensor] = None, *,
+                         top_k: int = 50, top_p: float = 0.95, vocab: Optional[int] = None,
+                         total: Optional[int] = None, out: Optional[ProposeOut] = None,
+                         ws: Optional[torch.Tensor] = None, stream=None) -> ProposeOut:
+    """isd_propose_filtered: proposals drawn from the filtered softmax(qnew/T)."""
+    device = qnew.device
+    C = seq_offsets.numel() - 1
+    total = _total(seq_offsets, total)
+    V = qnew.shape[1] if vocab is None else int(vocab)
+    qp, ld = _rows(qnew, "qnew")
+    if out is None:
+        out = ProposeOut(torch.empty(total, dtype=torch.int32, device=device),
+                         torch.empty(C, dtype=torch.uint8, device=device))
+    if ws is None:
+        ws = workspace(isd_propose_filtered_workspace_bytes(C, total, top_k), device)
+    acc = None if accept_len is None else _int32(accept_len, "accept_len")
+    status = _lib.load().isd_propose_filtered(
+        qp, ld, _dtype_code(qnew), V, _int32(seq_offsets, "seq_offsets"), C, total,
+        _f32(temperature, "temperature"), int(seed), int(offset), int(top_k), float(top_p), acc,
+        out.proposals.data_ptr(), out.valid.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
+        _stream(device, stream))
+    _lib.check("isd_propose_filtered", status)
     return out
 
 

@@ -11,7 +11,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libisd.so")
-SOURCES = ["isd_api.cu", "isd_verify.cu", "isd_propose.cu", "isd_alpha.cu", "isd_noalloc.cu", "isd_kv.cu"]
+SOURCES = ["isd_api.cu", "isd_verify.cu", "isd_propose.cu", "isd_alpha.cu", "isd_noalloc.cu", "isd_kv.cu",
+           "isd_filter.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

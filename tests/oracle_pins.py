@@ -405,6 +405,11 @@ def pin_filter_known(orc):
     sq = np.sqrt(pr)
     assert np.allclose(orc.filtered_probs(lg, 2.0, 2, 1.0), [sq[0] / (sq[0] + sq[1]), sq[1] / (sq[0] + sq[1]), 0, 0],
                        atol=1e-12)
+    # The cut's margin: shares 0.5, 0.8 of the whole row at top-p 0.75 -> min(0.05, 0.25);
+    # within the top 3 (mass 0.95) at top-p 0.82: shares 0.5/0.95, 0.8/0.95 -> min(0.8/0.95 - 0.82, 0.82 - 0.5/0.95).
+    assert abs(orc.filtered_probs(lg, 1.0, 0, 0.75, with_margin=True)[1] - 0.05) < 1e-12
+    assert abs(orc.filtered_probs(lg, 1.0, 3, 0.82, with_margin=True)[1] - (0.8 / 0.95 - 0.82)) < 1e-12
+    assert orc.filtered_probs(lg, 1.0, 3, 1.0, with_margin=True)[1] == np.inf
 
 
 def pin_filtered_verify_law(orc):

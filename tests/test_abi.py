@@ -27,7 +27,8 @@ def test_header_declares_the_entry_points():
     names = declared_symbols()
     for n in ("isd_verify", "isd_verify_relaxed", "isd_verify_propose", "isd_propose", "isd_alpha",
               "isd_verify_workspace_bytes", "isd_verify_propose_workspace_bytes",
-              "isd_propose_workspace_bytes", "isd_status_string", "isd_kv_commit"):
+              "isd_propose_workspace_bytes", "isd_status_string", "isd_kv_commit", "isd_verify_filtered",
+              "isd_propose_filtered"):
         assert n in names
 
 
@@ -142,6 +143,44 @@ def test_propose_and_alpha_host_checks(lib):
     assert lib.isd_alpha(FAKE, FAKE, 0, 0, FAKE, FAKE, None) == _lib.ISD_OK
     assert lib.isd_alpha(None, FAKE, 3, 4, FAKE, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
     assert lib.isd_alpha(FAKE, FAKE, -3, 4, FAKE, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
+
+
+def _verify_filtered(lib, **kw):
+    args = dict(p=FAKE, ldp=1024, q=FAKE, ldq=1024, dtype=0, vocab=1024, tokens=FAKE, offs=FAKE,
+                C=2, total=4, temp=FAKE, seed=0, offset=0, top_k=50, top_p=0.95, acc=FAKE, out=FAKE,
+                ratio=FAKE, alpha=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return lib.isd_verify_filtered(*args.values())
+
+
+def _propose_filtered(lib, **kw):
+    args = dict(qnew=FAKE, ld=1024, dtype=0, vocab=1024, offs=FAKE, C=2, total=4, temp=FAKE, seed=0,
+                offset=0, top_k=50, top_p=0.95, acc=None, props=FAKE, valid=FAKE, ws=FAKE, wsb=1 << 30,
+                stream=None)
+    args.update(kw)
+    return lib.isd_propose_filtered(*args.values())
+
+
+def test_filtered_host_checks(lib):
+    """top_k in [1, 64] and top_p in (0, 1]; the rest as isd_verify and
+    isd_propose; every refusal happens before a launch."""
+    for fn in (_verify_filtered, _propose_filtered):
+        assert fn(lib, C=0) == _lib.ISD_OK
+        for kw in (dict(top_k=0), dict(top_k=65), dict(top_p=0.0), dict(top_p=-0.5), dict(top_p=1.5),
+                   dict(top_p=float("nan")), dict(C=-1), dict(vocab=0), dict(dtype=3), dict(ws=None)):
+            assert fn(lib, **kw) == _lib.ISD_ERR_INVALID_ARG, (fn.__name__, kw)
+        assert fn(lib, wsb=16) == _lib.ISD_ERR_WORKSPACE
+        assert fn(lib, ws=FAKE + 16) == _lib.ISD_ERR_WORKSPACE
+    assert _verify_filtered(lib, p=FAKE + 2) == _lib.ISD_ERR_UNSUPPORTED
+    assert _verify_filtered(lib, ldq=1000) == _lib.ISD_ERR_INVALID_ARG
+    assert _propose_filtered(lib, qnew=FAKE + 4) == _lib.ISD_ERR_UNSUPPORTED
+    assert _propose_filtered(lib, ld=10) == _lib.ISD_ERR_INVALID_ARG
+    # 8 bytes per kept entry of every row read, 256-byte granular; 0 for a bad top_k.
+    a = lib.isd_verify_filtered_workspace_bytes(64, 512, 50)
+    assert a >= 8 * 50 * (2 * 512 + 64) and a % 256 == 0
+    assert lib.isd_propose_filtered_workspace_bytes(64, 512, 50) >= 8 * 50 * 512
+    assert lib.isd_verify_filtered_workspace_bytes(64, 512, 0) == 0
+    assert lib.isd_propose_filtered_workspace_bytes(64, 512, 65) == 0
 
 
 def _kv_commit(lib, **kw):
