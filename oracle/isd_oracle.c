@@ -20,6 +20,9 @@
  *     (the greedy, temperature-0 rule: accept while x_k is the argmax of p_k).
  *   - §3.1 Introspective-Consistency Training: logits[i] predict token[i+1]
  *     (next-token shift), which fixes which logit row scores which token.
+ *   - §3.3 I-DLM Serving Stack, the fused verification kernel: Gumbel-max
+ *     correction draws (oracle_gumbel_*, next to the uniforms below), an
+ *     exact sampler of the same distributions as the inverse-CDF draws.
  *   - §3.3 I-DLM Serving Stack, the stationary-batch loop: KV slots are
  *     allocated with a batched scatter, and the entries of rejected
  *     proposals and of mask positions are trimmed after verification
@@ -92,6 +95,52 @@ ORACLE_API double oracle_uniform(uint64_t seed, uint64_t offset, uint64_t seq, u
     uint64_t out[4];
     oracle_philox4x64_10(ctr, key, out);
     return (double)(out[0] >> 40) * (1.0 / 16777216.0);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gumbel-max draws (the sampler of the pages' fused verification kernel,   */
+/* §3.3): the id maximising log w_v + g_v, g_v = -log(-log u_v) i.i.d.      */
+/* standard Gumbel noise, is distributed as w / sum(w) (the Gumbel-max      */
+/* property).                                                               */
+/* ------------------------------------------------------------------------ */
+
+enum { GUMBEL_TAG_BASE = 16, GUMBEL_IDS_PER_BLOCK = 4 };
+
+/* The uniform of vocabulary id v in one Gumbel-max draw: counter (offset,
+ * sequence, position, 16 + purpose + 256 * (v / 4)), key (seed, 0), output
+ * word v % 4; u = (top 23 bits + 1/2) * 2^-23, strictly inside (0, 1) and
+ * exact in float and double. */
+ORACLE_API double oracle_gumbel_uniform(uint64_t seed, uint64_t offset, uint64_t seq, uint64_t pos, uint64_t tag,
+                                        uint64_t v) {
+    uint64_t ctr[4] = {offset, seq, pos, GUMBEL_TAG_BASE + tag + 256 * (v / GUMBEL_IDS_PER_BLOCK)};
+    uint64_t key[2] = {seed, 0};
+    uint64_t out[4];
+    oracle_philox4x64_10(ctr, key, out);
+    return ((double)(out[v % GUMBEL_IDS_PER_BLOCK] >> 41) + 0.5) * (1.0 / 8388608.0);
+}
+
+/* Gumbel-max draw over weights w (w_v > 0 take part): the id of the largest
+ * log w_v - log(-log u_v), the lower id on ties; -1 if no weight is
+ * positive.  `margin` (optional) receives the gap between the best and the
+ * second-best score (+inf with one candidate). */
+ORACLE_API int oracle_gumbel_draw(const double* w, int V, uint64_t seed, uint64_t offset, uint64_t seq,
+                                  uint64_t pos, uint64_t tag, double* margin) {
+    int best = -1;
+    double top = -INFINITY, second = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        if (!(w[v] > 0.0)) continue;
+        double u = oracle_gumbel_uniform(seed, offset, seq, pos, tag, (uint64_t)v);
+        double score = log(w[v]) - log(-log(u));
+        if (score > top) {
+            second = top;
+            top = score;
+            best = v;
+        } else if (score > second) {
+            second = score;
+        }
+    }
+    if (margin) *margin = best < 0 ? 0.0 : top - second;
+    return best;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -62,6 +62,11 @@ def _declare(L):
     L.oracle_propose.restype = None
     L.oracle_alpha.argtypes = [_fp, _ip, C.c_int, _dp, C.POINTER(C.c_double)]
     L.oracle_alpha.restype = None
+    L.oracle_gumbel_uniform.argtypes = [C.c_uint64] * 6
+    L.oracle_gumbel_uniform.restype = C.c_double
+    L.oracle_gumbel_draw.argtypes = [_dp, C.c_int, C.c_uint64, C.c_uint64, C.c_uint64, C.c_uint64, C.c_uint64,
+                                     C.POINTER(C.c_double)]
+    L.oracle_gumbel_draw.restype = C.c_int
     L.oracle_kv_commit.argtypes = [_ip, C.c_int64, _ip, _ip, _ip, _ip, _ip, C.c_int, _ip, C.c_int, C.c_int]
     L.oracle_kv_commit.restype = C.c_int
     L.oracle_max_threads.argtypes = [C.c_int]
@@ -248,6 +253,58 @@ class Oracle:
                 w, cm = self.filtered_probs(Qn[r], float(temp[i]), top_k, top_p, with_margin=True)
                 base["proposals"][r], tm = self.icdf(w, self.uniform(seed, offset, i, m, TAG_PROPOSE))
                 base["margin"][r] = min(tm, cm)
+        return base
+
+    def gumbel_uniform(self, seed, offset, seq, pos, tag, v):
+        """The uniform of vocabulary id v in one Gumbel-max draw, in (0, 1)."""
+        return self.lib.oracle_gumbel_uniform(seed, offset, seq, pos, tag, v)
+
+    def gumbel_draw(self, w, seed, offset, seq, pos, tag):
+        """Gumbel-max draw over weights w: (token, margin)."""
+        ww = _d(w)
+        m = C.c_double()
+        v = self.lib.oracle_gumbel_draw(ww, ww.size, seed, offset, seq, pos, tag, C.byref(m))
+        return v, m.value
+
+    def verify_gumbel(self, p_logits, q_logits, vocab, tokens, seq_offsets, temperature, seed, offset):
+        """The verify step with Gumbel-max draws for the correction and the
+        bonus token (the sampler of the pages' fused kernel) in place of
+        inverse-CDF draws; ratios, acceptance and alpha as verify().  T = 0
+        sequences and invalid ones follow verify().  Returns verify()'s
+        outputs; token_margin is the Gumbel score gap of the draw."""
+        offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+        temp = np.ascontiguousarray(temperature, dtype=np.float32)
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = self.verify(p_logits, q_logits, vocab, tokens, seq_offsets, temperature, seed, offset)
+        P, Q = _decode(p_logits, vocab), _decode(q_logits, vocab)
+        for i in range(offs.size - 1):
+            s, L, T = int(offs[i]), int(offs[i + 1] - offs[i]), float(temp[i])
+            a = int(out["accept_len"][i])
+            if a < 0 or T == 0.0:
+                continue
+            if a < L:
+                w = self.residual(P[s + i + a], Q[s + a], T)
+                tok, gap = self.gumbel_draw(w, seed, offset, i, a + 1, TAG_CORRECT)
+            else:
+                tok, gap = self.gumbel_draw(self.softmax(P[s + i + L], T), seed, offset, i, L + 1, TAG_BONUS)
+            out["out_tokens"][s + i + a] = tok
+            out["token_margin"][i] = gap
+        return out
+
+    def propose_gumbel(self, qnew_logits, vocab, seq_offsets, temperature, seed, offset, accept_len=None):
+        """Proposals by Gumbel-max draws from softmax(qnew/T) (argmax at
+        T = 0), with propose()'s validity rules; margin is the score gap."""
+        base = self.propose(qnew_logits, vocab, seq_offsets, temperature, seed, offset, accept_len=accept_len)
+        offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+        temp = np.ascontiguousarray(temperature, dtype=np.float32)
+        Qn = _decode(qnew_logits, vocab)
+        for i in range(offs.size - 1):
+            if not base["valid"][i] or temp[i] == 0.0:
+                continue
+            for m in range(1, int(offs[i + 1] - offs[i]) + 1):
+                r = int(offs[i]) + m - 1
+                w = self.softmax(Qn[r], float(temp[i]))
+                base["proposals"][r], base["margin"][r] = self.gumbel_draw(w, seed, offset, i, m, TAG_PROPOSE)
         return base
 
     def ratio_relaxed(self, P, Q, T, x, tau):

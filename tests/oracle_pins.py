@@ -569,6 +569,82 @@ def pin_invalid_inputs(orc):
 
 
 # ---------------------------------------------------------------------------
+# Gumbel-max draws (the pages' sampler, Summary §3.3)
+# ---------------------------------------------------------------------------
+
+def pin_gumbel_uniform_layout(orc):
+    """The uniform of id v is the top 23 bits (plus one half) of word v % 4 of
+    the block at counter (offset, i, k, 16 + tag + 256 (v // 4)), key
+    (seed, 0), scaled by 2^-23 (numpy's Philox as the reference)."""
+    rng = np.random.default_rng(31)
+    for _ in range(12):
+        seed, offset = (int(x) for x in rng.integers(0, 2**40, size=2))
+        offset += 1
+        i, k, tag = int(rng.integers(0, 4096)), int(rng.integers(1, 33)), int(rng.integers(1, 4))
+        for v in (0, 1, 2, 3, 4, 7, 8, 151935, int(rng.integers(0, 151936))):
+            words = np.random.Philox(counter=np.array([offset - 1, i, k, 16 + tag + 256 * (v // 4)], np.uint64),
+                                     key=np.array([seed, 0], np.uint64)).random_raw(4)
+            expect = (float(int(words[v % 4]) >> 41) + 0.5) / 2.0**23
+            assert orc.gumbel_uniform(seed, offset, i, k, tag, v) == expect, (v, tag)
+    us = np.array([orc.gumbel_uniform(5, 3, 2, 1, TAG_CORRECT, v) for v in range(65536)])
+    assert us.min() > 0.0 and us.max() < 1.0
+    assert _chi2_ok(np.bincount((us * 64).astype(int), minlength=64), np.full(64, 1 / 64))
+
+
+def pin_gumbel_law(orc):
+    """Gumbel-max property: the draw over weights w follows w / sum(w)
+    (chi-square over 20,000 draws); ids of weight 0 never come out; one
+    positive weight always wins; scaling w by a power of two changes no
+    draw whose score gap is not a rounding tie."""
+    w = np.array([0.1, 0.0, 0.5, 0.25, 0.15, 0.0])
+    draws = [orc.gumbel_draw(w, 7, off, 3, 2, TAG_BONUS) for off in range(20000)]
+    toks = np.array([d[0] for d in draws])
+    assert _chi2_ok(np.bincount(toks, minlength=w.size), w / w.sum())
+    one = np.zeros(9)
+    one[6] = 0.3
+    assert all(orc.gumbel_draw(one, 1, off, 0, 1, TAG_CORRECT)[0] == 6 for off in range(50))
+    assert orc.gumbel_draw(np.zeros(4), 1, 0, 0, 1, TAG_CORRECT)[0] == -1
+    for off in range(200):
+        t1, gap = orc.gumbel_draw(w, 7, off, 3, 2, TAG_BONUS)
+        if gap > 1e-9:
+            assert orc.gumbel_draw(w * 8.0, 7, off, 3, 2, TAG_BONUS)[0] == t1
+
+
+def pin_gumbel_verify_law(orc):
+    """Verify with Gumbel-max correction and bonus draws has the exact law of
+    (accept length, emitted token), as with inverse-CDF draws, and the first
+    emitted token follows p_1 when the proposals come from q; Gumbel
+    proposals follow softmax(qnew / T)."""
+    V, L, T = 3, 2, 1.0
+    pp = [np.array([0.5, 0.3, 0.2]), np.array([0.2, 0.2, 0.6]), np.array([0.1, 0.6, 0.3])]
+    qq = [np.array([0.2, 0.5, 0.3]), np.array([0.5, 0.1, 0.4])]
+    C = 12000
+    P = np.tile(np.log(np.stack(pp)).astype(np.float32), (C, 1))
+    Q = np.tile(np.log(np.stack(qq)).astype(np.float32), (C, 1))
+    offs = (np.arange(C + 1) * L).astype(np.int32)
+    pr = [sp_softmax(r) for r in np.log(np.stack(pp)).astype(np.float32).astype(np.float64)]
+    qr = [sp_softmax(r) for r in np.log(np.stack(qq)).astype(np.float32).astype(np.float64)]
+    r1, r2 = min(1, pr[0][1] / qr[0][1]), min(1, pr[1][0] / qr[1][0])
+    out = orc.verify_gumbel(P, Q, V, np.tile(np.array([1, 0], np.int32), C), offs, np.full(C, T, np.float32),
+                            77, 1)
+    a = out["accept_len"]
+    last = out["out_tokens"].reshape(C, L + 1)[np.arange(C), a]
+    w1 = np.maximum(pr[0] - qr[0], 0); w1 /= w1.sum()
+    w2 = np.maximum(pr[1] - qr[1], 0); w2 /= w2.sum()
+    probs = np.concatenate([(1 - r1) * w1, r1 * (1 - r2) * w2, r1 * r2 * pr[2]])
+    assert _chi2_ok(np.bincount(a * V + last, minlength=3 * V), probs)
+    rng = np.random.default_rng(18)
+    xs = np.stack([rng.choice(V, size=C, p=qr[0]), rng.choice(V, size=C, p=qr[1])], axis=1)
+    out = orc.verify_gumbel(P, Q, V, xs.reshape(-1).astype(np.int32), offs, np.full(C, T, np.float32), 99, 0)
+    assert _chi2_ok(np.bincount(out["out_tokens"].reshape(C, L + 1)[:, 0], minlength=V), pr[0])
+    # proposals: softmax(qnew / 0.5)
+    Qn = np.tile(np.log(qq[0]).astype(np.float32), (C, 1))
+    prop = orc.propose_gumbel(Qn, V, np.arange(C + 1, dtype=np.int32), np.full(C, 0.5, np.float32), 4, 2)
+    qn = sp_softmax(np.log(qq[0]).astype(np.float32).astype(np.float64) / 0.5)
+    assert _chi2_ok(np.bincount(prop["proposals"], minlength=V), qn)
+
+
+# ---------------------------------------------------------------------------
 # KV-slot bookkeeping of the stationary-batch loop (Summary §3.3)
 # ---------------------------------------------------------------------------
 
@@ -686,5 +762,5 @@ ALL_PINS = [
     pin_p_equals_q, pin_lossless_enumeration, pin_mc_verify_law, pin_mc_propose_law,
     pin_mc_step_independence, pin_alpha_mean, pin_bf16_decoding, pin_invalid_inputs, pin_relaxed_law,
     pin_filter_known, pin_filtered_verify_law, pin_kv_handworked, pin_kv_refusals_and_exact_fits,
-    pin_kv_cache_holds_token_stream,
+    pin_kv_cache_holds_token_stream, pin_gumbel_uniform_layout, pin_gumbel_law, pin_gumbel_verify_law,
 ]
