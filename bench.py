@@ -49,8 +49,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--separate", action="store_true",
                     help="time isd_verify then isd_propose (two launches) instead of isd_verify_propose")
-    ap.add_argument("--row", choices=["step", "kv"], default="step",
-                    help="kv: time the KV-slot commit of the stationary batch (isd_kv_commit) instead")
+    ap.add_argument("--row", choices=["step", "kv", "filtered"], default="step",
+                    help="kv: time the KV-slot commit of the stationary batch (isd_kv_commit); "
+                         "filtered: time the step under top-k 50 / top-p 0.95 (isd_verify_filtered + "
+                         "isd_propose_filtered)")
     return ap.parse_args()
 
 
@@ -582,12 +584,117 @@ def run_kv(args):
     print(json.dumps(line), flush=True)
 
 
+FILTER_TOP_K, FILTER_TOP_P = 50, 0.95
+
+
+def run_filtered(args):
+    """Positions per second of the step under the evaluation setting's
+    filters (top-k 50, top-p 0.95) on the bench workload: isd_verify_filtered
+    then isd_propose_filtered with its accept lengths, L2 flushed between
+    steps.  The roofline is the verify call's: every p and q row is streamed
+    once by its top-k kernel."""
+    import torch
+    from speculative_verify_accept_02_b300 import (_lib, build, isd_propose_filtered,
+                                                   isd_propose_filtered_workspace_bytes, isd_verify_filtered,
+                                                   isd_verify_filtered_workspace_bytes, workloads)
+    from speculative_verify_accept_02_b300.api import ProposeOut, VerifyOut, workspace
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    _lib.load()
+    batch = workloads.make(args.workload, device=dev)
+    C, total, V = batch.num_seqs, batch.total, batch.vocab
+    k, tp = FILTER_TOP_K, FILTER_TOP_P
+    i32, f32 = torch.int32, torch.float32
+    vout = VerifyOut(torch.empty(C, dtype=i32, device=dev), torch.empty(total + C, dtype=i32, device=dev),
+                     torch.empty(total, dtype=f32, device=dev), torch.empty(C, dtype=f32, device=dev))
+    pout = ProposeOut(torch.empty(total, dtype=i32, device=dev), torch.empty(C, dtype=torch.uint8, device=dev))
+    vws = workspace(isd_verify_filtered_workspace_bytes(C, total, k), dev)
+    pws = workspace(isd_propose_filtered_workspace_bytes(C, total, k), dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def verify(b):
+        isd_verify_filtered(b["p"], b["q"], b["tokens"], b["seq_offsets"], b["temperature"], batch.seed,
+                            batch.offset, top_k=k, top_p=tp, vocab=V, total=total, out=vout, ws=vws, stream=stream)
+
+    def propose(b):
+        isd_propose_filtered(b["qnew"], b["seq_offsets"], b["temperature"], batch.seed, batch.offset,
+                             vout.accept_len, top_k=k, top_p=tp, vocab=V, total=total, out=pout, ws=pws,
+                             stream=stream)
+
+    names = ("p", "q", "qnew", "tokens", "seq_offsets", "temperature")
+    resident = {n: getattr(batch, n) for n in names}
+    W, K = max(3, args.warmup), args.steps
+    for _ in range(W):
+        verify(resident)
+        propose(resident)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        for j in range(K):
+            flush.zero_()
+            ev[j][0].record(stream)
+            verify(resident)
+            ev[j][1].record(stream)
+            propose(resident)
+            ev[j][2].record(stream)
+        torch.cuda.synchronize(dev)
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+    verify_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    esz = 2 if batch.dtype == torch.bfloat16 else 4
+    verify_bytes = (2 * total + C) * V * esz  # every p and q row, read once
+    peak, peak_kind = load_peaks()
+    achieved = verify_bytes / (verify_ms / 1e3) / 1e9
+    # e2e: inputs from pinned host memory, every result read back
+    host_in = {n: resident[n].cpu().pin_memory() for n in names}
+    dev_in = {n: torch.empty_like(resident[n]) for n in names}
+    results = (vout.accept_len, vout.out_tokens, vout.ratio, vout.alpha, pout.proposals, pout.valid)
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in results]
+    E = max(1, args.e2e_steps)
+    e2e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E)]
+    for j in range(E):
+        e2e[j][0].record(stream)
+        for n in names:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        verify(dev_in)
+        propose(dev_in)
+        for hbuf, dbuf in zip(host_out, results):
+            hbuf.copy_(dbuf, non_blocking=True)
+        e2e[j][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e) / E
+    line = {
+        "metric": f"verified stride-positions/sec under top-k {k} / top-p {tp}", "value": total / (step_ms / 1e3),
+        "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(batch, {"top_k": k, "top_p": tp, "kept_ids_arithmetic": "f64",
+                                          "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write between timed steps",
+                                          "step": "isd_verify_filtered + isd_propose_filtered (four launches)"}),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "isd_verify_filtered (top-k selection + decisions)",
+                     "algorithmic_bytes": verify_bytes, "peak_source": f"{peak_kind} hbm_gbs",
+                     "avg_launch_us": verify_ms * 1e3},
+        "e2e": {"value": total / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host_in.values()),
+                "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in host_out)},
+        "gpu_launches": 4 * K,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.row == "kv":
         run_kv(args)
+    elif args.row == "filtered":
+        run_filtered(args)
     else:
         run_ours(args)
 
