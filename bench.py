@@ -587,6 +587,13 @@ def run_kv(args):
 FILTER_TOP_K, FILTER_TOP_P = 50, 0.95
 
 
+def filtered_verify_bytes(batch):
+    """Logit bytes isd_verify_filtered must read: every p row (sum L + C)
+    and every q row (sum L), once each."""
+    esz = 2 if str(batch.dtype).endswith("bfloat16") else 4
+    return (2 * batch.total + batch.num_seqs) * batch.vocab * esz
+
+
 def run_filtered(args):
     """Positions per second of the step under the evaluation setting's
     filters (top-k 50, top-p 0.95) on the bench workload: isd_verify_filtered
@@ -645,8 +652,7 @@ def run_filtered(args):
         torch.cuda.synchronize(dev)
     step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
     verify_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
-    esz = 2 if batch.dtype == torch.bfloat16 else 4
-    verify_bytes = (2 * total + C) * V * esz  # every p and q row, read once
+    verify_bytes = filtered_verify_bytes(batch)
     peak, peak_kind = load_peaks()
     achieved = verify_bytes / (verify_ms / 1e3) / 1e9
     # e2e: inputs from pinned host memory, every result read back

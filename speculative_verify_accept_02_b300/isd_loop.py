@@ -272,9 +272,11 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=64)
     ap.add_argument("--vocab", type=int, default=151936)
     ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--kv", action="store_true", help="keep the batch's KV-slot state with isd_kv_commit")
     args = ap.parse_args()
     model = TableModel(args.vocab, args.alpha, device="cuda")
-    loop = ISDLoop(model, args.num_seqs, args.stride, CudaBackend())
+    kv_len = 1 + (args.steps + 3) * args.stride + 2 * args.stride if args.kv else 0
+    loop = ISDLoop(model, args.num_seqs, args.stride, CudaBackend(), kv_len=kv_len)
     loop.run(3)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -286,7 +288,7 @@ def main():
     print(json.dumps({"stride": args.stride, "alpha": args.alpha, "num_seqs": args.num_seqs,
                       "steps": st.steps, "tpf": st.tpf, "tpf_closed_form": tpf_isd(args.stride, args.alpha),
                       "tpf_stderr": float(per.std(ddof=1) / np.sqrt(len(per))),
-                      "acceptance": st.acceptance,
+                      "acceptance": st.acceptance, "kv_commit": bool(args.kv),
                       "host_loop_ms_per_step": 1e3 * dt / args.steps}))
 
 

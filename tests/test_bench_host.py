@@ -54,3 +54,19 @@ def test_profiled_sources_are_the_verify_kernels():
     assert {csrc + "isd_verify.cu", csrc + "isd_api.cu", csrc + "isd_device.cuh", csrc + "isd_internal.h",
             "include/isd.h"} <= names
     assert csrc + "isd_kv.cu" not in names and csrc + "isd_propose.cu" not in names
+
+
+def test_filtered_bytes_count_every_row_once():
+    """The filtered verify streams all sum L + C anchor rows and sum L
+    proposal rows once: c64 reads 1088 rows of 303,872 bytes."""
+    b = workloads.make("c64", num_seqs=2, vocab=151936)
+    assert bench.filtered_verify_bytes(b) == (2 * 16 + 2) * 303872
+    f = workloads.make("tiny", num_seqs=3, vocab=100)
+    assert bench.filtered_verify_bytes(f) == (2 * f.total + 3) * 100 * 4
+
+
+def test_bench_rows_parse(monkeypatch):
+    for row in ("step", "kv", "filtered"):
+        monkeypatch.setattr("sys.argv", ["bench.py", "--row", row, "--steps", "5"])
+        a = bench.parse()
+        assert a.row == row and a.steps == 5
