@@ -562,7 +562,7 @@ static int kv_plan(const int32_t* table_row, int64_t ld, int len, int L, int w, 
                    int pool_size, int* kept, int* next_pend, int* status) {
     *status = 0;
     if (len < 0 || L < 0 || w < 0 || (int64_t)len + w > ld || (w == 0 && L != 0) ||
-        (w > 0 && w != 1 + L + M)) {
+        (w > 0 && (int64_t)w != 1 + (int64_t)L + M)) {
         *status = KV_ERR_STATE;
         return 0;
     }
