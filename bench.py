@@ -236,29 +236,36 @@ def _host_inputs(batch):
                 offs=batch.seq_offsets.cpu().numpy(), temp=batch.temperature.cpu().numpy())
 
 
-def _oracle_step(h, batch, seqs):
+def _oracle_step(h, batch, seqs, nthreads=0):
     import oracle
     v = oracle.verify(h["p"], h["q"], batch.vocab, h["tokens"], h["offs"], h["temp"], batch.seed,
-                      batch.offset, seqs=seqs)
+                      batch.offset, seqs=seqs, nthreads=nthreads)
     oracle.propose(h["qnew"], batch.vocab, h["offs"], h["temp"], batch.seed, batch.offset,
-                   accept_len=v["accept_len"], seqs=seqs)
+                   accept_len=v["accept_len"], seqs=seqs, nthreads=nthreads)
 
 
-def time_oracle(batch, seconds):
-    """oracle verify+propose on the whole batch, repeated for about `seconds`."""
+def time_oracle(batch, seconds, nthreads=0, seqs=None):
+    """oracle verify+propose on the batch (or the sequences `seqs`), repeated
+    for about `seconds`, on `nthreads` threads (0: all the host's)."""
     import oracle
     h = _host_inputs(batch)
-    seqs = list(range(batch.num_seqs))
-    positions = sum(batch.strides())
+    seqs = list(range(batch.num_seqs)) if seqs is None else list(seqs)
+    Ls = batch.strides()
+    positions = sum(Ls[i] for i in seqs)
+    before = oracle.threads()
     reps = 0
     t0 = time.perf_counter()
     while True:
-        _oracle_step(h, batch, seqs)
+        _oracle_step(h, batch, seqs, nthreads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return positions * reps / el, oracle.threads(), reps, el, positions
+    used = oracle.threads(nthreads)
+    if nthreads:  # the thread count sticks: put the earlier one back (an empty call sets it)
+        oracle.verify(np.zeros((1, 1), np.float32), np.zeros((1, 1), np.float32), 1, np.zeros(0, np.int32),
+                      np.zeros(1, np.int32), np.zeros(0, np.float32), 0, 0, nthreads=before)
+    return positions * reps / el, used, reps, el, positions
 
 
 def _sample_batch(batch, seqs, kp):
@@ -478,6 +485,12 @@ def run_ours(args):
         rate, threads, reps, el, pos = time_oracle(batch, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"full batch ({pos} positions) verify+propose, {reps} repetition(s) in {el:.1f} s"}
+        # the same oracle on one core, on the batch's first sequences (a bounded sample)
+        one = list(range(min(batch.num_seqs, max(1, threads))))
+        rate1, _, reps1, el1, pos1 = time_oracle(batch, args.cpu_seconds, nthreads=1, seqs=one)
+        cpu["single_core"] = {"value": rate1, "unit": UNIT, "cores": 1,
+                              "sample": f"{len(one)} sequences ({pos1} positions) verify+propose, "
+                                        f"{reps1} repetition(s) in {el1:.1f} s"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -3,6 +3,7 @@ roofline's numerator) and the code-only hash that keys profiled traffic."""
 import os
 import sys
 
+import pytest
 import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -70,3 +71,15 @@ def test_bench_rows_parse(monkeypatch):
         monkeypatch.setattr("sys.argv", ["bench.py", "--row", row, "--steps", "5"])
         a = bench.parse()
         assert a.row == row and a.steps == 5
+
+
+def test_time_oracle_all_cores_and_one():
+    """The CPU baseline's timer on a small batch: the rate counts the sampled
+    positions, and a single-core run reports one thread."""
+    import oracle
+    b = workloads.make("tiny", num_seqs=3, vocab=64)
+    rate, threads, reps, el, pos = bench.time_oracle(b, 0.05)
+    assert pos == sum(b.strides()) and reps >= 1 and rate == pytest.approx(pos * reps / el)
+    rate1, threads1, reps1, el1, pos1 = bench.time_oracle(b, 0.05, nthreads=1, seqs=[0])
+    assert threads1 == 1 and pos1 == b.strides()[0]
+    assert oracle.threads() == threads  # the single-core run put the thread count back
