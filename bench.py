@@ -442,7 +442,8 @@ def run_ours(args):
         t_wall = time.perf_counter() - t_wall
     if distributed:
         dist.barrier()
-    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
+    per_step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    step_ms = sum(per_step_ms)
     verify_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     total_ms = slowest_rank(step_ms, dev, distributed)
     ms_per_step = total_ms / K
@@ -507,6 +508,7 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} hbm_gbs", "avg_launch_us": verify_avg_s * 1e6},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "step_us": {"median": 1e3 * statistics.median(per_step_ms), "best": 1e3 * min(per_step_ms)},
         "gpu_launches": (1 if fused else 2) * K,  # verify_kernel (+ propose_kernel) per step
         "clocks": sampler.summary(),
         "wall_s_timed": t_wall,
