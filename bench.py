@@ -85,6 +85,16 @@ def algorithmic_bytes(batch, accept_len, valid):
     return verify, propose
 
 
+def reread_bytes(batch, accept_len):
+    """Bytes of the rejected row pairs the correction reads a second time
+    (p_j and q_j of every T > 0 sequence that rejects), reported beside the
+    algorithmic bytes, not in them: they should come from L2."""
+    esz = 2 if str(batch.dtype).endswith("bfloat16") else 4
+    temps = batch.temperature.cpu().tolist()
+    rejecting = sum(1 for i, L in enumerate(batch.strides()) if temps[i] > 0 and 0 <= int(accept_len[i]) < L)
+    return 2 * rejecting * batch.vocab * esz
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -415,7 +425,9 @@ def run_ours(args):
     for _ in range(max(3, args.warmup)):
         step(resident)
     torch.cuda.synchronize(dev)
-    vbytes, pbytes = algorithmic_bytes(batch, vout.accept_len.cpu().tolist(), pout.valid.cpu().tolist())
+    acc_host = vout.accept_len.cpu().tolist()
+    vbytes, pbytes = algorithmic_bytes(batch, acc_host, pout.valid.cpu().tolist())
+    rbytes = reread_bytes(batch, acc_host)
 
     # Timed region: K steps, each bracketed by its own events; the L2 flush
     # between steps lies outside them.
@@ -504,7 +516,7 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
                      "kernel": ("verify_kernel (isd_verify_propose: one persistent launch)" if fused
                                 else "verify_kernel (isd_verify: one persistent launch)"),
-                     "algorithmic_bytes": kernel_bytes,
+                     "algorithmic_bytes": kernel_bytes, "reread_bytes": rbytes,
                      "peak_source": f"{peak_kind} hbm_gbs", "avg_launch_us": verify_avg_s * 1e6},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -83,3 +83,13 @@ def test_time_oracle_all_cores_and_one():
     rate1, threads1, reps1, el1, pos1 = bench.time_oracle(b, 0.05, nthreads=1, seqs=[0])
     assert threads1 == 1 and pos1 == b.strides()[0]
     assert oracle.threads() == threads  # the single-core run put the thread count back
+
+
+def test_reread_bytes_count_rejecting_sampled_sequences():
+    """Two rows (p_j, q_j) per T > 0 sequence that rejects; greedy, invalid
+    and all-accepting sequences re-read nothing."""
+    b = workloads.make("ragged", num_seqs=6, vocab=1000)
+    Ls, temps = b.strides(), b.temperature.tolist()
+    acc = [0, Ls[1], 0, -1, 0, 0]
+    want = sum(2 * 2000 for i in range(6) if temps[i] > 0 and 0 <= acc[i] < Ls[i])
+    assert bench.reread_bytes(b, acc) == want
