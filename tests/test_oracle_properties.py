@@ -76,3 +76,38 @@ def test_filter_properties(V, k, top_p, T, seed):
     if k == 0 or k >= V:
         full = oracle.filtered_probs(z, T, k, 1.0)
         assert np.allclose(full, sp_softmax(z / T), atol=1e-14)
+
+
+@SETTINGS
+@given(C=st.integers(1, 6), V=st.integers(2, 40), Lmax=st.integers(1, 6), T=st.sampled_from([0.0, 0.5, 1.0, 2.0]),
+       seed=st.integers(0, 2**16), same=st.booleans())
+def test_verify_structure(C, V, Lmax, T, seed, same):
+    """Per sequence: 0 <= a <= L; the emitted slots are x_1..x_a, one token,
+    then -1; ratios in [0, 1] with alpha their mean; q == p accepts every
+    proposal; at T = 0 a is the count of leading argmax proposals and the
+    token is the argmax of p_{a+1}."""
+    rng = np.random.default_rng(seed)
+    Ls = rng.integers(1, Lmax + 1, C)
+    offs = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int32)
+    total = int(offs[-1])
+    P = rng.normal(0, 2, (total + C, V)).astype(np.float32)
+    Q = np.empty((total, V), np.float32)
+    for i in range(C):
+        for k in range(Ls[i]):
+            Q[offs[i] + k] = P[offs[i] + i + k] if same else rng.normal(0, 2, V)
+    toks = rng.integers(0, V, total).astype(np.int32)
+    out = oracle.verify(P, Q, V, toks, offs, np.full(C, T, np.float32), seed, 3)
+    for i in range(C):
+        s, L = int(offs[i]), int(Ls[i])
+        a = int(out["accept_len"][i])
+        r = out["ratio"][s:s + L]
+        slots = out["out_tokens"][s + i:s + i + L + 1]
+        assert 0 <= a <= L
+        assert np.array_equal(slots[:a], toks[s:s + a]) and 0 <= slots[a] < V and np.all(slots[a + 1:] == -1)
+        assert np.all((r >= 0) & (r <= 1)) and abs(out["alpha"][i] - r.mean()) < 1e-12
+        if same and T > 0:
+            assert a == L
+        if T == 0.0:
+            hits = [toks[s + k] == int(np.argmax(P[s + i + k])) for k in range(L)]
+            want_a = hits.index(False) if False in hits else L
+            assert a == want_a and slots[a] == int(np.argmax(P[s + i + a]))
