@@ -108,6 +108,43 @@ def test_filtered_parity(name, kw, top_k, top_p):
     assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 10)
 
 
+def _pattern_rows(kind, rows, V, g):
+    if kind == "ties":        # a ramp in bf16: long runs of equal logits, broken by id
+        base = torch.linspace(-8.0, 8.0, V)
+        return (base + 0.0 * torch.randn(rows, V, generator=g)).to(torch.bfloat16).float()
+    if kind == "ascending":   # every id beats the list: the worst case for the running lists
+        return torch.linspace(-4.0, 4.0, V).repeat(rows, 1) + 0.01 * torch.randn(rows, V, generator=g)
+    if kind == "equal":       # all logits equal: the lowest ids are kept
+        return torch.zeros(rows, V)
+    z = torch.randn(rows, V, generator=g)   # "masked": most logits -inf, a few finite
+    keep = torch.rand(rows, V, generator=g) < 0.01
+    keep[:, 0] = True
+    return torch.where(keep, z, torch.full_like(z, -float("inf")))
+
+
+@pytest.mark.parametrize("kind", ["ties", "ascending", "equal", "masked"])
+def test_filtered_adversarial_rows(kind):
+    """Rows that stress the top-k lists: runs of equal logits, ascending
+    logits (every id a candidate), all-equal rows, and rows that are mostly
+    -inf; bf16, rows not 16-byte aligned."""
+    g = torch.Generator().manual_seed(11)
+    C, L, V, ld = 3, 4, 4099, 4103
+    total = C * L
+    offs = torch.arange(C + 1, dtype=torch.int32) * L
+    P = _pattern_rows(kind, total + C, V, g)
+    Q = _pattern_rows(kind, total, V, g) + (0.0 if kind == "equal" else 0.5 * torch.randn(total, V, generator=g))
+    Q = torch.where(torch.isfinite(P[:total]) | (kind != "masked"), Q, torch.full_like(Q, -float("inf")))
+    Q[:, 0] = torch.where(torch.isfinite(Q[:, 0]), Q[:, 0], torch.zeros(total))
+    toks = torch.stack([torch.multinomial(torch.softmax(Q[r], 0), 1, generator=g)[0] for r in range(total)])
+    pad = lambda x: torch.nn.functional.pad(x, (0, ld - V)).to(torch.bfloat16)
+    batch = workloads.Batch(kind, V, ld, torch.bfloat16, offs, torch.ones(C), toks.to(torch.int32),
+                            pad(P), pad(Q), pad(_pattern_rows(kind, total, V, g)))
+    rep = Report()
+    skipped = compare_step(batch, 3, 1, 50, 0.95, rep)
+    rep.check()
+    assert skipped <= 1
+
+
 def test_filtered_invalid_sequences():
     """Strides outside [1, 32], bad temperatures and out-of-range tokens are
     flagged as isd_verify flags them: accept_len -1, slots -1, NaN ratios."""
