@@ -14,7 +14,9 @@ float32 the C ABI receives.  Cases:
 the evaluation setting on full-size rows, ragged strides with mixed
 temperatures and q == p, padded rows whose first ids are not 16-byte
 aligned (both dtypes), top-k above the vocabulary, top-1, a tight top-p,
-the largest stride, greedy batches, and invalid sequences.
+the largest stride, greedy batches, invalid sequences, and rows that
+stress the top-k lists (runs of equal logits, ascending logits, all-equal
+and mostly -inf rows).
 """
 import numpy as np
 import pytest
