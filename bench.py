@@ -85,6 +85,15 @@ def algorithmic_bytes(batch, accept_len, valid):
     return verify, propose
 
 
+def accepted_share(batch, accept_len):
+    """Accepted proposals over verified ones in this batch: the share of
+    positions on the common acceptance path (the pages report about 78 % on
+    their serving runs; here it is a property of the synthetic logits)."""
+    Ls = batch.strides()
+    total = sum(Ls)
+    return sum(max(0, int(a)) for a in accept_len) / total if total else 0.0
+
+
 def reread_bytes(batch, accept_len):
     """Bytes of the rejected row pairs the correction reads a second time
     (p_j and q_j of every T > 0 sequence that rejects), reported beside the
@@ -510,7 +519,8 @@ def run_ours(args):
         "dtype": "f32", "data": "synthetic",
         "config": workload_config(batch, {
             "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write between timed steps",
-            "parallelism": f"replicas x{world}", "step": "isd_verify_propose (one launch)" if fused else "isd_verify + isd_propose"}),
+            "parallelism": f"replicas x{world}", "step": "isd_verify_propose (one launch)" if fused else "isd_verify + isd_propose",
+            "accepted_share": accepted_share(batch, acc_host)}),
         "logit_gbs": logit_gbs, "hbm_frac": logit_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),

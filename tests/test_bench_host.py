@@ -93,3 +93,9 @@ def test_reread_bytes_count_rejecting_sampled_sequences():
     acc = [0, Ls[1], 0, -1, 0, 0]
     want = sum(2 * 2000 for i in range(6) if temps[i] > 0 and 0 <= acc[i] < Ls[i])
     assert bench.reread_bytes(b, acc) == want
+
+
+def test_accepted_share():
+    b = workloads.make("ragged", num_seqs=4, vocab=1000)
+    Ls = b.strides()
+    assert bench.accepted_share(b, [Ls[0], 0, -1, 1]) == (Ls[0] + 1) / sum(Ls)
