@@ -112,21 +112,27 @@ class CudaBackend:
         from .workloads import KVState
         return KVState.from_torch(handle)
 
-    def verify(self, p, q, tokens, offs, temp, seed, offset):
-        from .api import isd_verify
+    def verify(self, p, q, tokens, offs, temp, seed, offset, filters=None):
+        from .api import isd_verify, isd_verify_filtered
         d = self.device
-        out = isd_verify(p.to(d), q.to(d), torch.as_tensor(tokens, dtype=torch.int32, device=d),
-                         torch.as_tensor(offs, dtype=torch.int32, device=d),
-                         torch.as_tensor(temp, dtype=torch.float32, device=d), seed, offset,
-                         total=int(offs[-1]))
+        args = (p.to(d), q.to(d), torch.as_tensor(tokens, dtype=torch.int32, device=d),
+                torch.as_tensor(offs, dtype=torch.int32, device=d),
+                torch.as_tensor(temp, dtype=torch.float32, device=d), seed, offset)
+        if filters is None:
+            out = isd_verify(*args, total=int(offs[-1]))
+        else:
+            out = isd_verify_filtered(*args, top_k=filters[0], top_p=filters[1], total=int(offs[-1]))
         return out.accept_len.cpu().numpy(), out.out_tokens.cpu().numpy()
 
-    def propose(self, qnew, offs, temp, seed, offset):
-        from .api import isd_propose
+    def propose(self, qnew, offs, temp, seed, offset, filters=None):
+        from .api import isd_propose, isd_propose_filtered
         d = self.device
-        out = isd_propose(qnew.to(d), torch.as_tensor(offs, dtype=torch.int32, device=d),
-                          torch.as_tensor(temp, dtype=torch.float32, device=d), seed, offset,
-                          total=int(offs[-1]))
+        args = (qnew.to(d), torch.as_tensor(offs, dtype=torch.int32, device=d),
+                torch.as_tensor(temp, dtype=torch.float32, device=d), seed, offset)
+        if filters is None:
+            out = isd_propose(*args, total=int(offs[-1]))
+        else:
+            out = isd_propose_filtered(*args, top_k=filters[0], top_p=filters[1], total=int(offs[-1]))
         return out.proposals.cpu().numpy(), out.valid.cpu().numpy()
 
 
@@ -155,13 +161,15 @@ class LoopStats:
 class ISDLoop:
     """C sequences decoded with stride n (n-1 proposals per step) by ISD.
 
-    backend: an object with verify(p, q, tokens, offs, temp, seed, offset) ->
-    (accept_len, out_tokens) and propose(qnew, offs, temp, seed, offset) ->
-    (proposals, valid), over the library's layout (include/isd.h).
+    backend: an object with verify(p, q, tokens, offs, temp, seed, offset,
+    filters) -> (accept_len, out_tokens) and propose(qnew, offs, temp, seed,
+    offset, filters) -> (proposals, valid), over the library's layout
+    (include/isd.h).  filters: (top_k, top_p) to decode under the evaluation
+    setting's sampling filters (include/isd_filter.h), or None.
     """
 
     def __init__(self, model: TableModel, num_seqs: int, stride: int, backend, seed: int = 0,
-                 kv_len: int = 0):
+                 kv_len: int = 0, filters=None):
         if not 2 <= stride <= 32:
             raise ValueError("stride n must lie in [2, 32] (n - 1 proposals, one anchor row more)")
         self.model, self.C, self.n, self.backend, self.seed = model, num_seqs, stride, backend, seed
@@ -170,6 +178,7 @@ class ISDLoop:
         self.tokens: List[List[int]] = [[] for _ in range(num_seqs)]
         self.stats = LoopStats(per_seq_tokens=[0] * num_seqs)
         self.offset = 0
+        self.filters = filters  # (top_k, top_p) of the evaluation setting, or None
         self.kv = None
         if kv_len:
             # every row holds the cache of kv_len positions; the pool backs all rows
@@ -202,7 +211,7 @@ class ISDLoop:
         rows = torch.where(torch.as_tensor(is_anchor, device=A.device)[:, None], A, Qr)
         offs = np.asarray(offs, dtype=np.int32)
         temp = np.ones(len(jobs), np.float32)
-        props, valid = self.backend.propose(rows, offs, temp, self.seed, self.offset)
+        props, valid = self.backend.propose(rows, offs, temp, self.seed, self.offset, filters=self.filters)
         assert np.all(valid == 1)
         return [props[offs[j]:offs[j + 1]] for j in range(len(jobs))]
 
@@ -222,7 +231,7 @@ class ISDLoop:
             toks = np.concatenate([self.pending[i] for i in ver]).astype(np.int32)
             offs = np.arange(len(ver) + 1, dtype=np.int32) * L
             temp = np.ones(len(ver), np.float32)
-            acc, out = self.backend.verify(p, q, toks, offs, temp, self.seed, self.offset)
+            acc, out = self.backend.verify(p, q, toks, offs, temp, self.seed, self.offset, filters=self.filters)
             assert np.all(acc >= 0), acc
             for j, i in enumerate(ver):
                 a = int(acc[j])

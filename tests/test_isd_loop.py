@@ -17,15 +17,22 @@ from speculative_verify_accept_02_b300.isd_loop import CudaBackend, ISDLoop, Tab
 
 
 class OracleBackend:
-    def verify(self, p, q, tokens, offs, temp, seed, offset):
+    def verify(self, p, q, tokens, offs, temp, seed, offset, filters=None):
         V = p.shape[1]
-        ov = oracle.verify(workloads.host_logits(p), workloads.host_logits(q), V, tokens, offs, temp, seed,
-                           offset)
+        hp, hq = workloads.host_logits(p), workloads.host_logits(q)
+        if filters is None:
+            ov = oracle.verify(hp, hq, V, tokens, offs, temp, seed, offset)
+        else:
+            ov = oracle.verify_filtered(hp, hq, V, tokens, offs, temp, seed, offset, filters[0], filters[1])
         return ov["accept_len"], ov["out_tokens"]
 
-    def propose(self, qnew, offs, temp, seed, offset):
+    def propose(self, qnew, offs, temp, seed, offset, filters=None):
         V = qnew.shape[1]
-        op = oracle.propose(workloads.host_logits(qnew), V, offs, temp, seed, offset)
+        hq = workloads.host_logits(qnew)
+        if filters is None:
+            op = oracle.propose(hq, V, offs, temp, seed, offset)
+        else:
+            op = oracle.propose_filtered(hq, V, offs, temp, seed, offset, filters[0], filters[1])
         return op["proposals"], op["valid"]
 
     def kv_state(self, state):
@@ -143,3 +150,20 @@ def test_loop_kv_on_oracle():
 def test_loop_kv_on_cuda():
     assert torch.cuda.is_available(), "GPU test needs a CUDA device"
     _kv_loop(CudaBackend(), 4096, "cuda")
+
+
+def test_loop_under_filters_on_oracle():
+    """The evaluation setting's filters change what the table model accepts,
+    exactly: q is uniform on a support S and p puts alpha/s on S, (1-alpha)/s
+    on a disjoint S'.  Top-10 of 32 keeps the 10 lowest ids of the larger
+    block: for alpha > 1/2 both filtered p and q are uniform on the same 10
+    ids of S, so every proposal passes (TPF = n after the first step); for
+    alpha < 1/2 filtered p lives on S' and nothing passes (TPF = 1)."""
+    n, C, S = 4, 3, 7
+    for alpha, all_pass in ((0.6, True), (0.4, False)):
+        model = TableModel(256, alpha, entries=5, support=32, seed=8)
+        st = ISDLoop(model, C, n, OracleBackend(), filters=(10, 1.0)).run(S)
+        if all_pass:
+            assert st.per_seq_tokens == [1 + n * (S - 1)] * C and st.accepted == st.verified
+        else:
+            assert st.per_seq_tokens == [S] * C and st.accepted == 0
