@@ -263,6 +263,17 @@ def _oracle_step(h, batch, seqs, nthreads=0):
                    accept_len=v["accept_len"], seqs=seqs, nthreads=nthreads)
 
 
+def _oracle_filtered_step(h, batch, seqs, nthreads=0):
+    """The oracle's filtered step (top-k 50, top-p 0.95) on the whole sub-batch
+    (its filtered functions take every sequence)."""
+    import oracle
+    tp = float(np.float32(FILTER_TOP_P))
+    v = oracle.verify_filtered(h["p"], h["q"], batch.vocab, h["tokens"], h["offs"], h["temp"], batch.seed,
+                               batch.offset, FILTER_TOP_K, tp)
+    oracle.propose_filtered(h["qnew"], batch.vocab, h["offs"], h["temp"], batch.seed, batch.offset,
+                            FILTER_TOP_K, tp, accept_len=v["accept_len"])
+
+
 def time_oracle(batch, seconds, nthreads=0, seqs=None):
     """oracle verify+propose on the batch (or the sequences `seqs`), repeated
     for about `seconds`, on `nthreads` threads (0: all the host's)."""
@@ -307,11 +318,44 @@ def _sample_batch(batch, seqs, kp):
     return sub, sum(Ls)
 
 
+def run_reference_kv(args):
+    """The oracle's KV commit on the --row kv workload (C=64 sequences,
+    stride 8, accept lengths uniform on 0..7), timed per commit on the host."""
+    import oracle
+    from speculative_verify_accept_02_b300 import workloads
+    C, M = KV_NUM_SEQS, KV_MASKS
+    W, K = max(3, args.warmup), args.steps
+    n = W + K
+    ld = n * (M + 1) + 2 * M + 2
+    state = workloads.make_kv_state(C, ld, C * ld, 0, seed=7)
+    accept = np.random.default_rng(7).integers(0, M + 1, (n, C)).astype(np.int32)
+    for j in range(W):
+        oracle.kv_commit(state, accept[j], M)
+    t0 = time.perf_counter()
+    refused = sum(1 for j in range(W, n) if oracle.kv_commit(state, accept[j], M) != 0)
+    us = 1e6 * (time.perf_counter() - t0) / K
+    desc = f"every commit of the stationary batch ({C} sequences, {M} masks), one thread"
+    line = {"impl": "reference", "metric": f"KV-slot commits/sec (isd_kv_commit), C={C} stride {M + 1}",
+            "value": 1e6 / us, "unit": "commits/s", "n_gpus": args.gpus, "steps": K, "warmup": W,
+            "ms_per_step": us / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int32", "data": "synthetic",
+            "config": {"workload": f"stationary batch of {C} sequences, {M} masks, accept lengths uniform on 0..{M}",
+                       "refused_commits": refused, "sample": desc},
+            "cpu_baseline": {"value": 1e6 / us, "unit": "commits/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": 1e6 / us, "unit": "commits/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return  # the oracle runs once, on rank 0
+    if args.row == "kv":
+        run_reference_kv(args)
+        return
     import oracle
     from speculative_verify_accept_02_b300 import workloads
+    filtered = args.row == "filtered"
+    stepper = _oracle_filtered_step if filtered else _oracle_step
     batch = workloads.make(args.workload, device="cpu")
     # The sample per step is sized so that the whole run (warm-up and timed
     # steps) takes about REFERENCE_BUDGET_S: up to 8 whole sequences, or one
@@ -319,7 +363,7 @@ def run_reference(args):
     one, _ = _sample_batch(batch, [0], 1 << 30)
     h1 = _host_inputs(one)
     t0 = time.perf_counter()
-    _oracle_step(h1, one, [0])
+    stepper(h1, one, [0])
     t_seq = time.perf_counter() - t0
     t_step = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
     L0 = batch.strides()[0]
@@ -334,22 +378,25 @@ def run_reference(args):
     h = _host_inputs(sub)
     idx = list(range(len(seqs)))
     for _ in range(args.warmup):
-        _oracle_step(h, sub, idx)
+        stepper(h, sub, idx)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_step(h, sub, idx)
+        stepper(h, sub, idx)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
     value = positions / (ms / 1e3)
     desc = (f"{len(seqs)} of {batch.num_seqs} sequences" + (f", cut to {kp} positions" if kp < L0 else "")
-            + f" ({positions} positions) per step, verify+propose")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            + f" ({positions} positions) per step, "
+            + (f"verify+propose under top-k {FILTER_TOP_K} / top-p {FILTER_TOP_P}" if filtered else "verify+propose"))
+    metric = f"verified stride-positions/sec under top-k {FILTER_TOP_K} / top-p {FILTER_TOP_P}" if filtered else METRIC
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(batch, {"sample": desc}),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-                             "sample": desc},
+            # the filtered oracle runs row by row on one thread
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1 if filtered else oracle.threads(),
+                             "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
