@@ -1,5 +1,5 @@
 """Python binding of libisd: the entry points declared under include/
-(isd.h, isd_filter.h, isd_kv.h) over torch CUDA tensors.  Argument marshalling only — every step of the computation runs
+(isd.h, isd_filter.h, isd_kv.h, isd_debug.h) over torch CUDA tensors.  Argument marshalling only — every step of the computation runs
 in the library's kernels; torch supplies device memory and the stream.
 
 Tensors:
@@ -296,3 +296,20 @@ def isd_kv_commit(state: dict, accept_len: torch.Tensor, num_masks: int, *,
                                    _int32(status, "status"), _stream(device, stream))
     _lib.check("isd_kv_commit", rc)
     return status
+
+
+def isd_decision_uniforms(seed: int, offset: int, counters: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """isd_decision_uniforms (include/isd_debug.h): the decision uniform of
+    each (sequence, position, purpose) row of ``counters`` ([n, 3] int64 on
+    a CUDA device, non-negative) under (seed, offset).  Returns [n] float32."""
+    if counters.dtype != torch.int64 or counters.dim() != 2 or counters.shape[1] != 3 or \
+            not counters.is_contiguous() or not counters.is_cuda:
+        raise ValueError("counters must be a contiguous [n, 3] int64 CUDA tensor")
+    n = counters.shape[0]
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=counters.device)
+    status = _lib.load().isd_decision_uniforms(int(seed), int(offset), counters.data_ptr(), n,
+                                               _f32(out, "out"), _stream(counters.device, stream))
+    _lib.check("isd_decision_uniforms", status)
+    return out

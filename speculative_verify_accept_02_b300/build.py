@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libisd.so")
 SOURCES = ["isd_api.cu", "isd_verify.cu", "isd_propose.cu", "isd_alpha.cu", "isd_noalloc.cu", "isd_kv.cu",
-           "isd_filter.cu"]
+           "isd_filter.cu", "isd_debug.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

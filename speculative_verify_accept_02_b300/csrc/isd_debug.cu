@@ -1,0 +1,37 @@
+// Check entry points (include/isd_debug.h): the building blocks of the step,
+// exposed one at a time so that they can be compared bit for bit with an
+// independent implementation.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/isd_debug.h"
+#include "isd_device.cuh"
+
+namespace isd {
+namespace {
+
+constexpr int kThreads = 256;
+
+// One uniform per counter triple, with the same device function the
+// decision, selection and proposal code calls.
+__global__ void __launch_bounds__(kThreads) uniforms_kernel(uint64_t seed, uint64_t offset, const uint64_t* ctr,
+                                                          int n, float* out) {
+    for (long long j = blockIdx.x * static_cast<long long>(kThreads) + threadIdx.x; j < n;
+         j += static_cast<long long>(gridDim.x) * kThreads)
+        out[j] = decision_uniform(seed, offset, ctr[3 * j], ctr[3 * j + 1], ctr[3 * j + 2]);
+}
+
+}  // namespace
+}  // namespace isd
+
+extern "C" isd_status isd_decision_uniforms(uint64_t seed, uint64_t offset, const uint64_t* counters, int n,
+                                            float* out, void* stream) {
+    if (n < 0 || (n > 0 && (!counters || !out))) return ISD_ERR_INVALID_ARG;
+    if (n == 0) return ISD_OK;
+    const int blocks = (n + isd::kThreads - 1) / isd::kThreads;
+    const int grid = blocks < 1024 ? blocks : 1024;
+    isd::uniforms_kernel<<<grid, isd::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(seed, offset, counters, n,
+                                                                                        out);
+    return cudaGetLastError() == cudaSuccess ? ISD_OK : ISD_ERR_CUDA;
+}

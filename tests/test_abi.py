@@ -202,6 +202,13 @@ def test_kv_commit_host_checks(lib):
     assert _kv_commit(lib, C=-1, table=None, seq_len=None) == _lib.ISD_ERR_INVALID_ARG
 
 
+def test_decision_uniforms_host_checks(lib):
+    assert lib.isd_decision_uniforms(0, 0, None, 0, None, None) == _lib.ISD_OK   # nothing to do
+    assert lib.isd_decision_uniforms(0, 0, FAKE, -1, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
+    assert lib.isd_decision_uniforms(0, 0, None, 4, FAKE, None) == _lib.ISD_ERR_INVALID_ARG
+    assert lib.isd_decision_uniforms(0, 0, FAKE, 4, None, None) == _lib.ISD_ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     monkeypatch.setattr(_lib, "LIBRARY", str(tmp_path / "missing.so"))
