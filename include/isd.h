@@ -86,7 +86,7 @@ typedef enum {
     ISD_OK = 0,
     ISD_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld < vocab, bad dtype */
     ISD_ERR_UNSUPPORTED = 2,   /* logits base not 16-byte aligned; isd_verify: vocab above
-                                  523,264 (bf16) or 261,632 (fp32); isd_propose: vocab above
+                                  524,288 (bf16) or 262,144 (fp32); isd_propose: vocab above
                                   1,047,552 (bf16) or 523,776 (fp32) */
     ISD_ERR_WORKSPACE = 3,     /* workspace too small or not 256-byte aligned */
     ISD_ERR_CUDA = 4           /* a CUDA call failed (launch or device query) */
@@ -182,6 +182,32 @@ ISD_API isd_status isd_verify_propose(const void* p_logits, int64_t ld_p, const 
                                       int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
                                       const void* qnew_logits, int64_t ld_qnew, int32_t* proposals,
                                       uint8_t* valid, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * isd_verify_propose_gumbel — isd_verify_propose with Gumbel-max draws in
+ * place of inverse-CDF draws for the correction, the bonus token and the
+ * proposals: the sampler of the pages' fused verification kernel (§3.3,
+ * "online softmax and Gumbel-max correction").  A draw from weights w gives
+ * the id that maximises log w_v - log(-log u_v) over the ids with w_v > 0,
+ * the lower id on ties, with one uniform per vocabulary id and draw: u_v
+ * from Philox4x64-10 with key (seed, 0) and counter (offset, i, position,
+ * 16 + tag + 256 floor(v / 4)), output word v mod 4, taken as (top 23 bits
+ * + 1/2) 2^-23, strictly inside (0, 1).  The weights are those of the
+ * inverse-CDF draws: the residual max(0, p_j - q_j) (p_j where it is zero
+ * everywhere), p_{L+1}, softmax(Qnew_m / T).  Both samplers draw exactly from
+ * the same distributions (the Gumbel-max property), so every guarantee of
+ * isd_verify_propose holds; the tokens differ because the random numbers
+ * differ.  Ratios, accept lengths, alpha, greedy (T = 0) tokens and valid
+ * are those of isd_verify_propose.  Arguments and workspace as
+ * isd_verify_propose.
+ */
+ISD_API isd_status isd_verify_propose_gumbel(const void* p_logits, int64_t ld_p, const void* q_logits,
+                                             int64_t ld_q, isd_dtype dtype, int vocab, const int32_t* tokens,
+                                             const int32_t* seq_offsets, int num_seqs, int total_positions,
+                                             const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                                             int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                                             const void* qnew_logits, int64_t ld_qnew, int32_t* proposals,
+                                             uint8_t* valid, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace isd_propose needs for this batch shape. */
 ISD_API size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype);

@@ -126,9 +126,12 @@ def isd_verify_propose(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, q
                        seq_offsets: torch.Tensor, temperature: torch.Tensor, seed: int = 0, offset: int = 0, *,
                        vocab: Optional[int] = None, total: Optional[int] = None, tau: float = 0.0,
                        out: Optional[VerifyOut] = None, pout: Optional[ProposeOut] = None,
-                       ws: Optional[torch.Tensor] = None, stream=None):
+                       ws: Optional[torch.Tensor] = None, stream=None, sampler: str = "icdf"):
     """isd_verify_propose: verify and the next stride's proposals in one
-    launch.  Returns (VerifyOut, ProposeOut)."""
+    launch; sampler="gumbel" calls isd_verify_propose_gumbel (Gumbel-max
+    draws in place of inverse-CDF draws).  Returns (VerifyOut, ProposeOut)."""
+    if sampler not in ("icdf", "gumbel"):
+        raise ValueError(f"sampler must be 'icdf' or 'gumbel', not {sampler!r}")
     device = p.device
     C = seq_offsets.numel() - 1
     total = _total(seq_offsets, total)
@@ -149,13 +152,45 @@ def isd_verify_propose(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, q
     need = isd_verify_propose_workspace_bytes(C, total, V, p.dtype)
     if ws is None:
         ws = workspace(need, device)
-    status = _lib.load().isd_verify_propose(
+    name = "isd_verify_propose_gumbel" if sampler == "gumbel" else "isd_verify_propose"
+    status = getattr(_lib.load(), name)(
         pp, ldp, qp, ldq, _dtype_code(p), V, _int32(tokens, "tokens"), _int32(seq_offsets, "seq_offsets"),
         C, total, _f32(temperature, "temperature"), int(seed), int(offset), float(tau),
         out.accept_len.data_ptr(), out.out_tokens.data_ptr(), out.ratio.data_ptr(), out.alpha.data_ptr(),
         np_, ldn, pout.proposals.data_ptr(), pout.valid.data_ptr(),
         ws.data_ptr(), ws.numel() * ws.element_size(), _stream(device, stream))
-    _lib.check("isd_verify_propose", status)
+    _lib.check(name, status)
+    return out, pout
+
+
+def isd_debug_verify_stall(p: torch.Tensor, q: torch.Tensor, tokens: torch.Tensor, qnew: torch.Tensor,
+                           seq_offsets: torch.Tensor, temperature: torch.Tensor, seed: int, offset: int,
+                           stall_seq: int, wait_ns: int, *, total: int, ws: torch.Tensor,
+                           out: Optional[VerifyOut] = None, pout: Optional[ProposeOut] = None, stream=None):
+    """isd_debug_verify_stall (include/isd_debug.h): isd_verify_propose with
+    the decision of sequence ``stall_seq`` held back and the kernel's waits on
+    other CTAs bounded by ``wait_ns``.  Returns (VerifyOut, ProposeOut)."""
+    device = p.device
+    C = seq_offsets.numel() - 1
+    V = p.shape[1]
+    pp, ldp = _rows(p, "p")
+    qp, ldq = _rows(q, "q")
+    np_, ldn = _rows(qnew, "qnew")
+    if out is None:
+        out = VerifyOut(torch.empty(C, dtype=torch.int32, device=device),
+                        torch.empty(total + C, dtype=torch.int32, device=device),
+                        torch.empty(total, dtype=torch.float32, device=device),
+                        torch.empty(C, dtype=torch.float32, device=device))
+    if pout is None:
+        pout = ProposeOut(torch.empty(total, dtype=torch.int32, device=device),
+                          torch.empty(C, dtype=torch.uint8, device=device))
+    status = _lib.load().isd_debug_verify_stall(
+        pp, ldp, qp, ldq, _dtype_code(p), V, _int32(tokens, "tokens"), _int32(seq_offsets, "seq_offsets"),
+        C, int(total), _f32(temperature, "temperature"), int(seed), int(offset),
+        out.accept_len.data_ptr(), out.out_tokens.data_ptr(), out.ratio.data_ptr(), out.alpha.data_ptr(),
+        np_, ldn, pout.proposals.data_ptr(), pout.valid.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), int(stall_seq), int(wait_ns), _stream(device, stream))
+    _lib.check("isd_debug_verify_stall", status)
     return out, pout
 
 

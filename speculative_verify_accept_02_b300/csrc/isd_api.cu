@@ -23,37 +23,25 @@ bool dtype_ok(int dtype) { return dtype == ISD_DTYPE_BF16 || dtype == ISD_DTYPE_
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Workspace of isd_verify (persistent kernel):
-//   [control block | per-sequence counters | per-sequence tail state |
-//    tail-task queue and flags | per (row slot, segment) partials |
-//    per (tail sub-chunk, consumer warp) slice partials]
+//   [control block | per-sequence counters | per-tail piece counts |
+//    tail descriptors | tail piece results | piece block sums |
+//    per (row slot, chunk) partials]
 struct VerifyPlan {
-    int ck, nck, spseg, nseg, ckt, nt, tpt, ntask;
+    int ck, nck, ps, np;
 };
-
-constexpr int kSubChunksPerSegment = 8;  // one main item: 8 x 16 KB
-constexpr int kTailSubChunksPerTask = 2;
-constexpr double kL2KeepBytes = 40.0 * (1 << 20);  // of the 126 MB L2
 
 VerifyPlan verify_plan(int vocab, int esz) {
     VerifyPlan pl;
     const Chunking main = isd::make_chunking(vocab, esz);
     pl.ck = main.chunk;
     pl.nck = main.nchunks;
-    pl.spseg = kSubChunksPerSegment;
-    pl.nseg = (pl.nck + pl.spseg - 1) / pl.spseg;
-    // Tail sub-chunks hold one piece of p and one of q: half a stage each.
-    const int vec = 16 / esz;
-    const int tmax = ((isd::kStageBytes / 2 - 16) / esz) / vec * vec;
-    pl.nt = (vocab + tmax - 1) / tmax;
-    const int even = (vocab + pl.nt - 1) / pl.nt;
-    pl.ckt = (even + vec - 1) / vec * vec;
-    pl.tpt = kTailSubChunksPerTask;
-    pl.ntask = (pl.nt + pl.tpt - 1) / pl.tpt;
+    pl.ps = isd::kPieceBytes / esz;
+    pl.np = (vocab + pl.ps - 1) / pl.ps;
     return pl;
 }
 
 struct VerifyLayout {
-    size_t ctl, seq_count, seq_pending, tail_count, tails, tasks, task_ready, part, tpart, bytes;
+    size_t ctl, seq_count, seq_done, dready, tcount, tdesc, tpart, tbsum, part, bytes;
 };
 
 // Tails: one per sequence (its correction or bonus), plus one per qnew row
@@ -67,20 +55,20 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl, bool f
     off = align_up(off + sizeof(isd::VerifyCtl));
     l.seq_count = off;
     off = align_up(off + sizeof(int) * C);
-    l.seq_pending = off;
+    l.seq_done = off;
     off = align_up(off + sizeof(int) * C);
-    l.tail_count = off;
+    l.dready = off;
+    off = align_up(off + sizeof(uint64_t) * C);
+    l.tcount = off;
     off = align_up(off + sizeof(int) * NT);
-    l.tails = off;
-    off = align_up(off + sizeof(isd::SeqTail) * NT);
-    l.tasks = off;
-    off = align_up(off + 2 * sizeof(int4) * NT * pl.ntask);
-    l.task_ready = off;
-    off = align_up(off + sizeof(int) * NT * pl.ntask);
-    l.part = off;
-    off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * pl.nseg);
+    l.tdesc = off;
+    off = align_up(off + sizeof(uint64_t) * isd::kTailWords * NT);
     l.tpart = off;
-    off = align_up(off + sizeof(float2) * NT * pl.nt * 8);  // 8 consumer-warp slices per tail sub-chunk
+    off = align_up(off + sizeof(uint64_t) * 4 * NT * static_cast<size_t>(pl.np));  // four words per piece
+    l.tbsum = off;
+    off = align_up(off + sizeof(float) * 32 * NT * static_cast<size_t>(pl.np));  // a block sum per lane and piece
+    l.part = off;
+    off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * pl.nck);
     l.bytes = off;
     return l;
 }
@@ -119,13 +107,11 @@ isd_status resident_grid(long long n_items, int ctas_per_sm, int* grid) {
 extern "C" {
 
 size_t isd_verify_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
-    if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return 0;
-    return verify_layout(num_seqs, total_positions, verify_plan(vocab, elem_bytes_of(dtype)), false).bytes;
+    return isd::verify_workspace(num_seqs, total_positions, vocab, dtype, false);
 }
 
 size_t isd_verify_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
-    if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return 0;
-    return verify_layout(num_seqs, total_positions, verify_plan(vocab, elem_bytes_of(dtype)), true).bytes;
+    return isd::verify_workspace(num_seqs, total_positions, vocab, dtype, true);
 }
 
 size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype) {
@@ -135,33 +121,48 @@ size_t isd_propose_workspace_bytes(int num_seqs, int total_positions, int vocab,
 
 }  // extern "C"
 
-namespace {
+namespace isd {
 
-isd_status verify_impl(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
-                       isd_dtype dtype, int vocab, const int32_t* tokens,
-                       const int32_t* seq_offsets, int num_seqs, int total_positions,
-                       const float* temperature, uint64_t seed, uint64_t offset, float tau,
-                       int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
-                       bool fused, const void* qnew_logits, int64_t ld_qnew, int32_t* proposals,
-                       uint8_t* valid, void* workspace, size_t workspace_bytes, void* stream) {
+isd_status verify_check(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q, isd_dtype dtype,
+                        int vocab, const int32_t* tokens, const int32_t* seq_offsets, int num_seqs,
+                        int total_positions, const float* temperature, int32_t* accept_len, int32_t* out_tokens,
+                        float* ratio, float* alpha, const VerifyOptions& o) {
     if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return ISD_ERR_INVALID_ARG;
-    if (!(tau >= 0.0f) || !std::isfinite(tau)) return ISD_ERR_INVALID_ARG;
+    if (!(o.tau >= 0.0f) || !std::isfinite(o.tau)) return ISD_ERR_INVALID_ARG;
+    if (o.sampler != kSamplerIcdf && o.sampler != kSamplerGumbel) return ISD_ERR_INVALID_ARG;
     if (num_seqs == 0) return ISD_OK;
-    if (!p_logits || !q_logits || !tokens || !seq_offsets || !temperature || !accept_len ||
-        !out_tokens || !ratio || !alpha || !workspace)
+    if (!p_logits || !q_logits || !tokens || !seq_offsets || !temperature || !accept_len || !out_tokens ||
+        !ratio || !alpha)
         return ISD_ERR_INVALID_ARG;
     if (ld_p < vocab || ld_q < vocab) return ISD_ERR_INVALID_ARG;
-    if (fused && (!qnew_logits || !proposals || !valid || ld_qnew < vocab)) return ISD_ERR_INVALID_ARG;
-    if (!aligned16(p_logits) || !aligned16(q_logits) || (fused && !aligned16(qnew_logits)))
-        return ISD_ERR_UNSUPPORTED;
+    if (o.fused && (!o.qnew || !o.proposals || !o.valid || o.ld_qnew < vocab)) return ISD_ERR_INVALID_ARG;
+    if (!aligned16(p_logits) || !aligned16(q_logits) || (o.fused && !aligned16(o.qnew))) return ISD_ERR_UNSUPPORTED;
+    if (verify_plan(vocab, elem_bytes_of(dtype)).np > kMaxPieces) return ISD_ERR_UNSUPPORTED;
+    return ISD_OK;
+}
+
+size_t verify_workspace(int num_seqs, int total_positions, int vocab, isd_dtype dtype, bool fused) {
+    if (num_seqs < 0 || total_positions < 0 || vocab < 1 || !dtype_ok(dtype)) return 0;
+    return verify_layout(num_seqs, total_positions, verify_plan(vocab, elem_bytes_of(dtype)), fused).bytes;
+}
+
+isd_status verify_run(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q, isd_dtype dtype,
+                      int vocab, const int32_t* tokens, const int32_t* seq_offsets, int num_seqs,
+                      int total_positions, const float* temperature, uint64_t seed, uint64_t offset,
+                      int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha, const VerifyOptions& o,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    const isd_status chk = verify_check(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets,
+                                        num_seqs, total_positions, temperature, accept_len, out_tokens, ratio,
+                                        alpha, o);
+    if (chk != ISD_OK || num_seqs == 0) return chk;
+    if (!workspace) return ISD_ERR_INVALID_ARG;
     const int esz = elem_bytes_of(dtype);
     const VerifyPlan pl = verify_plan(vocab, esz);
-    if (pl.nt > isd::kMaxTailChunks) return ISD_ERR_UNSUPPORTED;
-    const VerifyLayout lay = verify_layout(num_seqs, total_positions, pl, fused);
+    const VerifyLayout lay = verify_layout(num_seqs, total_positions, pl, o.fused);
     if (workspace_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
         return ISD_ERR_WORKSPACE;
     char* ws = static_cast<char*>(workspace);
-    isd::VerifyArgs va{};
+    VerifyArgs va{};
     va.p = static_cast<const char*>(p_logits);
     va.ldp_bytes = ld_p * esz;
     va.q = static_cast<const char*>(q_logits);
@@ -174,46 +175,43 @@ isd_status verify_impl(const void* p_logits, int64_t ld_p, const void* q_logits,
     va.vocab = vocab;
     va.ck = pl.ck;
     va.nck = pl.nck;
-    va.spseg = pl.spseg;
-    va.nseg = pl.nseg;
-    va.ckt = pl.ckt;
-    va.nt = pl.nt;
-    va.tpt = pl.tpt;
-    va.ntask = pl.ntask;
-    va.n_main = 2LL * total_positions * pl.nseg;
-    // Rows of the first position of every sequence, both p and q, kept in L2
-    // while they fit in about a third of it.
-    va.keep_first = 2.0 * num_seqs * vocab * esz <= kL2KeepBytes ? 1 : 0;
+    va.ps = pl.ps;
+    va.np = pl.np;
     va.seed = seed;
-    va.relax_log2 = tau > 0.0f ? std::log2(1.0f + tau) : 0.0f;
     va.offset = offset;
-    va.ctl = reinterpret_cast<isd::VerifyCtl*>(ws + lay.ctl);
+    va.relax_log2 = o.tau > 0.0f ? std::log2(1.0f + o.tau) : 0.0f;
+    va.sampler = o.sampler;
+    va.ctl = reinterpret_cast<VerifyCtl*>(ws + lay.ctl);
     va.seq_count = reinterpret_cast<int*>(ws + lay.seq_count);
-    va.seq_pending = reinterpret_cast<int*>(ws + lay.seq_pending);
-    va.n_tail = num_seqs + (fused ? total_positions : 0);
-    va.fused = fused ? 1 : 0;
-    va.qnew = static_cast<const char*>(qnew_logits);
-    va.ldqnew_bytes = ld_qnew * esz;
-    va.proposals = proposals;
-    va.valid = valid;
-    va.tail_count = reinterpret_cast<int*>(ws + lay.tail_count);
-    va.tails = reinterpret_cast<isd::SeqTail*>(ws + lay.tails);
-    va.tasks = reinterpret_cast<int4*>(ws + lay.tasks);
-    va.task_ready = reinterpret_cast<int*>(ws + lay.task_ready);
+    va.seq_done = reinterpret_cast<int*>(ws + lay.seq_done);
+    va.dready = reinterpret_cast<uint64_t*>(ws + lay.dready);
+    va.n_tail = num_seqs + (o.fused ? total_positions : 0);
+    va.tdesc = reinterpret_cast<uint64_t*>(ws + lay.tdesc);
+    va.tpart = reinterpret_cast<uint64_t*>(ws + lay.tpart);
+    va.tcount = reinterpret_cast<int*>(ws + lay.tcount);
+    va.tbsum = reinterpret_cast<float*>(ws + lay.tbsum);
     va.part = reinterpret_cast<float2*>(ws + lay.part);
-    va.tpart = reinterpret_cast<float2*>(ws + lay.tpart);
+    va.fused = o.fused ? 1 : 0;
+    va.qnew = static_cast<const char*>(o.qnew);
+    va.ldqnew_bytes = o.ld_qnew * esz;
+    va.proposals = o.proposals;
+    va.valid = o.valid;
     va.accept_len = accept_len;
     va.out_tokens = out_tokens;
     va.ratio = ratio;
     va.alpha = alpha;
+    va.wait_ns = o.wait_ns;
+    va.stall_seq = o.stall_seq;
+    // Units: at most one per chunk of every p and q row.
+    const long long units = (2LL * total_positions + num_seqs) * pl.nck;
     int grid = 1;
-    const isd_status gs = resident_grid(va.n_main, isd::kVerifyCtasPerSm, &grid);
+    const isd_status gs = resident_grid(units, kVerifyCtasPerSm, &grid);
     if (gs != ISD_OK) return gs;
-    if (isd::launch_verify(va, esz, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ISD_ERR_CUDA;
+    if (launch_verify(va, esz, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ISD_ERR_CUDA;
     return ISD_OK;
 }
 
-}  // namespace
+}  // namespace isd
 
 extern "C" {
 
@@ -223,9 +221,9 @@ isd_status isd_verify(const void* p_logits, int64_t ld_p, const void* q_logits, 
                       const float* temperature, uint64_t seed, uint64_t offset,
                       int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
                       void* workspace, size_t workspace_bytes, void* stream) {
-    return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
-                       total_positions, temperature, seed, offset, 0.0f, accept_len, out_tokens, ratio, alpha,
-                       false, nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
+    return isd::verify_run(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                           total_positions, temperature, seed, offset, accept_len, out_tokens, ratio, alpha,
+                           isd::VerifyOptions{}, workspace, workspace_bytes, stream);
 }
 
 isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
@@ -234,9 +232,31 @@ isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const void* q_
                               const float* temperature, uint64_t seed, uint64_t offset, float tau,
                               int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
                               void* workspace, size_t workspace_bytes, void* stream) {
-    return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
-                       total_positions, temperature, seed, offset, tau, accept_len, out_tokens, ratio, alpha,
-                       false, nullptr, 0, nullptr, nullptr, workspace, workspace_bytes, stream);
+    isd::VerifyOptions o;
+    o.tau = tau;
+    return isd::verify_run(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                           total_positions, temperature, seed, offset, accept_len, out_tokens, ratio, alpha, o,
+                           workspace, workspace_bytes, stream);
+}
+
+static isd_status verify_propose_with(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                                      isd_dtype dtype, int vocab, const int32_t* tokens,
+                                      const int32_t* seq_offsets, int num_seqs, int total_positions,
+                                      const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                                      int sampler, int32_t* accept_len, int32_t* out_tokens, float* ratio,
+                                      float* alpha, const void* qnew_logits, int64_t ld_qnew, int32_t* proposals,
+                                      uint8_t* valid, void* workspace, size_t workspace_bytes, void* stream) {
+    isd::VerifyOptions o;
+    o.tau = tau;
+    o.sampler = sampler;
+    o.fused = true;
+    o.qnew = qnew_logits;
+    o.ld_qnew = ld_qnew;
+    o.proposals = proposals;
+    o.valid = valid;
+    return isd::verify_run(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                           total_positions, temperature, seed, offset, accept_len, out_tokens, ratio, alpha, o,
+                           workspace, workspace_bytes, stream);
 }
 
 isd_status isd_verify_propose(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
@@ -246,9 +266,23 @@ isd_status isd_verify_propose(const void* p_logits, int64_t ld_p, const void* q_
                               int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
                               const void* qnew_logits, int64_t ld_qnew, int32_t* proposals, uint8_t* valid,
                               void* workspace, size_t workspace_bytes, void* stream) {
-    return verify_impl(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
-                       total_positions, temperature, seed, offset, tau, accept_len, out_tokens, ratio, alpha,
-                       true, qnew_logits, ld_qnew, proposals, valid, workspace, workspace_bytes, stream);
+    return verify_propose_with(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                               total_positions, temperature, seed, offset, tau, isd::kSamplerIcdf, accept_len,
+                               out_tokens, ratio, alpha, qnew_logits, ld_qnew, proposals, valid, workspace,
+                               workspace_bytes, stream);
+}
+
+isd_status isd_verify_propose_gumbel(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
+                                     isd_dtype dtype, int vocab, const int32_t* tokens,
+                                     const int32_t* seq_offsets, int num_seqs, int total_positions,
+                                     const float* temperature, uint64_t seed, uint64_t offset, float tau,
+                                     int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha,
+                                     const void* qnew_logits, int64_t ld_qnew, int32_t* proposals, uint8_t* valid,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    return verify_propose_with(p_logits, ld_p, q_logits, ld_q, dtype, vocab, tokens, seq_offsets, num_seqs,
+                               total_positions, temperature, seed, offset, tau, isd::kSamplerGumbel, accept_len,
+                               out_tokens, ratio, alpha, qnew_logits, ld_qnew, proposals, valid, workspace,
+                               workspace_bytes, stream);
 }
 
 isd_status isd_propose(const void* qnew_logits, int64_t ld, isd_dtype dtype, int vocab,

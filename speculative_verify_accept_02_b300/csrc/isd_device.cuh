@@ -27,10 +27,11 @@ constexpr int kErrWaitTimeout = 1;
 // ---------------------------------------------------------------------------
 // Philox4x64-10 — Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
 // easy as 1, 2, 3" (SC'11), the 4-word, 64-bit Philox bijection with ten
-// rounds and the Weyl key schedule.
+// rounds and the Weyl key schedule.  All four output words for one counter
+// and key.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t philox4x64_10_word0(uint64_t c0, uint64_t c1, uint64_t c2,
-                                                        uint64_t c3, uint64_t k0, uint64_t k1) {
+__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3, uint64_t k0,
+                                              uint64_t k1, uint64_t out[4]) {
     constexpr uint64_t kMul0 = 0xD2E7470EE14C6C93ULL, kMul1 = 0xCA5A826395121157ULL;
     constexpr uint64_t kWeyl0 = 0x9E3779B97F4A7C15ULL, kWeyl1 = 0xBB67AE8584CAA73BULL;
 #pragma unroll
@@ -48,7 +49,18 @@ __device__ __forceinline__ uint64_t philox4x64_10_word0(uint64_t c0, uint64_t c1
         c2 = n2;
         c3 = lo0;
     }
-    return c0;
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+// Output word 0 alone (the decision uniforms use only it).
+__device__ __forceinline__ uint64_t philox4x64_10_word0(uint64_t c0, uint64_t c1, uint64_t c2,
+                                                        uint64_t c3, uint64_t k0, uint64_t k1) {
+    uint64_t out[4];
+    philox4x64_10(c0, c1, c2, c3, k0, k1, out);
+    return out[0];
 }
 
 // The uniform of one decision: counter (offset, sequence, position, purpose),
@@ -200,6 +212,40 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// 64-bit words that carry a flag in their high half and 32 bits of data in
+// their low half.  An aligned 64-bit access is single-copy atomic, so a
+// reader that sees the flag also sees the data written with it: a consumer
+// polls the data itself, with no fence and no second load.
+__device__ __forceinline__ uint64_t flagged(uint32_t flag, uint32_t data) {
+    return (static_cast<uint64_t>(flag) << 32) | data;
+}
+__device__ __forceinline__ uint64_t ld_volatile_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_volatile_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Two flagged words at once (each 64-bit half is its own atomic access).
+__device__ __forceinline__ void st_volatile_v2u64(uint64_t* p, uint64_t v0, uint64_t v1) {
+    asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(v0), "l"(v1) : "memory");
+}
+__device__ __forceinline__ void ld_volatile_v2u64(const uint64_t* p, uint64_t& v0, uint64_t& v1) {
+    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(v0), "=l"(v1) : "l"(p) : "memory");
+}
+
+// A flagged word published with release semantics (cumulative: it also
+// publishes what this thread acquired before), and its acquiring read.
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Loads that bypass L1 (data written by other CTAs of the running grid).
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 __device__ __forceinline__ void st_volatile(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }

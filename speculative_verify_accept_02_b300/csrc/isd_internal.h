@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/isd.h"
+
 namespace isd {
 
 // One pipeline stage of the streaming kernel holds one chunk of one row.
@@ -66,39 +68,38 @@ constexpr int kProposeCtasPerSm = 2;
 // Each counter has a 128-byte line of its own: hundreds of CTAs poll and
 // update them concurrently.
 struct VerifyCtl {
-    alignas(128) int err;                  // error word (bounded waits)
-    alignas(128) unsigned long long grab;  // main items handed out (dynamic scheduling)
-    alignas(128) int tail_reserve;         // tail-task slots reserved by decisions
-    alignas(128) int tail_claim;           // tail-task tickets handed to producers
-    alignas(128) int finalized;            // sequences whose outputs are complete
-    alignas(128) int exited;               // CTAs that have finished
+    alignas(128) int err;                   // error word (bounded waits)
+    alignas(128) int tail_reserve;          // tail slots reserved by decisions
+    alignas(128) unsigned long long claim;  // tail-piece tickets handed to workers
+    alignas(128) unsigned long long dclaim; // decision tickets (sequence indices) handed to workers
+    alignas(128) int finalized;             // sequences whose outputs are complete
+    alignas(128) int exited;                // CTAs that have finished
 };
 
-// Tail kinds: which row(s) the work after a decision reads.
+// Tail modes: what the pieces of a draw after a decision reduce.
 enum TailMode : int {
-    kTailRes = 2,   // T > 0, rejection: residual max(0, p_j - q_j) over row pair j
-    kTailSoft = 3,  // T > 0: softmax draw from one row (bonus from p_{L+1}, or a proposal)
-    kTailArg = 4    // T = 0: argmax of one row (a proposal)
+    kTailRes = 1,   // T > 0, rejection: residual max(0, p_j - q_j) over row pair j
+    kTailSoft = 2,  // T > 0: softmax draw from one row (bonus from p_{L+1}, or a proposal)
+    kTailArg = 3    // T = 0: argmax of one row (a proposal)
 };
-// Flag on a tail mode: its row is a qnew row (a proposal draw of the fused
-// verify-and-propose call), not a p row.
-constexpr int kTailQnew = 8;
 
-// What a sequence's tail needs, written by its decision (48 bytes).
-// What a tail (one draw after a decision) needs: written by the decision,
-// read by the tail's producers and its selection (48 bytes).
-struct alignas(16) SeqTail {
-    int mode;         // TailMode, with kTailQnew for a proposal row
-    int a;            // accept length of the sequence
-    int prow, qrow;   // rows: p_j (or p_{L+1}, or the qnew row) and q_j
-    float c2;         // log2(e) / T
-    float nz0;        // p_j: log2 of its normaliser, p_j(v) = exp2(x_v c2 - nz0)
-    float nz1;        // q_j: the same
-    int seq;          // the sequence
-    int pos;          // position of the draw's uniform (1-based)
-    int tag;          // the uniform's purpose (CORRECT, BONUS or PROPOSE)
-    int dest;         // >= 0: out_tokens slot; < 0: proposals slot -1 - dest
-    int pad;
+// Sampler of the draws after a decision.
+enum Sampler : int {
+    kSamplerIcdf = 0,    // inverse CDF in vocabulary order, one uniform per draw
+    kSamplerGumbel = 1   // Gumbel-max, one uniform per vocabulary id and draw
+};
+
+// Words of a tail descriptor (each a flagged 64-bit word, flag = slot + 1).
+enum TailWord : int {
+    kTwPRow = 0,   // the drawn row: p_j, p_{L+1}, or a qnew row
+    kTwQRow = 1,   // q_j (residual)
+    kTwMeta = 2,   // mode | qnew << 4 | tag << 8 | pos << 16 | draws of the sequence << 24
+    kTwC2 = 3,     // log2(e) / T
+    kTwNz0 = 4,    // log2 of p_j's normaliser in the exp2 domain
+    kTwNz1 = 5,    // the same for q_j
+    kTwSeq = 6,    // the sequence
+    kTwDest = 7,   // >= 0: out_tokens slot; < 0: proposals slot -1 - dest
+    kTailWords = 8
 };
 
 struct VerifyArgs {
@@ -112,32 +113,27 @@ struct VerifyArgs {
     int num_seqs;
     int total;
     int vocab;
-    int ck;           // elements of a main sub-chunk (one stage)
-    int nck;          // main sub-chunks per row
-    int spseg;        // sub-chunks per segment (one main item)
-    int nseg;         // segments per row
-    int ckt;          // elements of a tail sub-chunk (half a stage per row)
-    int nt;           // tail sub-chunks per row
-    int tpt;          // tail sub-chunks per tail task
-    int ntask;        // tail tasks per sequence
-    long long n_main; // 2 * total * nseg main items
-    int keep_first;   // 1: first-position rows of T > 0 sequences are kept in L2 for their tails
+    int ck;            // elements of a main chunk (one stage, one unit)
+    int nck;           // chunks per row
+    int ps;            // elements of a tail piece
+    int np;            // pieces per row
     uint64_t seed;
     uint64_t offset;
-    float relax_log2; // log2(1 + tau) of relaxed acceptance, 0 for strict
+    float relax_log2;  // log2(1 + tau) of relaxed acceptance, 0 for strict
+    int sampler;       // Sampler of the draws after a decision
     VerifyCtl* ctl;
-    int* seq_count;   // [C] main items finished
-    // Tails are indexed by tail id: sequence i's correction or bonus is tail
-    // i; with `fused`, the proposal draw of qnew row r is tail C + r.
-    int n_tail;       // C, or C + total when fused
-    int* tail_count;  // [n_tail] tail tasks finished
-    SeqTail* tails;   // [n_tail]
-    int4* tasks;      // [n_tail * ntask][2] task records in reservation order:
-                      // {tail id, task, mode, row}, {q row, c2, nz0, nz1}
-    int* task_ready;  // [n_tail * ntask] 1 once the slot's task is published
-    float2* part;     // [2 * total * nseg] per (row slot, segment) partials
-    float2* tpart;    // [n_tail * nt * 8] per (tail sub-chunk, consumer warp) slice partials
-    int* seq_pending; // [C] draws of the sequence still to finish
+    int* seq_count;    // [C] units counted
+    int* seq_done;     // [C] draws after the decision finished
+    uint64_t* dready;  // [C] flagged word: every unit of the sequence is counted
+    // Tails are queued in the order decisions reserve them: a sequence's
+    // correction or bonus draw, and in the fused call one draw per qnew row
+    // of a sequence that accepted its whole stride.
+    int n_tail;        // capacity: C, or C + total when fused
+    uint64_t* tdesc;   // [n_tail][kTailWords] flagged descriptor words
+    uint64_t* tpart;   // [n_tail][np][4] flagged piece results
+    int* tcount;       // [n_tail] pieces finished
+    float* tbsum;      // [n_tail][np][32] per-lane block sums of each piece (published before its result)
+    float2* part;      // [2 * total][nck] per (row slot, chunk) partials
     // The fused call (isd_verify_propose): the next stride's proposals of the
     // sequences that accept their whole stride, drawn from qnew rows.
     int fused;
@@ -149,16 +145,56 @@ struct VerifyArgs {
     int32_t* out_tokens;
     float* ratio;
     float* alpha;
+    // Bounds of the waits on other CTAs (global-timer nanoseconds), and a
+    // check hook: the decision of sequence `stall_seq` (if >= 0) publishes
+    // nothing, so that the waits for it run out (isd_debug.h).
+    uint64_t wait_ns;
+    int stall_seq;
 };
 
-// Largest number of tail sub-chunks per row the verify kernel supports
-// (vocabularies up to 523,264 bf16 or 261,632 fp32 ids).
-constexpr int kMaxTailChunks = 128;
+// Bytes of a tail piece per row, and the most pieces per row the verify
+// kernel supports (vocabularies up to 524,288 bf16 or 262,144 fp32 ids).
+constexpr int kPieceBytes = 8192;
+constexpr int kMaxPieces = 128;
 
 // Resident CTAs of the verify kernel per SM.
 constexpr int kVerifyCtasPerSm = 2;
 
 cudaError_t launch_verify(const VerifyArgs& a, int elem_bytes, int grid, cudaStream_t stream);
+
+// Default bound of the verify kernel's waits on other CTAs (nanoseconds).
+constexpr uint64_t kVerifyWaitNs = 4000000000ull;
+
+// What distinguishes the verify entry points: relaxed acceptance, the
+// sampler, the fused proposal draws, and the check hooks of isd_debug.h.
+struct VerifyOptions {
+    float tau = 0.0f;
+    int sampler = kSamplerIcdf;
+    bool fused = false;
+    const void* qnew = nullptr;
+    int64_t ld_qnew = 0;
+    int32_t* proposals = nullptr;
+    uint8_t* valid = nullptr;
+    uint64_t wait_ns = kVerifyWaitNs;
+    int stall_seq = -1;
+};
+
+// The host-side checks of a verify call, everything but the workspace:
+// ISD_OK or the status the call returns (it then launches nothing).
+isd_status verify_check(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q, isd_dtype dtype,
+                        int vocab, const int32_t* tokens, const int32_t* seq_offsets, int num_seqs,
+                        int total_positions, const float* temperature, int32_t* accept_len, int32_t* out_tokens,
+                        float* ratio, float* alpha, const VerifyOptions& o);
+
+// Workspace bytes of a verify call (0 for an invalid shape).
+size_t verify_workspace(int num_seqs, int total_positions, int vocab, isd_dtype dtype, bool fused);
+
+// Checks, then one launch of the verify kernel.
+isd_status verify_run(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q, isd_dtype dtype,
+                      int vocab, const int32_t* tokens, const int32_t* seq_offsets, int num_seqs,
+                      int total_positions, const float* temperature, uint64_t seed, uint64_t offset,
+                      int32_t* accept_len, int32_t* out_tokens, float* ratio, float* alpha, const VerifyOptions& o,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_propose(const ProposeArgs& a, int elem_bytes, int grid, cudaStream_t stream);

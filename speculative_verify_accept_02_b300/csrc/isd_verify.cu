@@ -5,44 +5,48 @@
 // correction work), optionally with the next stride's proposal draws of the
 // fused step (§3.2: one forward verifies and proposes).
 //
-// Work is handed out dynamically, in sequence order, by a global counter:
-//   main item   one segment (up to eight 16 KB sub-chunks) of one p_k or q_k
-//               row; greedy sequences stream their final anchor p_{L+1} in
-//               place of their (unread) last q row.
-//   decision    once a sequence's last item is done: ratio_k =
-//               min(1, p_k(x_k) / q_k(x_k)), alpha, the accept prefix
-//               (Philox uniforms, one warp ballot; relaxed acceptance tests
-//               min(1, (1 + tau) p/q)) and the emitted prefix.  A greedy
-//               correction or bonus is complete here (argmaxes of the
-//               partials).
-//   tail task   otherwise the decision publishes tails on a device queue: the
-//               residual max(0, p_j - q_j) of the one rejected row pair, or
-//               the final anchor row p_{L+1}; in the fused call also one per
-//               qnew row of a sequence that accepted its whole stride.
-//               Producers take queued tail tasks before new main items.
-//   selection   once a tail's last task is done: the draw by inverse CDF, a
-//               slice of about 500 ids from the tail partials, then an
-//               in-order scan of that one slice (an argmax merge at T = 0).
+// Three kinds of work:
+//   unit       one chunk (at most 16 KB) of one row a decision needs: p_k and
+//              q_k for k <= L_i (T > 0), or p_1 .. p_{L+1} (T = 0).  Units
+//              are numbered in sequence order and dealt round-robin to the
+//              CTAs, so all CTAs walk the batch front to back in step and the
+//              sequences complete one after another at an even pace.  A
+//              unit's softmax partial (max, sum) or argmax lands in the
+//              workspace and is counted against its sequence.
+//   decision   once a sequence's last unit is counted: ratio_k =
+//              min(1, p_k(x_k) / q_k(x_k)), alpha, the accept prefix
+//              (Philox uniforms, one warp ballot; relaxed acceptance tests
+//              min(1, (1 + tau) p/q)) and the emitted prefix; a greedy
+//              correction or bonus (argmaxes of the partials).  The draws
+//              left are published as tails.
+//   tail       one draw after a decision: from the residual max(0, p_j - q_j)
+//              of the one rejected row pair, from the final anchor p_{L+1}
+//              (bonus), or from a qnew row (proposals of the fused call).  A
+//              tail is cut into pieces of 4 KB per row; worker warps of every
+//              CTA take pieces by ticket and reduce them with vector loads
+//              (the rows were streamed moments before, so mostly from L2).
+//              The worker that finishes a tail's last outstanding piece makes
+//              the draw: by inverse CDF (the piece from the piece sums, then
+//              an in-order scan of that piece) or, with the Gumbel-max
+//              sampler, as the largest perturbed score over the pieces.  No
+//              worker ever waits for another.
 //
-// Warp roles of a CTA:
-//   scheduler   (one thread) takes work: the next main item from the global
-//               counter into a 2-entry work ring, a published tail task into
-//               a priority slot; it absorbs every global memory round trip;
-//   issuer      (one thread) streams the scheduled sub-chunks into a 4-stage
-//               shared-memory ring with 1-D bulk copies under L2 eviction
-//               policies, serving the priority slot between any two
-//               sub-chunks; it never waits on global memory;
-//   consumers   (8 warps) fold each stage into per-thread online softmax
-//               partials (packed bf16 maxima, packed fp32 FMAs, one ex2 per
-//               logit) or an exact argmax; at the end of an item every warp
-//               hands its warp partial to the bookkeeper through a record
-//               ring and moves on: consumers never wait on each other or on
-//               global memory;
-//   bookkeeper  (one warp) merges the records in batches, stores partials and
-//               counts finished items per sequence with device-scope atomics;
-//   finishers   (two warps) run the decisions and selections it triggers.
-// The grid exits once every sequence is final; its last CTA re-zeroes the
-// control block for the next call.  Every wait is bounded by the global timer.
+// Warps of a CTA:
+//   consumers  (8) reduce the staged chunk, one partial per warp, handed to
+//              the bookkeeper through a record ring;
+//   producer   (one thread) streams the CTA's units into a 4-stage ring with
+//              1-D bulk copies completing on mbarriers;
+//   bookkeeper merges the eight warp partials of a unit, stores and counts
+//              it (device-scope acquire-release), and marks a sequence whose
+//              count completes ready;
+//   workers    (2) take decisions and tail pieces by ticket, and make the
+//              draws.
+// Tail descriptors and piece results travel as 64-bit words that carry a
+// flag in their high half, so a reader polls the data itself: one global
+// round trip per hand-over.  The grid exits once every sequence is final;
+// its last CTA re-zeroes the control block.  Every wait is bounded by the
+// global timer; on expiry the error word is set and every accept length
+// reads -2.
 #include <climits>
 #include <type_traits>
 
@@ -52,97 +56,69 @@
 namespace isd {
 namespace {
 
-constexpr int kCW = 8;                    // consumer warps
-constexpr int kCT = kCW * 32;             // consumer threads
-constexpr int kIssuerWarp = kCW;
+constexpr int kCW = 8;                 // consumer warps
+constexpr int kCT = kCW * 32;          // consumer threads
+constexpr int kProdWarp = kCW;
 constexpr int kBookWarp = kCW + 1;
-constexpr int kSchedWarp = kCW + 2;
-constexpr int kFinWarp = kCW + 3;         // first of kFinishers finisher warps
-constexpr int kFinishers = 2;
-constexpr int kThreadsV = kCT + 32 * (3 + kFinishers);  // + issuer, bookkeeper, scheduler, finishers
-constexpr int kStagesV = 4;
-constexpr int kJobs = 16;                 // job ring between bookkeeper and finisher
-constexpr int kWork = 2;                  // work ring between scheduler and issuer
-constexpr int kRecs = 8;                  // record ring between consumers and bookkeeper
+constexpr int kWorkWarp = kCW + 2;     // first of kWorkers worker warps
+constexpr int kWorkers = 2;
+constexpr int kThreadsV = 32 * (kCW + 2 + kWorkers);
+constexpr int kStagesV = 3;
+constexpr int kRecs = 16;              // record ring between consumers and bookkeeper
 constexpr int kVecPT = kStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
-constexpr int kHalf = kStageBytes / 2;          // tail stages: [p piece | q piece]
-constexpr int kSmemSeqs = 512;                  // batches up to this size keep offsets in shared memory
-constexpr int kSmemToks = 2048;                 // batches up to this many positions keep their tokens there
-constexpr int kSliceMax = 512;                  // ids in one tail slice (tail sub-chunk / 8 warps)
-static_assert(kHalf / 2 <= kSliceMax * kCW, "a tail sub-chunk of bf16 ids splits into slices of at most kSliceMax");
+constexpr int kSmemSeqs = 1024;        // batches up to this size keep offsets in shared memory
+constexpr int kSmemToks = 2048;        // batches up to this many positions keep their tokens there
+constexpr int kPartWords = 4;          // flagged words per piece result
 static_assert(kVecPT * 16 * kCT == kStageBytes, "stage split");
-static_assert(kHalf / kCW <= kSliceMax * 2, "a slice fits its staging buffer");
-static_assert(kHalf / kCW <= 64 * 16, "a tail slice is at most two 16-byte vectors per lane");
+// A staged piece row keeps 16 bytes of padding after every 256: a lane that
+// reads its own contiguous block of ids then meets no bank conflict.
+constexpr int kPieceRow = kPieceBytes + kPieceBytes / 16;
+__host__ __device__ constexpr int pad_off(int b) { return b + ((b >> 8) << 4); }
+static_assert(kMaxPieces % 32 == 0, "pieces per lane");
 
-enum : int { kEnd = 0, kMain = 1 };  // descriptor / record kinds besides the TailMode values
-enum : int { kFirst = 1, kLast = 2 };
+enum : int { kEnd = 0, kUnit = 1 };
 
 struct Desc {
     int kind;
-    int flags;
     int seq;
-    int slot;      // main: row slot (2 r + {0: p, 1: q}); tail: tail sub-chunk
-    int seg;
-    int expect;    // main: items of the sequence
-    int e0;        // first element of the sub-chunk in its row
-    int n;         // elements of the sub-chunk
-    int nvec;      // main: 16-byte vectors in the stage
-    int nsm0, skip0, nsm1, skip1;
-    const char* tail0;  // global address of the first element not in shared memory
-    const char* tail1;
-    float c2, nz0, nz1;
+    int slot;        // row slot of the partial: 2 r + {0: p, 1: q}
+    int chunk;
+    int expect;      // units of the sequence
+    int e0;          // first element of the chunk in its row
+    int n;           // elements of the chunk
+    int nvec;        // 16-byte vectors in shared memory
+    int nsm;         // elements of the chunk in shared memory
+    int skip;        // elements before e0 in the first vector
+    const char* tail;  // global address of the first element not in shared memory
+    float c2;        // log2(e) / T, or 0 for an argmax
 };
-
-// flags of a main record: which partial the warps hand in.
-enum : int { kRecSoft = 0, kRecArg = 1 };
 
 struct Rec {
-    int kind, flags, seq, slot, seg, expect;
+    int kind, seq, slot, chunk, expect, arg;
     float2 wp[kCW];  // one partial per consumer warp
-};
-
-// One unit of scheduled streaming: sub-chunks [c0, c1) of one row (main item)
-// or of a tail row (pair).
-struct Work {
-    int kind;
-    int seq, slot, seg, expect, c0, c1;
-    int keep;  // load under the L2 evict_last policy (rows likely re-read by a tail)
-    float c2, nz0, nz1;
-    const char* row0;
-    const char* row1;
-};
-
-// A finisher job: decide or select one sequence, or stop.
-enum : int { kJobEnd = 0, kJobDecide = 1, kJobSelect = 2 };
-struct Job {
-    int kind, seq;
 };
 
 struct SmemV {
     alignas(128) unsigned char stage[kStagesV][kStageBytes];
+    alignas(16) unsigned char piece[kWorkers][2][kPieceRow];     // each worker's staged piece of p and q
+    float4 ppart[kWorkers][kMaxPieces];                         // each worker's piece results of one draw
     uint64_t full[kStagesV];
     uint64_t empty[kStagesV];
     uint64_t rec_full[kRecs];
     uint64_t rec_empty[kRecs];
-    uint64_t work_full[kWork];
-    uint64_t work_empty[kWork];
-    uint64_t prio_full;   // scheduler -> issuer: one tail task ahead of queued main items
-    uint64_t prio_empty;
-    uint64_t job_full[kJobs];
-    uint64_t job_empty[kJobs];
-    Job job[kJobs];
-    alignas(16) float2 tsel[kFinishers][kMaxTailChunks * kCW];  // each finisher's copy of one sequence's slice partials
-    alignas(16) unsigned char sslice[kFinishers][2][kSliceMax * 2];  // each finisher's chosen slice of p and q
-    int job_take;
     Desc desc[kStagesV];
-    Work work[kWork];
-    Work prio;
     Rec rec[kRecs];
     int n_valid;
     int batch_bad;
     int offs[kSmemSeqs + 1];
     float temp[kSmemSeqs];
     int tok[kSmemToks];
+};
+
+// A decoded tail descriptor.
+struct Tail {
+    int prow, qrow, mode, qnew, tag, pos, npub, seq, dest;
+    float c2, nz0, nz1;
 };
 
 template <typename Elem>
@@ -153,20 +129,53 @@ __device__ __forceinline__ float load_elem(const void* p) {
         return *static_cast<const float*>(p);
 }
 
-// Element e of a staged piece: shared memory first, then the unaligned tail.
-template <typename Elem>
-__device__ __forceinline__ float piece_elem(const unsigned char* st, int nsm, int skip, const char* tail, int e) {
-    return e < nsm ? load_elem<Elem>(st + static_cast<size_t>(e + skip) * sizeof(Elem))
-                   : load_elem<Elem>(tail + static_cast<size_t>(e - nsm) * sizeof(Elem));
+__device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Sum of N values as a balanced tree (short dependency chains).
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+    if constexpr (N == 1) {
+        return v[0];
+    } else {
+        return tree_sum<N / 2>(v) + tree_sum<N - N / 2>(v + N / 2);
+    }
 }
 
-// Residual weight max(0, p - q) of one id, and p itself.
-// nz0, nz1: log2 of the normalisers of p and q in the exp2 domain, so that
-// p(v) = exp2(x_v c2 - nz0).
+
+// Residual weight max(0, p - q) of one id, and p itself.  nz0, nz1: log2 of
+// the normalisers of p and q in the exp2 domain, so p(v) = exp2(x_v c2 - nz0).
 __device__ __forceinline__ float resid_w(float xp, float xq, float c2, float nz0, float nz1, float& pv) {
     pv = soft_w(xp, c2, nz0);
     const float qv = soft_w(xq, c2, nz1);
     return fmaxf(0.0f, __fsub_rn(pv, qv));
+}
+
+// log2 by the hardware approximation (absolute error about 2^-22, subnormal
+// inputs kept).
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(-ln u) of a Gumbel uniform u in (0, 1): -log2(-ln u) is the Gumbel
+// noise in log2 units.  Below 1/2, -ln u = -ln 2 log2 u keeps its relative
+// accuracy; near u = 1 it is taken as -log1p(u - 1), u - 1 being exact there.
+__device__ __forceinline__ float log2_neg_ln(float u) {
+    const float nl = u < 0.5f ? -0.6931471805599453f * lg2_approx(u) : -log1pf(-(1.0f - u));
+    return lg2_approx(nl);
+}
+
+// The Gumbel uniforms of ids 4b .. 4b+3 of one draw: counter (offset,
+// sequence, position, 16 + purpose + 256 b), key (seed, 0), one output word
+// per id; u = (top 23 bits + 1/2) 2^-23, exact in float, inside (0, 1).
+__device__ __forceinline__ void gumbel_block(const VerifyArgs& a, const Tail& t, int b, float u[4]) {
+    uint64_t w[4];
+    philox4x64_10(a.offset, static_cast<uint64_t>(t.seq), static_cast<uint64_t>(t.pos),
+                  16ull + static_cast<uint64_t>(t.tag) + 256ull * static_cast<uint64_t>(b), a.seed, 0, w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        u[j] = (static_cast<float>(static_cast<uint32_t>(w[j] >> 41)) + 0.5f) * (1.0f / 8388608.0f);
 }
 
 // Softmax partials in the mc domain: (mc, s) holds sum exp2(x c2 - mc);
@@ -185,18 +194,6 @@ __device__ __forceinline__ void warp_merge_arg(float& M, int& I) {
 }
 
 // Sequence lookups on a table in shared memory (small batches) or global memory.
-__device__ __forceinline__ int seq_of_position_t(const int* offs, int C, int r) {
-    int lo = 0, hi = C - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (offs[mid] <= r)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
 __device__ __forceinline__ SeqInfo seq_info_t(const int* offs, const float* temp, int i, int total) {
     SeqInfo s;
     s.start = offs[i];
@@ -210,8 +207,11 @@ __device__ __forceinline__ SeqInfo seq_info_t(const int* offs, const float* temp
 
 __device__ __forceinline__ SeqInfo seq_lookup(const VerifyArgs& a, const SmemV& sm, int i) {
     return a.num_seqs <= kSmemSeqs ? seq_info_t(sm.offs, sm.temp, i, a.total)
-                                   : seq_info_t(a.seq_offsets, a.temperature, i, a.total);
+                                   : seq_info(a.seq_offsets, a.temperature, i, a.total);
 }
+
+// Rows a valid sequence streams: p_k and q_k (T > 0), or p_1 .. p_{L+1} (T = 0).
+__device__ __forceinline__ int rows_of(const SeqInfo& s) { return s.T > 0.0f ? 2 * s.len : s.len + 1; }
 
 // ---- outputs of an invalid sequence (one warp) -------------------------------
 __device__ void write_invalid(const VerifyArgs& a, int i, const SeqInfo& s, int lane, int code) {
@@ -260,26 +260,23 @@ __device__ __forceinline__ Piece make_piece(const char* row, int e0, int n) {
     return pc;
 }
 
-// Slice of a tail sub-chunk of n ids owned by consumer warp w: ids [b, e).
-// Slices start on 16-byte boundaries of the sub-chunk.
-template <int E>
-__device__ __forceinline__ void tail_slice(int n, int w, int& b, int& e) {
-    constexpr int vec = 16 / E;
-    const int spw = ((n + kCW - 1) / kCW + vec - 1) / vec * vec;
-    b = min(n, w * spw);
-    e = min(n, b + spw);
+// =============================================================================
+// Decision (bookkeeper warp; lane k handles position k + 1)
+// =============================================================================
+
+// Publish tail `slot`: eight flagged words (two per 16-byte store).
+__device__ __forceinline__ void publish_tail(const VerifyArgs& a, int slot, const uint32_t w[kTailWords]) {
+    const uint32_t f = static_cast<uint32_t>(slot) + 1u;
+    uint64_t* d = a.tdesc + static_cast<size_t>(slot) * kTailWords;
+#pragma unroll
+    for (int k = 0; k < kTailWords; k += 2) st_volatile_v2u64(d + k, flagged(f, w[k]), flagged(f, w[k + 1]));
 }
 
-// =============================================================================
-// Bookkeeper warp
-// =============================================================================
-
-// Decision of sequence i (L <= 32: lane k handles position k + 1).
 template <typename Elem>
-__device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lane) {
+__device__ void decide(const VerifyArgs& a, SmemV& sm, int wi, int i, int lane) {
     constexpr int E = sizeof(Elem);
-    // The bookkeeper's acquiring count saw every partial of this sequence
-    // published; the job ring orders that before this warp's loads.
+    // The acquiring read of the sequence's ready word saw every partial of it
+    // published.
     const SeqInfo s = seq_lookup(a, sm, i);
     const int L = s.len;
     const float T = s.T;
@@ -295,34 +292,59 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         }
         return;
     }
+    const bool stall = i == a.stall_seq;
+    // A T > 0 sequence always makes one draw after its decision: its queue
+    // slot is reserved now, so that the round trip overlaps the loads below.
+    int tslot = 0;
+    if (T > 0.0f && lane == 0 && !stall) tslot = atomicAdd(&a.ctl->tail_reserve, 1);
+    // The sequence's partials are one contiguous block, [2 L rows][nck]: it
+    // is staged in this worker's shared buffer in one round trip, together
+    // with the proposed tokens' logits, when it fits.
+    const float2* blk = a.part + static_cast<size_t>(2 * s.start) * a.nck;
+    const int nblk = 2 * L * a.nck;
+    const bool staged = nblk * static_cast<int>(sizeof(float2)) <= static_cast<int>(sizeof(sm.piece[wi]));
+    float2* sblk = reinterpret_cast<float2*>(&sm.piece[wi][0][0]);
+    if (staged)
+        for (int v = lane; v < nblk / 2; v += 32) cp_async16(sblk + 2 * v, blk + 2 * v);
+    float zp = 0.0f, zq = 0.0f;
+    if (mine && T > 0.0f) {  // the proposed token's logits, from rows read moments ago
+        zp = load_elem<Elem>(a.p + static_cast<int64_t>(r + i) * a.ldp_bytes + static_cast<size_t>(x) * E);
+        zq = load_elem<Elem>(a.q + static_cast<int64_t>(r) * a.ldq_bytes + static_cast<size_t>(x) * E);
+    }
+    // The accept uniform does not depend on the loads: it is drawn while
+    // they are in flight.
+    const float u_acc = (mine && T > 0.0f) ? decision_uniform(a.seed, a.offset, i, lane + 1, kTagAccept) : 0.0f;
+    if (staged) cp_async_wait_all();
+    __syncwarp();
+    const float2* part_of = staged ? sblk : blk;
     float ratio = 0.0f, racc = 0.0f, Mp = -INFINITY, Sp = 0.0f, Mq = -INFINITY, Sq = 0.0f;
     int amax = INT_MAX;
     if (mine) {
-        const float2* pp = a.part + static_cast<size_t>(2 * r) * a.nseg;
-        const float2* pq = pp + a.nseg;
-        // Every load of this lane is issued before any is used.
-        float zp = 0.0f, zq = 0.0f;
-        if (T > 0.0f) {  // the proposed token's logits, from rows read moments ago
-            zp = load_elem<Elem>(a.p + static_cast<int64_t>(r + i) * a.ldp_bytes + static_cast<size_t>(x) * E);
-            zq = load_elem<Elem>(a.q + static_cast<int64_t>(r) * a.ldq_bytes + static_cast<size_t>(x) * E);
-        }
-        float M = -INFINITY;
-        for (int j0 = 0; j0 < a.nseg; j0 += 8) {
-            float2 u[8], v[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const int j = j0 + jj;
-                u[jj] = j < a.nseg ? __ldcg(pp + j) : make_float2(-INFINITY, 0.0f);
-                v[jj] = (T > 0.0f && j < a.nseg) ? __ldcg(pq + j) : make_float2(-INFINITY, 0.0f);
+        const float2* pp = part_of + static_cast<size_t>(2 * lane) * a.nck;
+        const float2* pq = pp + a.nck;
+        auto part = [&](const float2* b, int j) -> float2 { return staged ? b[j] : __ldcg(b + j); };
+        if (T > 0.0f) {
+            // Two passes, so that the exponentials are independent of each
+            // other: the largest mc, then the sum rescaled to it.
+#pragma unroll 4
+            for (int j = 0; j < a.nck; ++j) {
+                Mp = fmaxf(Mp, part(pp, j).x);
+                Mq = fmaxf(Mq, part(pq, j).x);
             }
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                if (T > 0.0f) {
-                    merge_mc(Mp, Sp, u[jj].x, u[jj].y);
-                    merge_mc(Mq, Sq, v[jj].x, v[jj].y);
-                } else if (j0 + jj < a.nseg) {
-                    merge_argmax(M, amax, u[jj].x, __float_as_int(u[jj].y));
-                }
+            float sp4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sq4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+            for (int j = 0; j < a.nck; ++j) {
+                const float2 u = part(pp, j), v = part(pq, j);
+                if (u.x != -INFINITY) sp4[j & 3] += u.y * ex2_approx(u.x - Mp);
+                if (v.x != -INFINITY) sq4[j & 3] += v.y * ex2_approx(v.x - Mq);
+            }
+            Sp = tree_sum<4>(sp4);
+            Sq = tree_sum<4>(sq4);
+        } else {
+            float M = -INFINITY;
+            for (int j = 0; j < a.nck; ++j) {
+                const float2 u = part(pp, j);
+                merge_argmax(M, amax, u.x, __float_as_int(u.y));
             }
         }
         if (T > 0.0f) {
@@ -338,7 +360,7 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         }
     }
     bool acc = false;
-    if (mine) acc = T > 0.0f ? decision_uniform(a.seed, a.offset, i, lane + 1, kTagAccept) < racc : ratio == 1.0f;
+    if (mine) acc = T > 0.0f ? u_acc < racc : ratio == 1.0f;
     const unsigned bits = __ballot_sync(0xffffffffu, acc);
     const int na = min(bits == 0xffffffffu ? 32 : __ffs(~bits) - 1, L);
     const float total = warp_sum(ratio);
@@ -362,18 +384,17 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         if (!props)
             for (int m = lane; m < L; m += 32) a.proposals[s.start + m] = -1;
     }
-    int tok = -1;  // greedy: the token, known now
     if (T == 0.0f) {
         // Greedy: the correction is the argmax of p_j, already known; the
         // bonus is the argmax of p_{L+1}, streamed in the last position's q
         // slot.
-        tok = amax_j;
+        int tok = amax_j;
         if (na == L) {
-            const float2* pb = a.part + static_cast<size_t>(2 * (s.start + L - 1) + 1) * a.nseg;
+            const float2* pb = part_of + static_cast<size_t>(2 * (L - 1) + 1) * a.nck;
             float M = -INFINITY;
             int I = INT_MAX;
-            for (int g = lane; g < a.nseg; g += 32) {
-                const float2 v = __ldcg(pb + g);
+            for (int g = lane; g < a.nck; g += 32) {
+                const float2 v = staged ? pb[g] : __ldcg(pb + g);
                 merge_argmax(M, I, v.x, __float_as_int(v.y));
             }
             warp_merge_arg(M, I);
@@ -381,303 +402,62 @@ __device__ void decide_warp(const VerifyArgs& a, const SmemV& sm, int i, int lan
         }
         if (lane == 0) a.out_tokens[s.start + i + na] = tok;
     }
-    // Tails: the correction or bonus draw (T > 0), then one per proposal row.
-    const int n_tok = T > 0.0f ? 1 : 0;
-    const int n_pub = n_tok + (props ? L : 0);
-    if (n_pub == 0) {
-        if (lane == 0) {
-            a.seq_count[i] = 0;
-            finalize(a);
-        }
+    if (stall) {  // check hook: nothing is published, the sequence never completes
+        if (lane == 0) a.seq_count[i] = 0;
         return;
     }
-    const int mode_tok = na < L ? kTailRes : kTailSoft;
-    const int mode_prop = (T > 0.0f ? kTailSoft : kTailArg) | kTailQnew;
+    // Draws left: the correction or bonus (T > 0), then one per proposal row.
+    const int n_tok = T > 0.0f ? 1 : 0;
+    const int n_prop = props ? L : 0;
+    const int n_pub = n_tok + n_prop;
+    if (lane == 0) a.seq_count[i] = 0;
+    if (n_pub == 0) {
+        if (lane == 0) finalize(a);
+        return;
+    }
+    int pbase = 0;
+    if (n_prop > 0 && lane == 0) pbase = atomicAdd(&a.ctl->tail_reserve, n_prop);
+    tslot = __shfl_sync(0xffffffffu, tslot, 0);
+    pbase = __shfl_sync(0xffffffffu, pbase, 0);
     float nz0 = 0.0f, nz1 = 0.0f;
     if (na < L) {
         nz0 = __fadd_rn(mc0, log2f(sp0));
         nz1 = __fadd_rn(mc1, log2f(sq0));
     }
-    // Tail record k of this decision (k < n_tok: the token; else proposal
-    // row k - n_tok): its tail id and what its producers and selection need.
-    auto tail_of = [&](int k, SeqTail& t) -> int {
-        t = SeqTail{};
-        t.seq = i;
-        t.a = na;
-        t.c2 = c2;
-        if (k < n_tok) {
-            t.mode = mode_tok;
-            t.prow = s.start + i + na;  // p_j, or p_{L+1} when na == L
-            t.qrow = s.start + na;
-            t.nz0 = nz0;
-            t.nz1 = nz1;
-            t.pos = na + 1;
-            t.tag = na < L ? kTagCorrect : kTagBonus;
-            t.dest = s.start + i + na;
-            return i;
-        }
-        const int row = s.start + (k - n_tok);  // qnew row of position m = k - n_tok + 1
-        t.mode = mode_prop;
-        t.prow = row;
-        t.pos = k - n_tok + 1;
-        t.tag = kTagPropose;
-        t.dest = -1 - row;
-        return a.num_seqs + row;
-    };
-    int base = 0;
-    if (lane == 0) {
-        a.seq_pending[i] = n_pub;
-        a.seq_count[i] = 0;
-        base = atomicAdd(&a.ctl->tail_reserve, n_pub * a.ntask);
-    }
-    base = __shfl_sync(0xffffffffu, base, 0);
     for (int k = lane; k < n_pub; k += 32) {
-        SeqTail t;
-        const int id = tail_of(k, t);
-        a.tails[id] = t;
+        uint32_t w[kTailWords];
+        int slot;
+        if (k < n_tok) {
+            slot = tslot;
+            const int mode = na < L ? kTailRes : kTailSoft;
+            const int tag = na < L ? static_cast<int>(kTagCorrect) : static_cast<int>(kTagBonus);
+            w[kTwPRow] = static_cast<uint32_t>(s.start + i + na);  // p_j, or p_{L+1} when na == L
+            w[kTwQRow] = static_cast<uint32_t>(s.start + na);
+            w[kTwMeta] = static_cast<uint32_t>(mode | (tag << 8) | ((na + 1) << 16) | (n_pub << 24));
+            w[kTwNz0] = __float_as_uint(nz0);
+            w[kTwNz1] = __float_as_uint(nz1);
+            w[kTwDest] = static_cast<uint32_t>(s.start + i + na);
+        } else {
+            const int m = k - n_tok;  // position m + 1, qnew row start + m
+            slot = pbase + m;
+            const int mode = T > 0.0f ? kTailSoft : kTailArg;
+            w[kTwPRow] = static_cast<uint32_t>(s.start + m);
+            w[kTwQRow] = 0;
+            w[kTwMeta] = static_cast<uint32_t>(mode | (1 << 4) | (static_cast<int>(kTagPropose) << 8) |
+                                               ((m + 1) << 16) | (n_pub << 24));
+            w[kTwNz0] = 0;
+            w[kTwNz1] = 0;
+            w[kTwDest] = static_cast<uint32_t>(-1 - (s.start + m));
+        }
+        w[kTwC2] = __float_as_uint(c2);
+        w[kTwSeq] = static_cast<uint32_t>(i);
+        publish_tail(a, slot, w);
     }
-    // Every task record carries what its producer needs, so that taking a
-    // task is one round trip.
-    for (int e = lane; e < n_pub * a.ntask; e += 32) {
-        const int k = e / a.ntask, y = e - k * a.ntask;
-        SeqTail t;
-        const int id = tail_of(k, t);
-        int4* tr = a.tasks + 2 * static_cast<size_t>(base + e);
-        tr[0] = make_int4(id, y, t.mode, t.prow);
-        tr[1] = make_int4(t.qrow, __float_as_int(t.c2), __float_as_int(t.nz0), __float_as_int(t.nz1));
-    }
-    // Tail state and tasks are visible before any task is flagged ready.
-    __threadfence();
-    __syncwarp();
-    for (int e = lane; e < n_pub * a.ntask; e += 32) st_volatile(a.task_ready + base + e, 1);
 }
 
-// Selection of sequence i's token from its tail partials (one warp).  The
-// partials are per (tail sub-chunk, consumer warp) slice of about 500 ids;
-// the draw picks a slice from them, then scans that slice in vocabulary
-// order from registers.
-template <typename Elem>
-__device__ void select_warp(const VerifyArgs& a, SmemV& sm, int fi, int i, int lane) {
-    constexpr int E = sizeof(Elem);
-    // One round trip: the tail state (written by the decision before its tasks
-    // were published) and every slice partial, into shared memory.
-    const int4* tw = reinterpret_cast<const int4*>(a.tails + i);
-    int4 tv = make_int4(0, 0, 0, 0);
-    if (lane < 3) tv = __ldcg(tw + lane);
-    const int U = a.nt * kCW;  // even: 16-byte pairs of partials
-    const float4* tp = reinterpret_cast<const float4*>(a.tpart + static_cast<size_t>(i) * U);
-    float4* ts = reinterpret_cast<float4*>(sm.tsel[fi]);
-    for (int u = lane; u < U / 2; u += 32) cp_async16(ts + u, tp + u);
-    cp_async_wait_all();
-    SeqTail t;
-    const int mode_flags = __shfl_sync(0xffffffffu, tv.x, 0);
-    t.mode = mode_flags & ~kTailQnew;
-    t.a = __shfl_sync(0xffffffffu, tv.y, 0);
-    t.prow = __shfl_sync(0xffffffffu, tv.z, 0);
-    t.qrow = __shfl_sync(0xffffffffu, tv.w, 0);
-    t.c2 = __int_as_float(__shfl_sync(0xffffffffu, tv.x, 1));
-    t.nz0 = __int_as_float(__shfl_sync(0xffffffffu, tv.y, 1));
-    t.nz1 = __int_as_float(__shfl_sync(0xffffffffu, tv.z, 1));
-    t.seq = __shfl_sync(0xffffffffu, tv.w, 1);
-    t.pos = __shfl_sync(0xffffffffu, tv.x, 2);
-    t.tag = __shfl_sync(0xffffffffu, tv.y, 2);
-    t.dest = __shfl_sync(0xffffffffu, tv.z, 2);
-    __syncwarp();
-    // The draw is written to its slot; the sequence is final with its last draw.
-    auto finish = [&](int token) {
-        if (lane == 0) {
-            if (t.dest >= 0)
-                a.out_tokens[t.dest] = token;
-            else
-                a.proposals[-1 - t.dest] = token;
-            a.tail_count[i] = 0;
-            if (atomicSub(a.seq_pending + t.seq, 1) == 1) finalize(a);
-        }
-    };
-    if (t.mode == kTailArg) {  // greedy proposal: merge the slice argmaxes
-        float M = -INFINITY;
-        int I = INT_MAX;
-        for (int u = lane; u < U; u += 32) merge_argmax(M, I, sm.tsel[fi][u].x, __float_as_int(sm.tsel[fi][u].y));
-        warp_merge_arg(M, I);
-        finish(I);
-        return;
-    }
-    // Slice weights in one scale, the target u * total, and its slice.  Lane
-    // l owns the consecutive slices [l * ub, (l + 1) * ub): the lanes reduce
-    // their blocks locally and meet in one scan, so the pass costs a handful
-    // of shuffles instead of a few per 32 slices.
-    const int ub = (U + 31) / 32;
-    const int u_lo = min(U, lane * ub), u_hi = min(U, u_lo + ub);
-    float MC = -INFINITY, W = 0.0f;
-    for (int u = u_lo; u < u_hi; ++u) {
-        const float x = sm.tsel[fi][u].x;
-        MC = fmaxf(MC, x);
-        W += x;
-    }
-    bool fallback = false;
-    if (t.mode == kTailSoft) MC = warp_max(MC);
-    else fallback = !(warp_sum(W) > 0.0f);  // residual rounded to zero: draw from p_j
-    auto slice_w = [&](int u) -> float {
-        const float2 v = sm.tsel[fi][u];
-        if (t.mode == kTailSoft) return v.x == -INFINITY ? 0.0f : v.y * ex2_approx(v.x - MC);
-        return fallback ? v.y : v.x;
-    };
-    const float rnd = decision_uniform(a.seed, a.offset, t.seq, t.pos, t.tag);
-    float own = 0.0f;
-    int lpos = -1;  // the lane's last slice with positive weight
-    for (int u = u_lo; u < u_hi; ++u) {
-        const float w = slice_w(u);
-        own += w;
-        if (w > 0.0f) lpos = u;
-    }
-    float incl = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    const float target = rnd * __shfl_sync(0xffffffffu, incl, 31);
-    const unsigned hit = __ballot_sync(0xffffffffu, u_hi > u_lo && incl > target);
-    int chosen = -1;
-    float tloc = INFINITY;
-    if (hit) {
-        const int owner = __ffs(hit) - 1;
-        if (lane == owner) {  // in-order scan of the owner's block
-            float cum = incl - own;
-            for (int u = u_lo; u < u_hi; ++u) {
-                const float w = slice_w(u);
-                if (cum + w > target) {
-                    chosen = u;
-                    tloc = target - cum;
-                    break;
-                }
-                cum += w;
-            }
-            if (chosen < 0) chosen = lpos;  // rounding inside the block: its last positive slice
-        }
-        chosen = __shfl_sync(0xffffffffu, chosen, owner);
-        tloc = __shfl_sync(0xffffffffu, tloc, owner);
-    }
-    if (chosen < 0) {  // rounding left the target past the last weight
-        const int last_pos = warp_max_int(lpos);
-        chosen = last_pos >= 0 ? last_pos : 0;
-        tloc = INFINITY;
-    }
-    // The chosen slice: ids [lo, lo + len) of the tail row(s).
-    const int c = chosen / kCW, w = chosen % kCW;
-    const int nc = min(a.ckt, a.vocab - c * a.ckt);
-    int sb, se;
-    tail_slice<E>(nc, w, sb, se);
-    const int lo = c * a.ckt + sb;
-    const int len = se - sb;
-    const char* prow = (mode_flags & kTailQnew) ? a.qnew + static_cast<int64_t>(t.prow) * a.ldqnew_bytes
-                                                : a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
-    const char* qrow = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes;
-    constexpr int kVec = 16 / E;
-    constexpr int kPer = 2 * kVec;  // ids per lane: at most two 16-byte vectors
-    static_assert(kPer * 32 * E == kSliceMax * 2, "a slice fills at most two vectors per lane");
-    const int q = ((len + 31) / 32 + kVec - 1) / kVec * kVec;  // whole vectors per lane
-    const int b = lane * q;
-    const int cnt = max(0, min(q, len - b));
-    // Stage the slice's logits in shared memory with every load in flight at
-    // once: 16-byte copies where both rows allow them, then the elements
-    // left (all of them for rows that are not 16-byte aligned).
-    const bool res = t.mode != kTailSoft;
-    unsigned char* sp = sm.sslice[fi][0];
-    unsigned char* sq = sm.sslice[fi][1];
-    const char* gp = prow + static_cast<size_t>(lo) * E;
-    const char* gq = qrow + static_cast<size_t>(lo) * E;
-    const bool v16 = (reinterpret_cast<uintptr_t>(gp) & 15u) == 0 && (!res || (reinterpret_cast<uintptr_t>(gq) & 15u) == 0);
-    const int nv16 = v16 ? (len * E) >> 4 : 0;
-    for (int v = lane; v < nv16; v += 32) {
-        cp_async16(sp + 16 * v, gp + 16 * v);
-        if (res) cp_async16(sq + 16 * v, gq + 16 * v);
-    }
-    using Raw = typename std::conditional<E == 2, uint16_t, uint32_t>::type;
-    for (int e0 = nv16 * (16 / E); e0 < len; e0 += 4 * 32) {
-        Raw rp[4], rq[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + lane + 32 * j;
-            rp[j] = e < len ? reinterpret_cast<const Raw*>(gp)[e] : Raw(0);
-            rq[j] = (res && e < len) ? reinterpret_cast<const Raw*>(gq)[e] : Raw(0);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + lane + 32 * j;
-            if (e < len) {
-                reinterpret_cast<Raw*>(sp)[e] = rp[j];
-                if (res) reinterpret_cast<Raw*>(sq)[e] = rq[j];
-            }
-        }
-    }
-    cp_async_wait_all();
-    __syncwarp();
-    const uint4* sp4 = reinterpret_cast<const uint4*>(sp) + b / kVec;
-    const uint4* sq4 = reinterpret_cast<const uint4*>(sq) + b / kVec;
-    uint4 P[2], Q[2];
-#pragma unroll
-    for (int v = 0; v < 2; ++v) {
-        P[v] = v * kVec < cnt ? sp4[v] : make_uint4(0, 0, 0, 0);
-        Q[v] = (res && v * kVec < cnt) ? sq4[v] : make_uint4(0, 0, 0, 0);
-    }
-    float wv[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        wv[k] = 0.0f;
-        if (k < cnt) {
-            const float xp = vec_elem<E>(P[k / kVec], k % kVec);
-            if (!res) {
-                wv[k] = soft_w(xp, t.c2, MC);
-            } else {
-                float pv;
-                const float rw = resid_w(xp, vec_elem<E>(Q[k / kVec], k % kVec), t.c2, t.nz0, t.nz1, pv);
-                wv[k] = fallback ? pv : rw;
-            }
-        }
-    }
-    float own2 = 0.0f;
-    int lp = -1;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        own2 += wv[k];
-        if (wv[k] > 0.0f) lp = b + k;
-    }
-    float incl2 = own2;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl2, o);
-        if (lane >= o) incl2 += y;
-    }
-    const unsigned hit2 = __ballot_sync(0xffffffffu, cnt > 0 && incl2 > tloc);
-    int found = -1;
-    if (hit2) {
-        const int owner = __ffs(hit2) - 1;
-        if (lane == owner) {
-            float cum = incl2 - own2;
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                cum += wv[k];
-                if (found < 0 && k < cnt && cum > tloc) found = b + k;
-            }
-            if (found < 0) found = lp;  // rounding inside this lane's ids
-        }
-        found = __shfl_sync(0xffffffffu, found, owner);
-    }
-    const int last = warp_max_int(lp);
-    finish(lo + (found >= 0 ? found : (last >= 0 ? last : 0)));
-}
-
-// Hand a decision or selection to the finisher warp (lane 0 of the bookkeeper).
-__device__ __forceinline__ void push_job(const VerifyArgs& a, SmemV& sm, long long& nj, int kind, int seq) {
-    const int js = static_cast<int>(nj % kJobs);
-    const uint32_t parity = (static_cast<uint32_t>(nj / kJobs) & 1u) ^ 1u;
-    ++nj;
-    if (!mbar_wait_ns(&sm.job_empty[js], parity, kDrainWaitNs)) atomicOr(&a.ctl->err, kErrWaitTimeout);
-    sm.job[js].kind = kind;
-    sm.job[js].seq = seq;
-    mbar_arrive(&sm.job_full[js]);
-}
+// =============================================================================
+// Bookkeeper warp
+// =============================================================================
 
 // Warp reductions within aligned groups of 8 lanes.
 __device__ __forceinline__ void group8_merge_mc(float& M, float& S) {
@@ -703,7 +483,6 @@ __device__ __forceinline__ void group8_merge_arg(float& M, int& I) {
 // group g (8 lanes, one per consumer warp) handles record r + g, so the
 // device-scope counts of a batch overlap in one round trip.
 __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
-    long long nj = 0;
     const int g = lane >> 3, wl = lane & 7;
     for (long long r = 0;;) {
         // Consumers may idle until other CTAs finish, hence the long bound.
@@ -719,7 +498,7 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
             ++nb;
         const bool mine = g < nb;
         const Rec& rc = sm.rec[(r + (mine ? g : 0)) % kRecs];
-        const int kind = rc.kind, flags = rc.flags, seq = rc.seq, rslot = rc.slot, seg = rc.seg, expect = rc.expect;
+        const int kind = rc.kind, seq = rc.seq, rslot = rc.slot, chunk = rc.chunk, expect = rc.expect, arg = rc.arg;
         const float2 v = rc.wp[wl];
         __syncwarp();
         if (lane < nb) mbar_arrive(&sm.rec_empty[(r + lane) % kRecs]);
@@ -727,7 +506,6 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
         const unsigned end_mask = __ballot_sync(0xffffffffu, mine && wl == 0 && kind == kEnd);
         const int n_real = end_mask ? (__ffs(end_mask) - 1) / 8 : nb;
         const bool act = g < n_real;
-        int trig = 0;  // 1: decide this sequence, 2: select its token
         // Both merges run on every lane (shuffles need the whole warp); each
         // group keeps the one its record asks for.
         float Mm = v.x, Sm = v.y;
@@ -735,246 +513,23 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
         float Ma = v.x;
         int Ia = __float_as_int(v.y);
         group8_merge_arg(Ma, Ia);
-        // A tail record's eight slice partials, gathered to the group leader so
-        // that its releasing count publishes them.
-        float2 sl[kCW];
-#pragma unroll
-        for (int k = 0; k < kCW; ++k) {
-            sl[k].x = __shfl_sync(0xffffffffu, v.x, (lane & ~7) + k);
-            sl[k].y = __shfl_sync(0xffffffffu, v.y, (lane & ~7) + k);
-        }
         if (act && wl == 0) {
-            if (kind == kMain) {
-                a.part[static_cast<size_t>(rslot) * a.nseg + seg] =
-                    flags == kRecArg ? make_float2(Ma, __int_as_float(Ia)) : make_float2(Mm, Sm);
-                if (atomic_add_acq_rel(a.seq_count + seq, 1) == expect - 1) trig = 1;
-            } else {
-                float4* dst = reinterpret_cast<float4*>(a.tpart + (static_cast<size_t>(seq) * a.nt + rslot) * kCW);
-#pragma unroll
-                for (int k = 0; k < kCW / 2; ++k) dst[k] = make_float4(sl[2 * k].x, sl[2 * k].y, sl[2 * k + 1].x, sl[2 * k + 1].y);
-                if ((flags & kLast) && atomic_add_acq_rel(a.tail_count + seq, 1) == a.ntask - 1) trig = 2;
-            }
-        }
-        // Hand the triggered jobs to the finishers, in record order.
-        const unsigned tmask = __ballot_sync(0xffffffffu, trig != 0);
-        for (unsigned m = tmask; m; m &= m - 1) {
-            const int src = __ffs(m) - 1;
-            const int tk = __shfl_sync(0xffffffffu, trig, src), ts = __shfl_sync(0xffffffffu, seq, src);
-            if (lane == 0) push_job(a, sm, nj, tk == 1 ? kJobDecide : kJobSelect, ts);
+            a.part[static_cast<size_t>(rslot) * a.nck + chunk] = arg ? make_float2(Ma, __int_as_float(Ia))
+                                                                     : make_float2(Mm, Sm);
+            // The count that completes a sequence acquires every partial of
+            // it; the release of its ready word passes them on to whichever
+            // worker holds the sequence's decision ticket.
+            if (atomic_add_acq_rel(a.seq_count + seq, 1) == expect - 1)
+                st_release_u64(a.dready + seq, flagged(static_cast<uint32_t>(seq) + 1u, 0));
         }
         __syncwarp();
         r += nb;
         if (end_mask) break;
     }
-    if (lane == 0)
-        for (int f = 0; f < kFinishers; ++f) push_job(a, sm, nj, kJobEnd, 0);
-}
-
-template <typename Elem>
-__device__ void finisher(const VerifyArgs& a, SmemV& sm, int fi, int lane) {
-    for (;;) {
-        // Jobs are claimed in order by whichever finisher is free.
-        int j = 0;
-        if (lane == 0) j = atomicAdd(&sm.job_take, 1);
-        j = __shfl_sync(0xffffffffu, j, 0);
-        const int js = j % kJobs;
-        const uint32_t parity = static_cast<uint32_t>(j / kJobs) & 1u;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&sm.job_full[js], parity, kDrainWaitNs + 2 * kWaitNs));
-        if (!ok) {
-            if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
-            return;
-        }
-        const int kind = sm.job[js].kind, seq = sm.job[js].seq;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.job_empty[js]);
-        if (kind == kJobEnd) return;
-        if (kind == kJobDecide)
-            decide_warp<Elem>(a, sm, seq, lane);
-        else
-            select_warp<Elem>(a, sm, fi, seq, lane);
-    }
 }
 
 // =============================================================================
-// Scheduler thread: decides what to stream next, absorbing every global
-// memory round trip (work counter, ticket flags, task records, sequence
-// lookups) so that the issuer never waits on one.
-// =============================================================================
-
-struct SeqCache {
-    int i, start, end, len;
-    float T;
-    bool ok;
-};
-
-// Main item w as work for the issuer; false if the item reads nothing.
-__device__ bool main_work(const VerifyArgs& a, const SmemV& sm, long long w, SeqCache& sc, Work& wk) {
-    const int slot = static_cast<int>(w / a.nseg);
-    const int seg = static_cast<int>(w - static_cast<long long>(slot) * a.nseg);
-    const int r = slot >> 1, kind = slot & 1;
-    if (!(r >= sc.start && r < sc.end)) {
-        const bool small = a.num_seqs <= kSmemSeqs;
-        const int* offs = small ? sm.offs : a.seq_offsets;
-        const int i = seq_of_position_t(offs, a.num_seqs, r);
-        const SeqInfo s = seq_lookup(a, sm, i);
-        sc.i = i;
-        sc.start = s.start;
-        sc.len = s.len;
-        sc.end = s.in_range ? s.start + max(s.len, 0) : s.start;
-        sc.T = s.T;
-        sc.ok = s.ok;
-        if (!(r >= sc.start && r < sc.end)) {
-            sc.start = sc.end = 0;
-            return false;  // position outside every sequence
-        }
-    }
-    if (!sc.ok) return false;
-    // Greedy verification reads no q rows; the last position's q slot streams
-    // the final anchor row p_{L+1} instead, whose argmax is the bonus token.
-    const bool greedy = !(sc.T > 0.0f);
-    const bool bonus = greedy && kind == 1;
-    if (bonus && r != sc.start + sc.len - 1) return false;
-    wk.kind = kMain;
-    wk.seq = sc.i;
-    wk.slot = slot;
-    wk.seg = seg;
-    wk.expect = (greedy ? sc.len + 1 : 2 * sc.len) * a.nseg;
-    // A rejection is likeliest at the first position: its rows stay in L2
-    // for the residual tail when the batch can afford it.
-    wk.keep = a.keep_first && !greedy && r == sc.start;
-    wk.c0 = seg * a.spseg;
-    wk.c1 = min(wk.c0 + a.spseg, a.nck);
-    wk.c2 = sc.T > 0.0f ? inv_temp_log2e(sc.T) : 0.0f;
-    wk.row0 = bonus  ? a.p + static_cast<int64_t>(r + sc.i + 1) * a.ldp_bytes
-              : kind ? a.q + static_cast<int64_t>(r) * a.ldq_bytes
-                     : a.p + static_cast<int64_t>(r + sc.i) * a.ldp_bytes;
-    wk.row1 = nullptr;
-    return true;
-}
-
-// Tail task of a published queue slot as work for the issuer.
-__device__ void tail_work(const VerifyArgs& a, int slot, Work& wk) {
-    st_volatile(a.task_ready + slot, 0);
-    const int4 w0 = __ldcg(a.tasks + 2 * static_cast<size_t>(slot)), w1 = __ldcg(a.tasks + 2 * static_cast<size_t>(slot) + 1);
-    const int i = w0.x, y = w0.y;
-    wk.kind = w0.z & ~kTailQnew;
-    wk.seq = i;
-    wk.slot = 0;
-    wk.seg = 0;
-    wk.expect = 0;
-    wk.keep = 0;
-    wk.c0 = y * a.tpt;
-    wk.c1 = min(wk.c0 + a.tpt, a.nt);
-    wk.c2 = __int_as_float(w1.y);
-    wk.nz0 = __int_as_float(w1.z);
-    wk.nz1 = __int_as_float(w1.w);
-    wk.row0 = (w0.z & kTailQnew) ? a.qnew + static_cast<int64_t>(w0.w) * a.ldqnew_bytes
-                                 : a.p + static_cast<int64_t>(w0.w) * a.ldp_bytes;
-    wk.row1 = a.q + static_cast<int64_t>(w1.x) * a.ldq_bytes;
-}
-
-__device__ void scheduler(const VerifyArgs& a, SmemV& sm, unsigned long long next) {
-    bool main_done = sm.batch_bad != 0 || a.n_main == 0;
-    SeqCache sc = {0, 0, 0, 0, 0.0f, false};
-    // Tail tasks are handed out as tickets: every scheduler holds at most one
-    // ticket (a task-queue slot, one atomic to take it) and passes that slot's
-    // task to the issuer through a priority slot as soon as a decision
-    // publishes it, ahead of the main items already queued.  Every global
-    // round trip is issued one pass before its result is looked at.
-    const int cap = a.n_tail * a.ntask;
-    bool tickets_left = cap > 0;
-    int ticket = -1, claim = 0, flag = 0;
-    bool claim_pending = false, claim_started = false;
-    long long k = 0, kp = 0;  // work items and priority items handed over
-    uint64_t t_idle = 0;
-    while (true) {
-        bool progress = false;
-        // 1. A published tail task goes to the priority slot.
-        if (claim_pending && ticket < 0) {
-            claim_pending = false;
-            if (claim < cap) {
-                ticket = claim;
-                flag = 0;
-            } else {
-                tickets_left = false;
-            }
-        }
-        if (ticket >= 0 && flag != 0 && mbar_test(&sm.prio_empty, (static_cast<uint32_t>(kp) & 1u) ^ 1u)) {
-            __threadfence();  // acquire: the task was published before its flag
-            tail_work(a, ticket, sm.prio);
-            mbar_arrive(&sm.prio_full);
-            ++kp;
-            ticket = -1;
-            flag = 0;
-            if (tickets_left) {
-                claim = atomicAdd(&a.ctl->tail_claim, 1);
-                claim_pending = true;
-            }
-            progress = true;
-        }
-        // 2. The next main item, while the work ring has room.
-        if (!main_done) {
-            const int ws = static_cast<int>(k % kWork);
-            if (mbar_test(&sm.work_empty[ws], (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u)) {
-                Work& wk = sm.work[ws];
-                bool have = false;
-                while (!have && !main_done) {
-                    const unsigned long long w = next;
-                    if (w < static_cast<unsigned long long>(a.n_main)) {
-                        next = atomicAdd(&a.ctl->grab, 1ull);
-                        have = main_work(a, sm, static_cast<long long>(w), sc, wk);
-                    } else {
-                        main_done = true;
-                    }
-                }
-                if (have) {
-                    mbar_arrive(&sm.work_full[ws]);
-                    ++k;
-                    progress = true;
-                }
-                // The first ticket is claimed once the first main item is on its way.
-                if (!claim_started && tickets_left) {
-                    claim_started = true;
-                    claim = atomicAdd(&a.ctl->tail_claim, 1);
-                    claim_pending = true;
-                }
-            }
-        }
-        // 3. Refresh the held ticket's flag (looked at on the next pass).
-        if (ticket >= 0) flag = ld_volatile(a.task_ready + ticket);
-        if (!claim_started && main_done && tickets_left) {
-            claim_started = true;
-            claim = atomicAdd(&a.ctl->tail_claim, 1);
-            claim_pending = true;
-        }
-        if (progress) {
-            t_idle = 0;
-            continue;
-        }
-        if (main_done && ld_volatile(&a.ctl->finalized) >= sm.n_valid) break;  // every sequence is final
-        if (t_idle == 0) {
-            t_idle = global_timer_ns();
-        } else if (global_timer_ns() - t_idle > kDrainWaitNs) {
-            atomicOr(&a.ctl->err, kErrWaitTimeout);
-            break;
-        }
-        if (!main_done)  // work ring full: sleep until a slot frees (or ~1 us, to look at the ticket)
-            (void)mbar_try_wait_for(&sm.work_empty[k % kWork], (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u, 1000);
-        else
-            __nanosleep(200);
-    }
-    // Stop the issuer: an end marker in the work ring (bounded wait for room).
-    const int ws = static_cast<int>(k % kWork);
-    if (!mbar_wait_ns(&sm.work_empty[ws], (static_cast<uint32_t>(k / kWork) & 1u) ^ 1u, kWaitNs)) {
-        atomicOr(&a.ctl->err, kErrWaitTimeout);
-        return;
-    }
-    sm.work[ws].kind = kEnd;
-    mbar_arrive(&sm.work_full[ws]);
-}
-
-// =============================================================================
-// Issuer thread: streams the scheduled work's sub-chunks into the stage ring.
+// Producer thread: streams this CTA's units into the stage ring
 // =============================================================================
 
 __device__ __forceinline__ int acquire_stage(SmemV& sm, long long n, int* err) {
@@ -987,94 +542,75 @@ __device__ __forceinline__ int acquire_stage(SmemV& sm, long long n, int* err) {
     return stage;
 }
 
-// Stream sub-chunks [c0, c1) of one unit of work into the stage ring.
 template <typename Elem>
-__device__ bool issue_work(const VerifyArgs& a, SmemV& sm, const Work& wk, int c0, int c1, long long& n,
-                           uint64_t pol_first, uint64_t pol_last) {
+__device__ void producer(const VerifyArgs& a, SmemV& sm) {
     constexpr int E = sizeof(Elem);
-    const bool main = wk.kind == kMain;
-    const int ck = main ? a.ck : a.ckt;
-    for (int c = c0; c < c1; ++c) {
-        const int e0 = c * ck;
-        const int nel = min(ck, a.vocab - e0);
-        const Piece pa = make_piece<E>(wk.row0, e0, nel);
-        Piece pb = {};
-        if (wk.kind == kTailRes) pb = make_piece<E>(wk.row1, e0, nel);
-        const int stage = acquire_stage(sm, n, &a.ctl->err);
-        if (stage < 0) return false;
-        Desc& d = sm.desc[stage];
-        d.kind = wk.kind;
-        d.flags = main ? ((c == wk.c0 ? kFirst : 0) | (c == wk.c1 - 1 ? kLast : 0)) : (c == wk.c1 - 1 ? kLast : 0);
-        d.seq = wk.seq;
-        d.slot = main ? wk.slot : c;
-        d.seg = wk.seg;
-        d.expect = wk.expect;
-        d.e0 = e0;
-        d.n = nel;
-        d.nvec = pa.bytes >> 4;
-        d.nsm0 = pa.nsm;
-        d.skip0 = pa.skip;
-        d.tail0 = pa.tail;
-        d.nsm1 = pb.nsm;
-        d.skip1 = pb.skip;
-        d.tail1 = pb.tail;
-        d.c2 = wk.c2;
-        d.nz0 = wk.nz0;
-        d.nz1 = wk.nz1;
-        const int bytes = pa.bytes + pb.bytes;
-        if (bytes > 0) {
-            mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(bytes));
-            const uint64_t pol = wk.keep ? pol_last : pol_first;
-            if (pa.bytes > 0)
-                bulk_copy_g2s_hint(sm.stage[stage], reinterpret_cast<const void*>(pa.lo),
-                                   static_cast<uint32_t>(pa.bytes), &sm.full[stage], pol);
-            if (pb.bytes > 0)
-                bulk_copy_g2s_hint(sm.stage[stage] + kHalf, reinterpret_cast<const void*>(pb.lo),
-                                   static_cast<uint32_t>(pb.bytes), &sm.full[stage], pol);
-        } else {
-            mbar_arrive(&sm.full[stage]);
-        }
-        ++n;
-    }
-    return true;
-}
-
-template <typename Elem>
-__device__ void issuer(const VerifyArgs& a, SmemV& sm) {
-    long long n = 0, kp = 0;
+    const long long G = gridDim.x;
+    long long n = 0;  // stages issued
     bool ok = true;
-    const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
-    // Tail work waiting in the priority slot goes first, between any two
-    // stages; returns -1 on a timeout, 1 if it issued work, 0 otherwise.
-    auto priority = [&]() -> int {
-        if (!mbar_test(&sm.prio_full, static_cast<uint32_t>(kp) & 1u)) return 0;
-        const Work pw = sm.prio;
-        mbar_arrive(&sm.prio_empty);
-        ++kp;
-        return issue_work<Elem>(a, sm, pw, pw.c0, pw.c1, n, pol_first, pol_last) ? 1 : -1;
-    };
-    for (long long k = 0; ok; ++k) {
-        const int ws = static_cast<int>(k % kWork);
-        const uint32_t parity = static_cast<uint32_t>(k / kWork) & 1u;
-        // Wait for the next main item, serving the priority slot meanwhile.
-        const uint64_t t0 = global_timer_ns();
-        bool got = false;
-        while (ok && !(got = mbar_test(&sm.work_full[ws], parity))) {
-            const int pr = priority();
-            ok = pr >= 0;
-            if (global_timer_ns() - t0 > kDrainWaitNs + kWaitNs) {
-                atomicOr(&a.ctl->err, kErrWaitTimeout);
-                ok = false;
+    if (!sm.batch_bad) {
+        // Units in sequence order: sequence i owns [base, base + units);
+        // within it, row index ri in [0, rows_of), chunk c in [0, nck).
+        int i = -1;
+        long long base = 0, units = 0;
+        SeqInfo s{};
+        float c2 = 0.0f;
+        for (long long U = blockIdx.x; ok; U += G) {
+            bool more = true;
+            while (U >= base + units) {
+                base += units;
+                if (++i >= a.num_seqs) {
+                    more = false;
+                    break;
+                }
+                s = seq_lookup(a, sm, i);
+                units = s.ok ? static_cast<long long>(rows_of(s)) * a.nck : 0;
+                c2 = s.T > 0.0f ? inv_temp_log2e(s.T) : 0.0f;
             }
-            if (pr == 0) __nanosleep(200);
-        }
-        if (!got) break;
-        const Work wk = sm.work[ws];
-        mbar_arrive(&sm.work_empty[ws]);
-        if (wk.kind == kEnd) break;
-        for (int c = wk.c0; c < wk.c1 && ok; ++c) {
-            ok = priority() >= 0;
-            if (ok) ok = issue_work<Elem>(a, sm, wk, c, c + 1, n, pol_first, pol_last);
+            if (!more) break;
+            const int u = static_cast<int>(U - base);
+            const int ri = u / a.nck, c = u - ri * a.nck;
+            const char* row;
+            int slot;
+            if (s.T > 0.0f) {  // p_k, q_k interleaved: ri = 2 (k - 1) + {0, 1}
+                const int k = (ri >> 1) + 1, kind = ri & 1;
+                slot = 2 * (s.start + k - 1) + kind;
+                row = kind ? a.q + static_cast<int64_t>(s.start + k - 1) * a.ldq_bytes
+                           : a.p + static_cast<int64_t>(s.start + i + k - 1) * a.ldp_bytes;
+            } else {  // p_1 .. p_{L+1}; the final anchor uses the last position's q slot
+                const int k = ri + 1;
+                slot = k <= s.len ? 2 * (s.start + k - 1) : 2 * (s.start + s.len - 1) + 1;
+                row = a.p + static_cast<int64_t>(s.start + i + k - 1) * a.ldp_bytes;
+            }
+            const int e0 = c * a.ck;
+            const int nel = min(a.ck, a.vocab - e0);
+            const Piece pc = make_piece<E>(row, e0, nel);
+            const int stage = acquire_stage(sm, n, &a.ctl->err);
+            if (stage < 0) {
+                ok = false;
+                break;
+            }
+            Desc& d = sm.desc[stage];
+            d.kind = kUnit;
+            d.seq = i;
+            d.slot = slot;
+            d.chunk = c;
+            d.expect = static_cast<int>(units);
+            d.e0 = e0;
+            d.n = nel;
+            d.nvec = pc.bytes >> 4;
+            d.nsm = pc.nsm;
+            d.skip = pc.skip;
+            d.tail = pc.tail;
+            d.c2 = c2;
+            if (pc.bytes > 0) {
+                mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(pc.bytes));
+                bulk_copy_g2s(sm.stage[stage], reinterpret_cast<const void*>(pc.lo), static_cast<uint32_t>(pc.bytes),
+                              &sm.full[stage]);
+            } else {
+                mbar_arrive(&sm.full[stage]);
+            }
+            ++n;
         }
     }
     const int stage = acquire_stage(sm, n, &a.ctl->err);
@@ -1088,16 +624,10 @@ __device__ void issuer(const VerifyArgs& a, SmemV& sm) {
 // Consumer warps
 // =============================================================================
 
-struct MainState {
-    float m, mc;
-    uint64_t acc0, acc1;
-    int amx;
-};
-
-// Hand this warp's partial for the current record to the bookkeeper.
+// Hand this warp's partial of a unit to the bookkeeper.
 __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemV& sm, long long& nrec, int warp, int lane,
-                                            float2 part, int kind, int flags, int seq, int slot, int seg,
-                                            int expect) {
+                                            float2 part, int kind, int seq, int slot, int chunk, int expect,
+                                            int arg) {
     const int rs = static_cast<int>(nrec % kRecs);
     const uint32_t parity = (static_cast<uint32_t>(nrec / kRecs) & 1u) ^ 1u;
     ++nrec;
@@ -1107,11 +637,11 @@ __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemV& sm, long
         rc.wp[warp] = part;
         if (warp == 0) {
             rc.kind = kind;
-            rc.flags = flags;
             rc.seq = seq;
             rc.slot = slot;
-            rc.seg = seg;
+            rc.chunk = chunk;
             rc.expect = expect;
+            rc.arg = arg;
         }
         mbar_arrive(&sm.rec_full[rs]);
     }
@@ -1119,8 +649,8 @@ __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemV& sm, long
 }
 
 template <typename Elem>
-__device__ __forceinline__ void main_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int tid,
-                                           int warp, int lane, MainState& ms, long long& nrec) {
+__device__ __forceinline__ void unit_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int tid,
+                                           int warp, int lane, long long& nrec) {
     constexpr bool kBf16 = sizeof(Elem) == 2;
     constexpr uint32_t kNeg = kBf16 ? 0xff80ff80u : 0xff800000u;  // -inf pattern
     uint32_t w[kVecPT * 4];
@@ -1134,30 +664,23 @@ __device__ __forceinline__ void main_stage(const VerifyArgs& a, SmemV& sm, int s
         w[4 * k + 2] = v.z;
         w[4 * k + 3] = v.w;
     }
-    if (d.skip0 != 0 && tid == 0) {  // elements before the sub-chunk in the first vector
+    if (d.skip != 0 && tid == 0) {  // elements before the chunk in the first vector
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if constexpr (kBf16) {
-                if (2 * j < d.skip0) w[j] = (w[j] & 0xffff0000u) | 0xff80u;
-                if (2 * j + 1 < d.skip0) w[j] = (w[j] & 0x0000ffffu) | 0xff800000u;
+                if (2 * j < d.skip) w[j] = (w[j] & 0xffff0000u) | 0xff80u;
+                if (2 * j + 1 < d.skip) w[j] = (w[j] & 0x0000ffffu) | 0xff800000u;
             } else {
-                if (j < d.skip0) w[j] = kNeg;
+                if (j < d.skip) w[j] = kNeg;
             }
         }
     }
-    const int ntail = d.n - d.nsm0;
+    const int ntail = d.n - d.nsm;
     float tv = -INFINITY;
-    if (tid < ntail) tv = load_elem<Elem>(d.tail0 + static_cast<size_t>(tid) * sizeof(Elem));
+    if (tid < ntail) tv = load_elem<Elem>(d.tail + static_cast<size_t>(tid) * sizeof(Elem));
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);
 
-    if (d.flags & kFirst) {
-        ms.m = -INFINITY;
-        ms.mc = -INFINITY;
-        ms.acc0 = 0;
-        ms.acc1 = 0;
-        ms.amx = INT_MAX;
-    }
     float cm;
     if constexpr (kBf16) {
         uint32_t mx = w[0];
@@ -1171,261 +694,708 @@ __device__ __forceinline__ void main_stage(const VerifyArgs& a, SmemV& sm, int s
     }
     cm = fmaxf(cm, tv);
     const float c2 = d.c2;
+    float2 part;
     if (c2 > 0.0f) {
-        if (cm > ms.m) {
-            const float mcn = cm * c2;
-            if (ms.m != -INFINITY) {
-                const float sc = ex2_approx(ms.mc - mcn);
-                const uint64_t sc2 = pack_f2(sc, sc);
-                ms.acc0 = mul_f2(ms.acc0, sc2);
-                ms.acc1 = mul_f2(ms.acc1, sc2);
-            }
-            ms.m = cm;
-            ms.mc = mcn;
-        }
-        if (ms.m != -INFINITY) {
-            const uint64_t C2 = pack_f2(c2, c2), NMC = pack_f2(-ms.mc, -ms.mc);
+        float M = -INFINITY, S = 0.0f;
+        if (cm != -INFINITY) {
+            const float mc = cm * c2;
+            const uint64_t C2 = pack_f2(c2, c2), NMC = pack_f2(-mc, -mc);
+            uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
             for (int j = 0; j < kVecPT * 4; j += 2) {
                 if constexpr (kBf16) {
                     float y0, y1, y2, y3;
                     unpack_f2(fma_f2(pack_f2(bf16lo(w[j]), bf16hi(w[j])), C2, NMC), y0, y1);
                     unpack_f2(fma_f2(pack_f2(bf16lo(w[j + 1]), bf16hi(w[j + 1])), C2, NMC), y2, y3);
-                    ms.acc0 = add_f2(ms.acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
-                    ms.acc1 = add_f2(ms.acc1, pack_f2(ex2_approx(y2), ex2_approx(y3)));
+                    acc0 = add_f2(acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+                    acc1 = add_f2(acc1, pack_f2(ex2_approx(y2), ex2_approx(y3)));
                 } else {
                     float y0, y1;
                     unpack_f2(fma_f2(pack_f2(__uint_as_float(w[j]), __uint_as_float(w[j + 1])), C2, NMC), y0, y1);
                     if (j & 2)
-                        ms.acc1 = add_f2(ms.acc1, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+                        acc1 = add_f2(acc1, pack_f2(ex2_approx(y0), ex2_approx(y1)));
                     else
-                        ms.acc0 = add_f2(ms.acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
+                        acc0 = add_f2(acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
                 }
             }
-            if (tv != -INFINITY) ms.acc1 = add_f2(ms.acc1, pack_f2(soft_w(tv, c2, ms.mc), 0.0f));
-        }
-    } else if (cm > ms.m) {
-        // First position of the new maximum in this thread's (ascending) elements.
-        constexpr int kPer = kBf16 ? 8 : 4;
-        int idx = INT_MAX;
-        if (tv == cm) idx = d.nsm0 + tid;
-#pragma unroll
-        for (int k = kVecPT - 1; k >= 0; --k) {
-#pragma unroll
-            for (int j = 3; j >= 0; --j) {
-                const uint32_t x = w[4 * k + j];
-                const int base = (tid + k * kCT) * kPer - d.skip0;
-                if constexpr (kBf16) {
-                    if (bf16hi(x) == cm) idx = base + 2 * j + 1;
-                    if (bf16lo(x) == cm) idx = base + 2 * j;
-                } else {
-                    if (__uint_as_float(x) == cm) idx = base + j;
-                }
-            }
-        }
-        ms.m = cm;
-        ms.amx = d.e0 + idx;
-    }
-
-    if (d.flags & kLast) {
-        float2 part;
-        int mode;
-        if (c2 > 0.0f) {
+            if (tv != -INFINITY) acc1 = add_f2(acc1, pack_f2(soft_w(tv, c2, mc), 0.0f));
             float s0, s1, s2, s3;
-            unpack_f2(ms.acc0, s0, s1);
-            unpack_f2(ms.acc1, s2, s3);
-            float M = ms.m == -INFINITY ? -INFINITY : ms.mc, S = (s0 + s1) + (s2 + s3);
-            warp_merge_mc(M, S);
-            part = make_float2(M, S);
-            mode = kRecSoft;
-        } else {
-            float M = ms.m;
-            int I = ms.amx;
-            warp_merge_arg(M, I);
-            part = make_float2(M, __int_as_float(I));
-            mode = kRecArg;
+            unpack_f2(acc0, s0, s1);
+            unpack_f2(acc1, s2, s3);
+            M = mc;
+            S = (s0 + s1) + (s2 + s3);
         }
-        push_record(a, sm, nrec, warp, lane, part, kMain, mode, d.seq, d.slot, d.seg, d.expect);
-    }
-}
-
-// Residual weights of two ids from packed p and q logits: accumulates the
-// residual sum and the p sum (bit-identical to resid_w per id).
-__device__ __forceinline__ void resid_pair(float xp0, float xp1, float xq0, float xq1, uint64_t C2, uint64_t NZ0,
-                                           uint64_t NZ1, uint64_t& sw, uint64_t& sp) {
-    float a0, a1, b0, b1;
-    unpack_f2(fma_f2(pack_f2(xp0, xp1), C2, NZ0), a0, a1);
-    unpack_f2(fma_f2(pack_f2(xq0, xq1), C2, NZ1), b0, b1);
-    const uint64_t pv = pack_f2(ex2_approx(a0), ex2_approx(a1));
-    const uint64_t qv = pack_f2(ex2_approx(b0), ex2_approx(b1));
-    float d0, d1;
-    unpack_f2(fma_f2(qv, pack_f2(-1.0f, -1.0f), pv), d0, d1);  // pv - qv, one rounding
-    sw = add_f2(sw, pack_f2(fmaxf(0.0f, d0), fmaxf(0.0f, d1)));
-    sp = add_f2(sp, pv);
-}
-
-// Residual weights of one 16-byte vector of p logits and the matching vector
-// of q logits.
-template <int E>
-__device__ __forceinline__ void resid_vec(const uint4& A, const uint4& B, uint64_t C2, uint64_t NZ0, uint64_t NZ1,
-                                          uint64_t& sw, uint64_t& sp) {
-    if constexpr (E == 2) {
-        resid_pair(bf16lo(A.x), bf16hi(A.x), bf16lo(B.x), bf16hi(B.x), C2, NZ0, NZ1, sw, sp);
-        resid_pair(bf16lo(A.y), bf16hi(A.y), bf16lo(B.y), bf16hi(B.y), C2, NZ0, NZ1, sw, sp);
-        resid_pair(bf16lo(A.z), bf16hi(A.z), bf16lo(B.z), bf16hi(B.z), C2, NZ0, NZ1, sw, sp);
-        resid_pair(bf16lo(A.w), bf16hi(A.w), bf16lo(B.w), bf16hi(B.w), C2, NZ0, NZ1, sw, sp);
-    } else {
-        resid_pair(__uint_as_float(A.x), __uint_as_float(A.y), __uint_as_float(B.x), __uint_as_float(B.y), C2, NZ0,
-                   NZ1, sw, sp);
-        resid_pair(__uint_as_float(A.z), __uint_as_float(A.w), __uint_as_float(B.z), __uint_as_float(B.w), C2, NZ0,
-                   NZ1, sw, sp);
-    }
-}
-
-// A tail stage: each consumer warp reduces its own contiguous slice of the
-// sub-chunk (about 1/8 of it), so the selection can later narrow a draw down
-// to one slice.  A slice holds at most 64 vectors: every lane loads its (at
-// most two) vectors of each row up front, then reduces them from registers.
-template <typename Elem>
-__device__ __forceinline__ void tail_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int warp,
-                                           int lane, long long& nrec) {
-    constexpr int E = sizeof(Elem);
-    constexpr int kVec = 16 / E;
-    constexpr uint32_t kNeg = E == 2 ? 0xff80ff80u : 0xff800000u;  // -inf pattern
-    const unsigned char* s0 = sm.stage[stage];
-    const unsigned char* s1 = s0 + kHalf;
-    int wb, we;
-    tail_slice<E>(d.n, warp, wb, we);
-    const bool vec0 = d.skip0 == 0 && d.nsm0 == d.n;  // piece whole and aligned in shared memory
-    const bool vec = vec0 && (d.kind != kTailRes || (d.skip1 == 0 && d.nsm1 == d.n));
-    // The lane's vectors v, v + 32 of the slice, -inf where past its end.
-    const int vb = wb / kVec, ve = we / kVec;
-    const int v0 = vb + lane, v1 = v0 + 32;
-    const uint4 neg = make_uint4(kNeg, kNeg, kNeg, kNeg);
-    uint4 A0 = neg, A1 = neg, B0 = neg, B1 = neg;
-    if (vec) {
-        const uint4* p4 = reinterpret_cast<const uint4*>(s0);
-        if (v0 < ve) A0 = p4[v0];
-        if (v1 < ve) A1 = p4[v1];
-        if (d.kind == kTailRes) {
-            const uint4* q4 = reinterpret_cast<const uint4*>(s1);
-            if (v0 < ve) B0 = q4[v0];
-            if (v1 < ve) B1 = q4[v1];
-        }
-    }
-    float2 part;
-    if (d.kind == kTailRes) {
-        float sws = 0.0f, sps = 0.0f;
-        if (vec) {
-            const uint64_t C2 = pack_f2(d.c2, d.c2);
-            const uint64_t NZ0 = pack_f2(-d.nz0, -d.nz0), NZ1 = pack_f2(-d.nz1, -d.nz1);
-            uint64_t sw0 = 0, sp0 = 0, sw1 = 0, sp1 = 0;
-            resid_vec<E>(A0, B0, C2, NZ0, NZ1, sw0, sp0);
-            resid_vec<E>(A1, B1, C2, NZ0, NZ1, sw1, sp1);
-            float w0, w1, w2, w3, p0, p1, p2, p3;
-            unpack_f2(sw0, w0, w1);
-            unpack_f2(sw1, w2, w3);
-            unpack_f2(sp0, p0, p1);
-            unpack_f2(sp1, p2, p3);
-            sws = (w0 + w1) + (w2 + w3);
-            sps = (p0 + p1) + (p2 + p3);
-        } else {
-            for (int e = wb + lane; e < we; e += 32) {
-                const float xp = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
-                const float xq = piece_elem<Elem>(s1, d.nsm1, d.skip1, d.tail1, e);
-                float pv;
-                sws += resid_w(xp, xq, d.c2, d.nz0, d.nz1, pv);
-                sps += pv;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        part = make_float2(warp_sum(sws), warp_sum(sps));
-    } else if (d.kind == kTailSoft) {
-        float mt = -INFINITY, st = 0.0f;
-        if (vec) {
-            mt = fmaxf(vec_max<E>(A0), vec_max<E>(A1));
-            if (mt != -INFINITY) {
-                const float mct = mt * d.c2;
-                const uint64_t C2 = pack_f2(d.c2, d.c2), NMC = pack_f2(-mct, -mct);
-                uint64_t acc0 = 0, acc1 = 0;
-                soft_vec<E>(A0, C2, NMC, acc0);
-                soft_vec<E>(A1, C2, NMC, acc1);
-                float a0, a1, a2, a3;
-                unpack_f2(acc0, a0, a1);
-                unpack_f2(acc1, a2, a3);
-                st = (a0 + a1) + (a2 + a3);
-            }
-        } else {
-            for (int e = wb + lane; e < we; e += 32) mt = fmaxf(mt, piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e));
-            if (mt != -INFINITY)
-                for (int e = wb + lane; e < we; e += 32)
-                    st += soft_w(piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e), d.c2, mt * d.c2);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        float M = mt == -INFINITY ? -INFINITY : mt * d.c2, S = st;
         warp_merge_mc(M, S);
         part = make_float2(M, S);
-    } else {  // kTailArg: the lane's first maximum in id order
-        float mt = -INFINITY;
-        int it = INT_MAX;
-        if (vec) {
+    } else {
+        // First position of the maximum in this thread's (ascending) elements.
+        constexpr int kPer = kBf16 ? 8 : 4;
+        int idx = INT_MAX;
+        if (cm != -INFINITY) {  // a chunk of -inf alone has no maximum to offer
+            if (tv == cm) idx = d.nsm + tid;
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float x = vec_elem<E>(A0, j);
-                if (v0 < ve && x > mt) {
-                    mt = x;
-                    it = d.e0 + v0 * kVec + j;
-                }
-            }
+            for (int k = kVecPT - 1; k >= 0; --k) {
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float x = vec_elem<E>(A1, j);
-                if (v1 < ve && x > mt) {
-                    mt = x;
-                    it = d.e0 + v1 * kVec + j;
-                }
-            }
-        } else {
-            for (int e = wb + lane; e < we; e += 32) {
-                const float x = piece_elem<Elem>(s0, d.nsm0, d.skip0, d.tail0, e);
-                if (x > mt) {
-                    mt = x;
-                    it = d.e0 + e;
+                for (int j = 3; j >= 0; --j) {
+                    const uint32_t x = w[4 * k + j];
+                    const int base = (tid + k * kCT) * kPer - d.skip;
+                    if constexpr (kBf16) {
+                        if (bf16hi(x) == cm) idx = base + 2 * j + 1;
+                        if (bf16lo(x) == cm) idx = base + 2 * j;
+                    } else {
+                        if (__uint_as_float(x) == cm) idx = base + j;
+                    }
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        warp_merge_arg(mt, it);
-        part = make_float2(mt, __int_as_float(it));
+        float M = cm;
+        int I = idx == INT_MAX ? INT_MAX : d.e0 + idx;
+        warp_merge_arg(M, I);
+        part = make_float2(M, __int_as_float(I));
     }
-    push_record(a, sm, nrec, warp, lane, part, d.kind, d.flags, d.seq, d.slot, 0, 0);
+    push_record(a, sm, nrec, warp, lane, part, kUnit, d.seq, d.slot, d.chunk, d.expect, c2 > 0.0f ? 0 : 1);
 }
 
 template <typename Elem>
 __device__ void consumer(const VerifyArgs& a, SmemV& sm, int tid, int warp, int lane) {
-    MainState ms = {-INFINITY, -INFINITY, 0, 0, INT_MAX};
     long long nrec = 0;
-    long long n = 0;
-    for (;; ++n) {
+    for (long long n = 0;; ++n) {
         const int stage = static_cast<int>(n % kStagesV);
         const uint32_t parity = static_cast<uint32_t>(n / kStagesV) & 1u;
-        // The issuer may idle until other CTAs finish, hence the long bound.
         if (!__all_sync(0xffffffffu, mbar_wait_ns(&sm.full[stage], parity, kDrainWaitNs + kWaitNs))) {
             if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
             break;
         }
         const Desc d = sm.desc[stage];
         if (d.kind == kEnd) break;
-        if (d.kind == kMain)
-            main_stage<Elem>(a, sm, stage, d, tid, warp, lane, ms, nrec);
-        else
-            tail_stage<Elem>(a, sm, stage, d, warp, lane, nrec);
+        unit_stage<Elem>(a, sm, stage, d, tid, warp, lane, nrec);
     }
     // Tell the bookkeeper there is no more work (a record of kind kEnd).
     push_record(a, sm, nrec, warp, lane, make_float2(0.0f, 0.0f), kEnd, 0, 0, 0, 0, 0);
+}
+
+// =============================================================================
+// Workers: tail pieces and draws
+// =============================================================================
+
+__device__ __forceinline__ Tail decode_tail(uint64_t w, int lane) {
+    const uint32_t x = static_cast<uint32_t>(w);
+    Tail t;
+    t.prow = static_cast<int>(__shfl_sync(0xffffffffu, x, kTwPRow));
+    t.qrow = static_cast<int>(__shfl_sync(0xffffffffu, x, kTwQRow));
+    const uint32_t meta = __shfl_sync(0xffffffffu, x, kTwMeta);
+    t.mode = static_cast<int>(meta & 15u);
+    t.qnew = static_cast<int>((meta >> 4) & 1u);
+    t.tag = static_cast<int>((meta >> 8) & 255u);
+    t.pos = static_cast<int>((meta >> 16) & 255u);
+    t.npub = static_cast<int>(meta >> 24);
+    t.c2 = __uint_as_float(__shfl_sync(0xffffffffu, x, kTwC2));
+    t.nz0 = __uint_as_float(__shfl_sync(0xffffffffu, x, kTwNz0));
+    t.nz1 = __uint_as_float(__shfl_sync(0xffffffffu, x, kTwNz1));
+    t.seq = static_cast<int>(__shfl_sync(0xffffffffu, x, kTwSeq));
+    t.dest = static_cast<int>(__shfl_sync(0xffffffffu, x, kTwDest));
+    return t;
+}
+
+template <typename Elem>
+__device__ __forceinline__ const char* tail_prow(const VerifyArgs& a, const Tail& t) {
+    return t.qnew ? a.qnew + static_cast<int64_t>(t.prow) * a.ldqnew_bytes
+                  : a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
+}
+
+// Stage elements [0, n) of a piece of one or two rows (from gp, and gq when
+// `two`) in shared memory (padded rows, pad_off), every load in flight at
+// once: 16-byte cp.async where both rows allow them, the elements left one
+// by one.
+template <typename Elem>
+__device__ __forceinline__ void stage_piece(unsigned char* sp, unsigned char* sq, const char* gp, const char* gq,
+                                            int n, bool two, int lane) {
+    constexpr int E = sizeof(Elem), VEC = 16 / E;
+    const bool v16 = aligned16(gp) && (!two || aligned16(gq));
+    const int nv16 = v16 ? (n * E) >> 4 : 0;
+    for (int v = lane; v < nv16; v += 32) {
+        cp_async16(sp + pad_off(16 * v), gp + 16 * v);
+        if (two) cp_async16(sq + pad_off(16 * v), gq + 16 * v);
+    }
+    using Raw = typename std::conditional<E == 2, uint16_t, uint32_t>::type;
+    for (int e = nv16 * VEC + lane; e < n; e += 32) {
+        *reinterpret_cast<Raw*>(sp + pad_off(e * E)) = reinterpret_cast<const Raw*>(gp)[e];
+        if (two) *reinterpret_cast<Raw*>(sq + pad_off(e * E)) = reinterpret_cast<const Raw*>(gq)[e];
+    }
+    cp_async_wait_all();
+    __syncwarp();
+}
+
+// Ids e .. e + 16/E - 1 of a staged (padded) piece row, -inf past n.
+template <typename Elem>
+__device__ __forceinline__ void staged_vec(const unsigned char* st, int e, int n, float x[16 / sizeof(Elem)]) {
+    constexpr int E = sizeof(Elem), VEC = 16 / E;
+    const uint4 v = *reinterpret_cast<const uint4*>(st + pad_off(e * E));
+#pragma unroll
+    for (int jv = 0; jv < VEC; ++jv) x[jv] = e + jv < n ? vec_elem<E>(v, jv) : -INFINITY;
+}
+
+// One piece (ids [k ps, k ps + ps) of the tail's row or row pair), staged in
+// this worker's buffer, then reduced.  Lane l takes the contiguous block of
+// ids [l q, l q + q), q = ps / 32, and publishes its block's weight (inverse
+// CDF), so that a draw can find its block without scanning the piece.  The
+// piece's result follows as four flagged words:
+//   inverse CDF, residual:  (sum of max(0, p - q), sum of p)
+//   inverse CDF, softmax:   (mc, sum exp2(x c2 - mc)), mc = the piece's largest logit times c2
+//   argmax (T = 0):         (max, lowest id)
+//   Gumbel-max:             (best score, its id, best score of p alone, its id)
+// where a Gumbel score is log2 w_v - log2(-ln u_v); the last pair is the
+// fallback for a residual that rounds to zero everywhere.  Returns true for
+// the piece that completes its tail.
+template <typename Elem>
+__device__ bool run_piece(const VerifyArgs& a, SmemV& sm, int wi, const Tail& t, int slot, int k, int lane) {
+    constexpr int E = sizeof(Elem), VEC = 16 / E;
+    constexpr int kPerLane = kPieceBytes / E / 32;
+    const int e0 = k * a.ps;
+    const int n = min(a.ps, a.vocab - e0);
+    const bool res = t.mode == kTailRes;
+    const bool gum = a.sampler == kSamplerGumbel && t.mode != kTailArg;
+    unsigned char* sp = sm.piece[wi][0];
+    unsigned char* sq = sm.piece[wi][1];
+    stage_piece<Elem>(sp, sq, tail_prow<Elem>(a, t) + static_cast<size_t>(e0) * E,
+                      a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes + static_cast<size_t>(e0) * E, n, res, lane);
+    const int b = lane * kPerLane;  // this lane's block of ids
+    uint32_t out[kPartWords] = {0, 0, 0, 0};
+    if (gum || t.mode == kTailArg) {
+        float best = -INFINITY, best_p = -INFINITY;
+        int bid = INT_MAX, bid_p = INT_MAX;
+        for (int j = 0; j < kPerLane; j += VEC) {
+            const int e = b + j;
+            if (e >= n) break;
+            float xp[VEC], xq[VEC];
+            staged_vec<Elem>(sp, e, n, xp);
+            if (res) staged_vec<Elem>(sq, e, n, xq);
+            if (gum) {
+                // One Philox block (four ids) at a time keeps the live
+                // registers of the uniforms and logarithms few.
+#pragma unroll 1
+                for (int bb = 0; bb < VEC; bb += 4) {
+                    float u[4];
+                    gumbel_block(a, t, (e0 + e + bb) >> 2, u);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int jv = bb + jj;
+                        const int id = e0 + e + jv;
+                        const float g = log2_neg_ln(u[jj]);
+                        float lw, lpw = -INFINITY;
+                        if (res) {
+                            float pv;
+                            const float w = resid_w(xp[jv], xq[jv], t.c2, t.nz0, t.nz1, pv);
+                            lw = w > 0.0f ? lg2_approx(w) : -INFINITY;
+                            lpw = pv > 0.0f ? lg2_approx(pv) : -INFINITY;
+                        } else {
+                            lw = xp[jv] * t.c2;
+                        }
+                        const float sc = lw - g, scp = lpw - g;
+                        if (lw != -INFINITY && sc > best) {
+                            best = sc;
+                            bid = id;
+                        }
+                        if (lpw != -INFINITY && scp > best_p) {
+                            best_p = scp;
+                            bid_p = id;
+                        }
+                    }
+                }
+            } else {  // argmax: the first maximum is kept
+#pragma unroll
+                for (int jv = 0; jv < VEC; ++jv)
+                    if (xp[jv] > best) {
+                        best = xp[jv];
+                        bid = e0 + e + jv;
+                    }
+            }
+        }
+        // Largest score, lowest id among equals.
+        const float W = warp_max(best);
+        const int I = warp_min_int(best == W ? bid : INT_MAX);
+        out[0] = __float_as_uint(W);
+        out[1] = static_cast<uint32_t>(I);
+        if (gum && res) {
+            const float Wp = warp_max(best_p);
+            const int Ip = warp_min_int(best_p == Wp ? bid_p : INT_MAX);
+            out[2] = __float_as_uint(Wp);
+            out[3] = static_cast<uint32_t>(Ip);
+        }
+    } else {
+        // Inverse CDF: the block's weight and the piece's sums, independent
+        // exponentials summed as small trees.
+        float mc = 0.0f;
+        if (!res) {  // the softmax partial's reference: the piece's largest logit times c2
+            float m = -INFINITY;
+#pragma unroll 4
+            for (int j = 0; j < kPerLane; j += VEC) {
+                float xp[VEC];
+                staged_vec<Elem>(sp, b + j, n, xp);
+#pragma unroll
+                for (int jv = 0; jv < VEC; ++jv) m = fmaxf(m, xp[jv]);
+            }
+            m = warp_max(m);
+            mc = m == -INFINITY ? -INFINITY : m * t.c2;
+        }
+        float bw = 0.0f, bp = 0.0f;
+        if (res || mc != -INFINITY) {
+#pragma unroll 2
+            for (int j = 0; j < kPerLane; j += VEC) {
+                float xp[VEC], w[VEC], pv[VEC];
+                staged_vec<Elem>(sp, b + j, n, xp);
+                if (res) {
+                    float xq[VEC];
+                    staged_vec<Elem>(sq, b + j, n, xq);
+#pragma unroll
+                    for (int jv = 0; jv < VEC; ++jv) w[jv] = resid_w(xp[jv], xq[jv], t.c2, t.nz0, t.nz1, pv[jv]);
+                    bp += tree_sum<VEC>(pv);
+                } else {
+#pragma unroll
+                    for (int jv = 0; jv < VEC; ++jv) w[jv] = soft_w(xp[jv], t.c2, mc);
+                }
+                bw += tree_sum<VEC>(w);
+            }
+        }
+        a.tbsum[(static_cast<size_t>(slot) * a.np + k) * 32 + lane] = bw;
+        if (res) {
+            out[0] = __float_as_uint(warp_sum(bw));
+            out[1] = __float_as_uint(warp_sum(bp));
+        } else {
+            out[0] = __float_as_uint(mc);
+            out[1] = __float_as_uint(mc == -INFINITY ? 0.0f : warp_sum(bw));
+        }
+        __syncwarp();
+        if (lane == 0) __threadfence();  // the block weights are visible before the result
+    }
+    int last = 0;
+    if (lane == 0) {
+        const uint32_t f = static_cast<uint32_t>(slot) + 1u;
+        uint64_t* dst = a.tpart + (static_cast<size_t>(slot) * a.np + k) * kPartWords;
+        st_volatile_v2u64(dst, flagged(f, out[0]), flagged(f, out[1]));
+        st_volatile_v2u64(dst + 2, flagged(f, out[2]), flagged(f, out[3]));
+        // The results carry their flags, so the count needs no ordering.
+        last = atomicAdd(a.tcount + slot, 1) == a.np - 1;
+    }
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+// The weight of one id in a draw, from its p (and q) logit: the softmax
+// weight exp2(x c2 - mc) (soft), the residual max(0, p - q), or p itself
+// (a residual that rounded to zero everywhere).  Passed by value.
+struct DrawW {
+    int kind;  // 0 soft, 1 residual, 2 p of the residual's row
+    float c2, mc, nz0, nz1;
+    __device__ __forceinline__ float operator()(float xp, float xq) const {
+        if (kind == 0) return soft_w(xp, c2, mc);
+        float pv;
+        const float rw = resid_w(xp, xq, c2, nz0, nz1, pv);
+        return kind == 1 ? rw : pv;
+    }
+};
+
+// The weight of piece kp of a draw, from its result (soft: (mc, s) rescaled
+// to the largest mc; residual: sum of max(0, p - q), or of p).
+struct PieceW {
+    const float4* pr;
+    int kind;  // as DrawW
+    float mc;
+    __device__ __forceinline__ float operator()(int kp) const {
+        const float4 v = pr[kp];
+        if (kind == 0) return v.x == -INFINITY ? 0.0f : v.y * ex2_approx(v.x - mc);
+        return kind == 1 ? v.x : v.y;
+    }
+};
+
+// Inverse-CDF position of `target` in the running sum of n weights w(0 ..
+// n-1) spread over the warp (lane l holds ids [l q, l q + q)): the first id
+// whose running sum exceeds the target, else the last id of positive weight
+// (rounding), else 0.  `local` receives the target minus the sum before the
+// chosen lane's block.
+template <typename F>
+__device__ __forceinline__ int warp_icdf(int n, int q, float target, const F& w, int lane, float* local = nullptr) {
+    const int b = lane * q;
+    const int cnt = max(0, min(q, n - b));
+    float own = 0.0f;
+    int lp = -1;
+    for (int e = 0; e < cnt; ++e) {
+        const float x = w(b + e);
+        own += x;
+        if (x > 0.0f) lp = b + e;
+    }
+    float incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && incl > target);
+    int found = -1;
+    if (hit) {
+        const int owner = __ffs(hit) - 1;
+        const float before = __shfl_sync(0xffffffffu, incl - own, owner);
+        // The owner's block, one id per lane at a time, in order.
+        const int ob = owner * q;
+        const int ocnt = max(0, min(q, n - ob));
+        float cum = before;
+        for (int e0 = 0; e0 < ocnt && found < 0; e0 += 32) {
+            const int e = e0 + lane;
+            const float x = e < ocnt ? w(ob + e) : 0.0f;
+            float c = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, c, o);
+                if (lane >= o) c += y;
+            }
+            const unsigned h = __ballot_sync(0xffffffffu, e < ocnt && cum + c > target);
+            if (h) {
+                const int hl = __ffs(h) - 1;
+                found = ob + e0 + hl;
+                // The target measured from the start of the chosen element.
+                if (local) *local = target - (cum + __shfl_sync(0xffffffffu, c - x, hl));
+            }
+            cum += __shfl_sync(0xffffffffu, c, 31);
+        }
+        if (found < 0) {  // rounding inside the block: its last element of positive weight
+            found = __shfl_sync(0xffffffffu, lp, owner);
+            if (local) *local = INFINITY;
+        }
+    }
+    if (found < 0) {
+        const int last = warp_max_int(lp);
+        found = last >= 0 ? last : 0;
+        if (local) *local = INFINITY;
+    }
+    return found;
+}
+
+// Inverse-CDF position of `target` in the running weight of a staged piece
+// of `len` ids (weights w(xp, xq) of its staged, padded p and q logits), in
+// vocabulary order.  Lane l sums ids [l q, l q + q) from 16-byte vectors;
+// the lane whose block holds the target is then walked by the whole warp, a
+// few ids per lane.  Rounding that leaves the target past the block's end
+// gives the block's last id of positive weight, past every weight the
+// piece's last one.
+template <typename Elem, typename F>
+__device__ __forceinline__ int piece_icdf(const unsigned char* sp, const unsigned char* sq, bool two, int len,
+                                          float target, const F& w, int lane) {
+    constexpr int E = sizeof(Elem), VEC = 16 / E;
+    constexpr int kPerLane = kPieceBytes / E / 32;
+    constexpr int kSub = kPerLane / 32;
+    const int b = lane * kPerLane;
+    float own = 0.0f;
+    int lp = -1;
+    // A whole vector's weights at a time, independent of each other (ids
+    // past the piece read as -inf, weight 0), summed as a small tree.
+#pragma unroll 2
+    for (int j = 0; j < kPerLane; j += VEC) {
+        const int e = b + j;
+        const uint4 vp = *reinterpret_cast<const uint4*>(sp + pad_off(e * E));
+        const uint4 vq = two ? *reinterpret_cast<const uint4*>(sq + pad_off(e * E)) : make_uint4(0, 0, 0, 0);
+        float wv[VEC];
+#pragma unroll
+        for (int jv = 0; jv < VEC; ++jv) {
+            const bool in = e + jv < len;
+            wv[jv] = w(in ? vec_elem<E>(vp, jv) : -INFINITY, in ? vec_elem<E>(vq, jv) : -INFINITY);
+        }
+#pragma unroll
+        for (int jv = 0; jv < VEC; ++jv)
+            if (wv[jv] > 0.0f) lp = e + jv;
+        own += tree_sum<VEC>(wv);
+    }
+    float incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, b < len && incl > target);
+    int found = -1;
+    if (hit) {
+        const int owner = __ffs(hit) - 1;
+        const float before = __shfl_sync(0xffffffffu, incl - own, owner);
+        const int olp = __shfl_sync(0xffffffffu, lp, owner);  // the block's last id of positive weight
+        const int ob = owner * kPerLane + lane * kSub;          // this lane's ids of the owner's block
+        float sub = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kSub; ++e)
+            if (ob + e < len)
+                sub += w(load_elem<Elem>(sp + pad_off((ob + e) * E)),
+                         two ? load_elem<Elem>(sq + pad_off((ob + e) * E)) : 0.0f);
+        float c = sub;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, c, o);
+            if (lane >= o) c += y;
+        }
+        const unsigned h = __ballot_sync(0xffffffffu, ob < len && before + c > target);
+        if (h) {
+            const int hl = __ffs(h) - 1;
+            if (lane == hl) {
+                float cum = before + c - sub;
+                int last = -1;
+#pragma unroll
+                for (int e = 0; e < kSub; ++e) {
+                    if (found < 0 && ob + e < len) {
+                        const float x = w(load_elem<Elem>(sp + pad_off((ob + e) * E)),
+                                          two ? load_elem<Elem>(sq + pad_off((ob + e) * E)) : 0.0f);
+                        cum += x;
+                        if (x > 0.0f) last = ob + e;
+                        if (cum > target) found = ob + e;
+                    }
+                }
+                if (found < 0) found = last >= 0 ? last : olp;  // rounding inside the lane
+            }
+            found = __shfl_sync(0xffffffffu, found, hl);
+        } else {
+            found = olp;  // rounding inside the block
+        }
+    }
+    if (found < 0) {
+        const int last = warp_max_int(lp);
+        found = last >= 0 ? last : 0;
+    }
+    return found;
+}
+
+// The draw of tail `slot`, by the worker whose piece completed it: reads every
+// piece result (all counted, their flagged words land moments later at
+// most), draws, writes the token, and clears the tail's words and count for
+// the next call.  False if a wait ran out.
+template <typename Elem>
+__device__ bool select_draw(const VerifyArgs& a, SmemV& sm, int wi, const Tail& t, int slot, int lane) {
+    constexpr int E = sizeof(Elem);
+    const int np = a.np;
+    const uint32_t f = static_cast<uint32_t>(slot) + 1u;
+    const uint64_t* src = a.tpart + static_cast<size_t>(slot) * np * kPartWords;
+    float4* pr = sm.ppart[wi];  // this worker's copy of the piece results
+    const bool gum = a.sampler == kSamplerGumbel && t.mode != kTailArg;
+    // The draw's uniform, while the results are on their way.
+    const float rnd = (gum || t.mode == kTailArg) ? 0.0f : decision_uniform(a.seed, a.offset, t.seq, t.pos, t.tag);
+    // Wait for every piece: each lane polls pieces lane, lane + 32, ...
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        bool mine = true;
+        for (int kp = lane; kp < np; kp += 32) {
+            uint64_t w0, w1, w2, w3;
+            ld_volatile_v2u64(src + static_cast<size_t>(kp) * kPartWords, w0, w1);
+            ld_volatile_v2u64(src + static_cast<size_t>(kp) * kPartWords + 2, w2, w3);
+            mine = mine && (w0 >> 32) == f && (w1 >> 32) == f && (w2 >> 32) == f && (w3 >> 32) == f;
+            pr[kp] = make_float4(__uint_as_float(static_cast<uint32_t>(w0)), __uint_as_float(static_cast<uint32_t>(w1)),
+                                 __uint_as_float(static_cast<uint32_t>(w2)), __uint_as_float(static_cast<uint32_t>(w3)));
+        }
+        if (__all_sync(0xffffffffu, mine)) break;
+        if (global_timer_ns() - t0 > a.wait_ns) {
+            if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    __syncwarp();
+    int token;
+    if (gum || t.mode == kTailArg) {
+        // Largest (score, lowest id) over the pieces; a Gumbel residual that
+        // rounded to zero everywhere draws from p_j (its second pair).
+        float M = -INFINITY, Mp = -INFINITY;
+        int I = INT_MAX, Ip = INT_MAX;
+        for (int kp = lane; kp < np; kp += 32) {
+            merge_argmax(M, I, pr[kp].x, __float_as_int(pr[kp].y));
+            merge_argmax(Mp, Ip, pr[kp].z, __float_as_int(pr[kp].w));
+        }
+        warp_merge_arg(M, I);
+        if (gum && t.mode == kTailRes && I == INT_MAX) {
+            warp_merge_arg(Mp, Ip);
+            I = Ip;
+        }
+        token = I == INT_MAX ? 0 : I;
+    } else {
+        // Inverse CDF: piece weights in one scale, the target u * total, its
+        // piece, then its id within the piece, every sum in vocabulary order.
+        const bool soft = t.mode == kTailSoft;
+        float MC = -INFINITY, W = 0.0f;
+        for (int kp = lane; kp < np; kp += 32) {
+            MC = fmaxf(MC, pr[kp].x);
+            W += pr[kp].x;
+        }
+        bool fallback = false;
+        if (soft) MC = warp_max(MC);
+        else fallback = !(warp_sum(W) > 0.0f);  // residual rounded to zero: draw from p_j
+        const int kind = soft ? 0 : (fallback ? 2 : 1);
+        const PieceW piece_w{pr, kind, MC};
+        float total = 0.0f;
+        for (int kp = lane; kp < np; kp += 32) total += piece_w(kp);
+        total = warp_sum(total);
+        float tloc = INFINITY;
+        const int chosen = warp_icdf(np, (np + 31) / 32, rnd * total, piece_w, lane, &tloc);
+        const int lo = chosen * a.ps;
+        const int len = min(a.ps, a.vocab - lo);
+        const bool res = t.mode == kTailRes;
+        const char* gp = tail_prow<Elem>(a, t) + static_cast<size_t>(lo) * E;
+        const char* gq = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes + static_cast<size_t>(lo) * E;
+        if (kind == 2) {
+            // A residual that rounded to zero everywhere draws from p_j: no
+            // block weights of p were kept, so the piece is staged and
+            // scanned whole (a path that rounding alone can reach).
+            unsigned char* sp = sm.piece[wi][0];
+            unsigned char* sq = sm.piece[wi][1];
+            stage_piece<Elem>(sp, sq, gp, gq, len, res, lane);
+            const DrawW id_w{kind, t.c2, MC, t.nz0, t.nz1};
+            token = lo + piece_icdf<Elem>(sp, sq, res, len, tloc, id_w, lane);
+        } else {
+            // The block: its weight per lane, published before the piece's
+            // result (acquired by the fence), in the piece's own scale.
+            __threadfence();
+            const float mc_k = soft ? pr[chosen].x : 0.0f;
+            const float tpiece = soft ? tloc * ex2_approx(MC - mc_k) : tloc;
+            const float bw = __ldcg(a.tbsum + (static_cast<size_t>(slot) * np + chosen) * 32 + lane);
+            constexpr int kPerLane = kPieceBytes / E / 32;
+            constexpr int kSub = kPerLane / 32;
+            float incl = bw;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, incl > tpiece);
+            int bb;
+            float tb;
+            if (hit) {
+                bb = __ffs(hit) - 1;
+                tb = tpiece - __shfl_sync(0xffffffffu, incl - bw, bb);
+            } else {  // rounding left the target past the piece: its last block of positive weight
+                bb = 31 - __clz(static_cast<int>(__ballot_sync(0xffffffffu, bw > 0.0f)) | 1);
+                tb = INFINITY;
+            }
+            // The block's ids straight from the rows: kSub per lane, in order.
+            const DrawW id_w{kind, t.c2, soft ? mc_k : MC, t.nz0, t.nz1};
+            const int ib = bb * kPerLane + lane * kSub;  // this lane's ids in the piece
+            float wv[kSub];
+            float own = 0.0f;
+            int lp = -1;
+#pragma unroll
+            for (int e = 0; e < kSub; ++e) {
+                const bool in = ib + e < len;
+                const float xp = in ? load_elem<Elem>(gp + static_cast<size_t>(ib + e) * E) : -INFINITY;
+                const float xq = (in && res) ? load_elem<Elem>(gq + static_cast<size_t>(ib + e) * E) : -INFINITY;
+                wv[e] = id_w(xp, xq);
+                own += wv[e];
+                if (wv[e] > 0.0f) lp = ib + e;
+            }
+            float c = own;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, c, o);
+                if (lane >= o) c += y;
+            }
+            const unsigned h = __ballot_sync(0xffffffffu, c > tb);
+            int found = -1;
+            if (h) {
+                const int hl = __ffs(h) - 1;
+                if (lane == hl) {
+                    float cum = c - own;
+#pragma unroll
+                    for (int e = 0; e < kSub; ++e) {
+                        cum += wv[e];
+                        if (found < 0 && cum > tb) found = ib + e;
+                    }
+                    if (found < 0) found = lp;  // rounding inside the lane
+                }
+                found = __shfl_sync(0xffffffffu, found, hl);
+            }
+            if (found < 0) {  // rounding inside the block: its last id of positive weight
+                const int lastp = warp_max_int(lp);
+                found = lastp >= 0 ? lastp : bb * kPerLane;
+            }
+            token = lo + found;
+        }
+    }
+    // Clear the tail's words for the next call (every piece has been read),
+    // write the draw, and finalise the sequence with its last draw.
+    uint64_t* dst = a.tpart + static_cast<size_t>(slot) * np * kPartWords;
+    for (int kk = lane; kk < np; kk += 32) {
+        st_volatile_v2u64(dst + static_cast<size_t>(kk) * kPartWords, 0, 0);
+        st_volatile_v2u64(dst + static_cast<size_t>(kk) * kPartWords + 2, 0, 0);
+    }
+    if (lane < kTailWords) st_volatile_u64(a.tdesc + static_cast<size_t>(slot) * kTailWords + lane, 0);
+    if (lane == 0) {
+        a.tcount[slot] = 0;
+        if (t.dest >= 0)
+            a.out_tokens[t.dest] = token;
+        else
+            a.proposals[-1 - t.dest] = token;
+        if (atomicAdd(a.seq_done + t.seq, 1) == t.npub - 1) {
+            a.seq_done[t.seq] = 0;
+            finalize(a);
+        }
+    }
+    return true;
+}
+
+// A worker holds one decision ticket (a sequence index: sequences complete
+// roughly in index order, as the units are dealt) and one tail-piece ticket
+// (a queue slot and a piece), and serves whichever comes ready first.
+template <typename Elem>
+__device__ void worker(const VerifyArgs& a, SmemV& sm, int wi, int lane) {
+    const unsigned long long cap = static_cast<unsigned long long>(a.n_tail) * static_cast<unsigned long long>(a.np);
+    const unsigned long long ndec = sm.batch_bad ? 0ull : static_cast<unsigned long long>(a.num_seqs);
+    const int n_valid = sm.n_valid;
+    unsigned long long raw = 0, rawd = 0;
+    if (lane == 0) {
+        raw = cap > 0 ? atomicAdd(&a.ctl->claim, 1ull) : cap;
+        rawd = ndec > 0 ? atomicAdd(&a.ctl->dclaim, 1ull) : ndec;
+    }
+    unsigned long long ticket = __shfl_sync(0xffffffffu, raw, 0);
+    unsigned long long dtk = __shfl_sync(0xffffffffu, rawd, 0);
+    uint64_t t_mark = global_timer_ns();
+    for (;;) {
+        // A decision ticket of a sequence that has nothing to stream (invalid
+        // as laid out) is passed over.
+        if (dtk < ndec && !seq_lookup(a, sm, static_cast<int>(dtk)).ok) {
+            if (lane == 0) rawd = atomicAdd(&a.ctl->dclaim, 1ull);
+            dtk = __shfl_sync(0xffffffffu, rawd, 0);
+            continue;
+        }
+        const bool have = ticket < cap;
+        const int slot = have ? static_cast<int>(ticket / static_cast<unsigned long long>(a.np)) : 0;
+        const int k = have ? static_cast<int>(ticket % static_cast<unsigned long long>(a.np)) : 0;
+        // One round trip: the decision's ready word, the piece's descriptor
+        // and the completion count.
+        uint64_t w = 0, dw = 0;
+        if (have && lane < kTailWords) w = ld_volatile_u64(a.tdesc + static_cast<size_t>(slot) * kTailWords + lane);
+        if (lane == 30 && dtk < ndec) dw = ld_acquire_u64(a.dready + dtk);
+        int fin = 0;
+        if (lane == 31) fin = ld_volatile(&a.ctl->finalized);
+        dw = __shfl_sync(0xffffffffu, dw, 30);
+        if (dtk < ndec && static_cast<uint32_t>(dw >> 32) == static_cast<uint32_t>(dtk) + 1u) {
+            const int seq = static_cast<int>(dtk);
+            if (lane == 0) {
+                st_volatile_u64(a.dready + seq, 0);  // cleared for the next call
+                rawd = atomicAdd(&a.ctl->dclaim, 1ull);
+            }
+            decide<Elem>(a, sm, wi, seq, lane);
+            dtk = __shfl_sync(0xffffffffu, rawd, 0);
+            t_mark = global_timer_ns();
+            continue;
+        }
+        const bool ready =
+            have && __all_sync(0xffffffffu, lane >= kTailWords || static_cast<uint32_t>(w >> 32) == static_cast<uint32_t>(slot) + 1u);
+        if (ready) {
+            const Tail t = decode_tail(w, lane);
+            // The next ticket is claimed now; its round trip overlaps the piece.
+            if (lane == 0) raw = atomicAdd(&a.ctl->claim, 1ull);
+            if (run_piece<Elem>(a, sm, wi, t, slot, k, lane) && !select_draw<Elem>(a, sm, wi, t, slot, lane)) return;
+            ticket = __shfl_sync(0xffffffffu, raw, 0);
+            t_mark = global_timer_ns();
+            continue;
+        }
+        fin = __shfl_sync(0xffffffffu, fin, 31);
+        if (fin >= n_valid) return;  // every sequence is final
+        if (global_timer_ns() - t_mark > a.wait_ns) {
+            if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+            return;
+        }
+        __nanosleep(100);
+    }
 }
 
 // =============================================================================
@@ -1449,23 +1419,9 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
             mbar_init(&sm.rec_full[s], kCW);
             mbar_init(&sm.rec_empty[s], 1);
         }
-        for (int s = 0; s < kWork; ++s) {
-            mbar_init(&sm.work_full[s], 1);
-            mbar_init(&sm.work_empty[s], 1);
-        }
-        mbar_init(&sm.prio_full, 1);
-        mbar_init(&sm.prio_empty, 1);
-        for (int s = 0; s < kJobs; ++s) {
-            mbar_init(&sm.job_full[s], 1);
-            mbar_init(&sm.job_empty[s], 1);
-        }
         fence_mbarrier_init();
         sm.n_valid = 0;
-        sm.job_take = 0;
     }
-    // The scheduler's first main item, requested while the prologue runs.
-    unsigned long long first = 0;
-    if (tid == kSchedWarp * 32 && a.n_main > 0) first = atomicAdd(&a.ctl->grab, 1ull);
     // Every CTA counts the valid sequences (the grid's exit condition) and
     // checks that the offsets never decrease; small batches keep the offsets
     // and temperatures in shared memory.
@@ -1494,14 +1450,12 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
     }
     __syncthreads();
 
-    if (warp == kIssuerWarp) {
-        if (lane == 0) issuer<Elem>(a, sm);
-    } else if (warp == kSchedWarp) {
-        if (lane == 0) scheduler(a, sm, first);
+    if (warp == kProdWarp) {
+        if (lane == 0) producer<Elem>(a, sm);
     } else if (warp == kBookWarp) {
         bookkeeper(a, sm, lane);
-    } else if (warp >= kFinWarp) {
-        finisher<Elem>(a, sm, warp - kFinWarp, lane);
+    } else if (warp >= kWorkWarp) {
+        worker<Elem>(a, sm, warp - kWorkWarp, lane);
     } else {
         // This CTA's share of the sequences that are invalid as laid out.
         for (long long i = blockIdx.x + static_cast<long long>(warp) * gridDim.x; i < a.num_seqs;
@@ -1521,9 +1475,9 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
                     a.accept_len[i] = -2;
                     if (a.fused) a.valid[i] = 0;
                 }
-            a.ctl->grab = 0;
             a.ctl->tail_reserve = 0;
-            a.ctl->tail_claim = 0;
+            a.ctl->claim = 0;
+            a.ctl->dclaim = 0;
             a.ctl->finalized = 0;
             a.ctl->exited = 0;
         }
