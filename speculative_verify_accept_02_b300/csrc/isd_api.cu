@@ -22,8 +22,8 @@ bool dtype_ok(int dtype) { return dtype == ISD_DTYPE_BF16 || dtype == ISD_DTYPE_
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Workspace of isd_verify (persistent kernel):
-//   [control block | per-sequence counters | per-tail piece counts |
+// Workspace of isd_verify (stream kernel, then draw kernel):
+//   [control block | per-sequence draw counts | per-tail piece counts |
 //    tail descriptors | tail piece results | piece block sums |
 //    per (row slot, chunk) partials]
 struct VerifyPlan {
@@ -41,7 +41,7 @@ VerifyPlan verify_plan(int vocab, int esz) {
 }
 
 struct VerifyLayout {
-    size_t ctl, seq_count, seq_done, dready, tcount, tdesc, tpart, tbsum, part, bytes;
+    size_t ctl, seq_done, tcount, tdesc, tpart, tbsum, part, bytes;
 };
 
 // Tails: one per sequence (its correction or bonus), plus one per qnew row
@@ -53,12 +53,8 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl, bool f
     size_t off = 0;
     l.ctl = off;
     off = align_up(off + sizeof(isd::VerifyCtl));
-    l.seq_count = off;
-    off = align_up(off + sizeof(int) * C);
     l.seq_done = off;
     off = align_up(off + sizeof(int) * C);
-    l.dready = off;
-    off = align_up(off + sizeof(uint64_t) * C);
     l.tcount = off;
     off = align_up(off + sizeof(int) * NT);
     l.tdesc = off;
@@ -182,9 +178,7 @@ isd_status verify_run(const void* p_logits, int64_t ld_p, const void* q_logits, 
     va.relax_log2 = o.tau > 0.0f ? std::log2(1.0f + o.tau) : 0.0f;
     va.sampler = o.sampler;
     va.ctl = reinterpret_cast<VerifyCtl*>(ws + lay.ctl);
-    va.seq_count = reinterpret_cast<int*>(ws + lay.seq_count);
     va.seq_done = reinterpret_cast<int*>(ws + lay.seq_done);
-    va.dready = reinterpret_cast<uint64_t*>(ws + lay.dready);
     va.n_tail = num_seqs + (o.fused ? total_positions : 0);
     va.tdesc = reinterpret_cast<uint64_t*>(ws + lay.tdesc);
     va.tpart = reinterpret_cast<uint64_t*>(ws + lay.tpart);

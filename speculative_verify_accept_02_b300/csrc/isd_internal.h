@@ -61,7 +61,7 @@ constexpr int kMaxProposeChunks = 128;
 constexpr int kProposeCtasPerSm = 2;
 
 // ---------------------------------------------------------------------------
-// Persistent verify kernel
+// Verify step: stream kernel, then draw kernel
 // ---------------------------------------------------------------------------
 
 // Control block (workspace); every call leaves it zero for the next one.
@@ -69,11 +69,12 @@ constexpr int kProposeCtasPerSm = 2;
 // update them concurrently.
 struct VerifyCtl {
     alignas(128) int err;                   // error word (bounded waits)
+    alignas(128) unsigned long long grab;   // units handed out by the stream kernel (batches, in sequence order)
     alignas(128) int tail_reserve;          // tail slots reserved by decisions
     alignas(128) unsigned long long claim;  // tail-piece tickets handed to workers
     alignas(128) unsigned long long dclaim; // decision tickets (sequence indices) handed to workers
     alignas(128) int finalized;             // sequences whose outputs are complete
-    alignas(128) int exited;                // CTAs that have finished
+    alignas(128) int exited;                // CTAs of the draw kernel that have finished
 };
 
 // Tail modes: what the pieces of a draw after a decision reduce.
@@ -122,9 +123,7 @@ struct VerifyArgs {
     float relax_log2;  // log2(1 + tau) of relaxed acceptance, 0 for strict
     int sampler;       // Sampler of the draws after a decision
     VerifyCtl* ctl;
-    int* seq_count;    // [C] units counted
     int* seq_done;     // [C] draws after the decision finished
-    uint64_t* dready;  // [C] flagged word: every unit of the sequence is counted
     // Tails are queued in the order decisions reserve them: a sequence's
     // correction or bonus draw, and in the fused call one draw per qnew row
     // of a sequence that accepted its whole stride.
@@ -157,7 +156,7 @@ struct VerifyArgs {
 constexpr int kPieceBytes = 8192;
 constexpr int kMaxPieces = 128;
 
-// Resident CTAs of the verify kernel per SM.
+// Resident CTAs of the verify step's stream kernel per SM.
 constexpr int kVerifyCtasPerSm = 2;
 
 cudaError_t launch_verify(const VerifyArgs& a, int elem_bytes, int grid, cudaStream_t stream);

@@ -1,52 +1,45 @@
-// The verify step of Introspective Strided Decoding as one persistent kernel
+// The verify step of Introspective Strided Decoding as two kernels
 // ("Introspective Diffusion Language Models | Summary", §2 acceptance rate,
 // §3.2 strict acceptance, residual correction and bonus token, §3.3 online
 // softmax over the vocabulary and a common acceptance path free of
 // correction work), optionally with the next stride's proposal draws of the
 // fused step (§3.2: one forward verifies and proposes).
 //
-// Three kinds of work:
-//   unit       one chunk (at most 16 KB) of one row a decision needs: p_k and
-//              q_k for k <= L_i (T > 0), or p_1 .. p_{L+1} (T = 0).  Units
-//              are numbered in sequence order and dealt round-robin to the
-//              CTAs, so all CTAs walk the batch front to back in step and the
-//              sequences complete one after another at an even pace.  A
-//              unit's softmax partial (max, sum) or argmax lands in the
-//              workspace and is counted against its sequence.
-//   decision   once a sequence's last unit is counted: ratio_k =
-//              min(1, p_k(x_k) / q_k(x_k)), alpha, the accept prefix
-//              (Philox uniforms, one warp ballot; relaxed acceptance tests
-//              min(1, (1 + tau) p/q)) and the emitted prefix; a greedy
-//              correction or bonus (argmaxes of the partials).  The draws
-//              left are published as tails.
-//   tail       one draw after a decision: from the residual max(0, p_j - q_j)
-//              of the one rejected row pair, from the final anchor p_{L+1}
-//              (bonus), or from a qnew row (proposals of the fused call).  A
-//              tail is cut into pieces of 4 KB per row; worker warps of every
-//              CTA take pieces by ticket and reduce them with vector loads
-//              (the rows were streamed moments before, so mostly from L2).
-//              The worker that finishes a tail's last outstanding piece makes
-//              the draw: by inverse CDF (the piece from the piece sums, then
-//              an in-order scan of that piece) or, with the Gumbel-max
-//              sampler, as the largest perturbed score over the pieces.  No
-//              worker ever waits for another.
-//
-// Warps of a CTA:
-//   consumers  (8) reduce the staged chunk, one partial per warp, handed to
-//              the bookkeeper through a record ring;
-//   producer   (one thread) streams the CTA's units into a 4-stage ring with
-//              1-D bulk copies completing on mbarriers;
-//   bookkeeper merges the eight warp partials of a unit, stores and counts
-//              it (device-scope acquire-release), and marks a sequence whose
-//              count completes ready;
-//   workers    (2) take decisions and tail pieces by ticket, and make the
-//              draws.
+// stream kernel  every chunk (at most 16 KB) of every row a decision needs:
+//                p_k and q_k for k <= L_i (T > 0), or p_1 .. p_{L+1}
+//                (T = 0).  Chunks are taken in small batches from a global
+//                counter, staged with 1-D bulk copies into a 4-stage ring
+//                (mbarrier completion) by one producer thread, and reduced by
+//                eight consumer warps to a softmax partial (max, sum) or an
+//                argmax per warp; a bookkeeper warp merges the eight and
+//                stores the chunk's partial.  Nothing else runs beside the
+//                stream: it keeps the HBM busy from its first chunk to its
+//                last.
+// draw kernel    launched behind it (programmatic dependent launch: its CTAs
+//                take the SMs as the stream's retire).  Every warp is a
+//                worker:
+//                  decisions   by ticket (a sequence index): ratio_k =
+//                              min(1, p_k(x_k) / q_k(x_k)), alpha, the accept
+//                              prefix (Philox uniforms, one warp ballot;
+//                              relaxed acceptance tests min(1, (1 + tau) p/q))
+//                              and the emitted prefix; a greedy correction or
+//                              bonus.  The draws left are published as tails;
+//                  pieces      by ticket: 8 KB of a tail's row or row pair (the
+//                              residual max(0, p_j - q_j) of the one rejected
+//                              row pair, the final anchor p_{L+1}, or a qnew
+//                              row of the fused call), staged in padded shared
+//                              memory and reduced, each lane's 128-id block
+//                              weight published before the piece's result;
+//                  draws       by the worker that finishes a tail's last
+//                              piece: by inverse CDF (the piece from the piece
+//                              weights, the block from its block weights, the
+//                              id from the block's logits) or, with the
+//                              Gumbel-max sampler, the largest perturbed score.
 // Tail descriptors and piece results travel as 64-bit words that carry a
 // flag in their high half, so a reader polls the data itself: one global
-// round trip per hand-over.  The grid exits once every sequence is final;
-// its last CTA re-zeroes the control block.  Every wait is bounded by the
-// global timer; on expiry the error word is set and every accept length
-// reads -2.
+// round trip per hand-over.  The draw kernel exits once every sequence is
+// final; its last CTA re-zeroes the control block.  Every wait is bounded;
+// on expiry the error word is set and every accept length reads -2.
 #include <climits>
 #include <type_traits>
 
@@ -56,25 +49,26 @@
 namespace isd {
 namespace {
 
-constexpr int kCW = 8;                 // consumer warps
+constexpr int kCW = 8;                 // consumer warps (stream kernel)
 constexpr int kCT = kCW * 32;          // consumer threads
 constexpr int kProdWarp = kCW;
 constexpr int kBookWarp = kCW + 1;
-constexpr int kWorkWarp = kCW + 2;     // first of kWorkers worker warps
-constexpr int kWorkers = 2;
-constexpr int kThreadsV = 32 * (kCW + 2 + kWorkers);
-constexpr int kStagesV = 3;
+constexpr int kThreadsA = 32 * (kCW + 2);
+constexpr int kStagesV = 4;
 constexpr int kRecs = 16;              // record ring between consumers and bookkeeper
+constexpr int kGrab = 4;               // units taken from the global counter at once
 constexpr int kVecPT = kStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
-constexpr int kSmemSeqs = 1024;        // batches up to this size keep offsets in shared memory
-constexpr int kSmemToks = 2048;        // batches up to this many positions keep their tokens there
+constexpr int kWarpsB = 4;             // workers per CTA of the draw kernel
+constexpr int kThreadsB = 32 * kWarpsB;
+constexpr int kCtasPerSmB = 2;
+constexpr int kSmemSeqs = 512;         // batches up to this size keep offsets in shared memory
+constexpr int kSmemToks = 1024;        // batches up to this many positions keep their tokens there
 constexpr int kPartWords = 4;          // flagged words per piece result
 static_assert(kVecPT * 16 * kCT == kStageBytes, "stage split");
 // A staged piece row keeps 16 bytes of padding after every 256: a lane that
 // reads its own contiguous block of ids then meets no bank conflict.
 constexpr int kPieceRow = kPieceBytes + kPieceBytes / 16;
 __host__ __device__ constexpr int pad_off(int b) { return b + ((b >> 8) << 4); }
-static_assert(kMaxPieces % 32 == 0, "pieces per lane");
 
 enum : int { kEnd = 0, kUnit = 1 };
 
@@ -98,21 +92,31 @@ struct Rec {
     float2 wp[kCW];  // one partial per consumer warp
 };
 
-struct SmemV {
+// The batch layout both kernels read: offsets and temperatures of small
+// batches, proposed tokens, the valid count.
+struct Tables {
+    int n_valid;
+    int batch_bad;
+    int offs[kSmemSeqs + 1];
+    float temp[kSmemSeqs];
+    int tok[kSmemToks];
+};
+
+struct SmemA {
     alignas(128) unsigned char stage[kStagesV][kStageBytes];
-    alignas(16) unsigned char piece[kWorkers][2][kPieceRow];     // each worker's staged piece of p and q
-    float4 ppart[kWorkers][kMaxPieces];                         // each worker's piece results of one draw
     uint64_t full[kStagesV];
     uint64_t empty[kStagesV];
     uint64_t rec_full[kRecs];
     uint64_t rec_empty[kRecs];
     Desc desc[kStagesV];
     Rec rec[kRecs];
-    int n_valid;
-    int batch_bad;
-    int offs[kSmemSeqs + 1];
-    float temp[kSmemSeqs];
-    int tok[kSmemToks];
+    Tables tb;
+};
+
+struct SmemB {
+    alignas(16) unsigned char piece[kWarpsB][2][kPieceRow];  // each worker's staged piece of p and q
+    float4 ppart[kWarpsB][kMaxPieces];                       // each worker's piece results of one draw
+    Tables tb;
 };
 
 // A decoded tail descriptor.
@@ -205,8 +209,8 @@ __device__ __forceinline__ SeqInfo seq_info_t(const int* offs, const float* temp
     return s;
 }
 
-__device__ __forceinline__ SeqInfo seq_lookup(const VerifyArgs& a, const SmemV& sm, int i) {
-    return a.num_seqs <= kSmemSeqs ? seq_info_t(sm.offs, sm.temp, i, a.total)
+__device__ __forceinline__ SeqInfo seq_lookup(const VerifyArgs& a, const Tables& tb, int i) {
+    return a.num_seqs <= kSmemSeqs ? seq_info_t(tb.offs, tb.temp, i, a.total)
                                    : seq_info(a.seq_offsets, a.temperature, i, a.total);
 }
 
@@ -261,7 +265,7 @@ __device__ __forceinline__ Piece make_piece(const char* row, int e0, int n) {
 }
 
 // =============================================================================
-// Decision (bookkeeper warp; lane k handles position k + 1)
+// Decision (one warp; lane k handles position k + 1)
 // =============================================================================
 
 // Publish tail `slot`: eight flagged words (two per 16-byte store).
@@ -273,23 +277,20 @@ __device__ __forceinline__ void publish_tail(const VerifyArgs& a, int slot, cons
 }
 
 template <typename Elem>
-__device__ void decide(const VerifyArgs& a, SmemV& sm, int wi, int i, int lane) {
+__device__ void decide(const VerifyArgs& a, const Tables& tb, float2* sblk, int i, int lane) {
     constexpr int E = sizeof(Elem);
-    // The acquiring read of the sequence's ready word saw every partial of it
-    // published.
-    const SeqInfo s = seq_lookup(a, sm, i);
+    // The stream kernel has completed: every partial of the sequence is in
+    // place.
+    const SeqInfo s = seq_lookup(a, tb, i);
     const int L = s.len;
     const float T = s.T;
     const float c2 = T > 0.0f ? inv_temp_log2e(T) : 0.0f;
     const int r = s.start + lane;
     const bool mine = lane < L;
-    const int x = mine ? (a.total <= kSmemToks ? sm.tok[r] : __ldg(a.tokens + r)) : 0;
+    const int x = mine ? (a.total <= kSmemToks ? tb.tok[r] : __ldg(a.tokens + r)) : 0;
     if (__any_sync(0xffffffffu, mine && (x < 0 || x >= a.vocab))) {
         write_invalid(a, i, s, lane, -1);
-        if (lane == 0) {
-            a.seq_count[i] = 0;
-            finalize(a);
-        }
+        if (lane == 0) finalize(a);
         return;
     }
     const bool stall = i == a.stall_seq;
@@ -298,12 +299,11 @@ __device__ void decide(const VerifyArgs& a, SmemV& sm, int wi, int i, int lane) 
     int tslot = 0;
     if (T > 0.0f && lane == 0 && !stall) tslot = atomicAdd(&a.ctl->tail_reserve, 1);
     // The sequence's partials are one contiguous block, [2 L rows][nck]: it
-    // is staged in this worker's shared buffer in one round trip, together
+    // is staged in this warp's shared buffer in one round trip, together
     // with the proposed tokens' logits, when it fits.
     const float2* blk = a.part + static_cast<size_t>(2 * s.start) * a.nck;
     const int nblk = 2 * L * a.nck;
-    const bool staged = nblk * static_cast<int>(sizeof(float2)) <= static_cast<int>(sizeof(sm.piece[wi]));
-    float2* sblk = reinterpret_cast<float2*>(&sm.piece[wi][0][0]);
+    const bool staged = nblk * static_cast<int>(sizeof(float2)) <= 2 * kPieceRow;
     if (staged)
         for (int v = lane; v < nblk / 2; v += 32) cp_async16(sblk + 2 * v, blk + 2 * v);
     float zp = 0.0f, zq = 0.0f;
@@ -402,15 +402,11 @@ __device__ void decide(const VerifyArgs& a, SmemV& sm, int wi, int i, int lane) 
         }
         if (lane == 0) a.out_tokens[s.start + i + na] = tok;
     }
-    if (stall) {  // check hook: nothing is published, the sequence never completes
-        if (lane == 0) a.seq_count[i] = 0;
-        return;
-    }
+    if (stall) return;  // check hook: nothing is published, the sequence never completes
     // Draws left: the correction or bonus (T > 0), then one per proposal row.
     const int n_tok = T > 0.0f ? 1 : 0;
     const int n_prop = props ? L : 0;
     const int n_pub = n_tok + n_prop;
-    if (lane == 0) a.seq_count[i] = 0;
     if (n_pub == 0) {
         if (lane == 0) finalize(a);
         return;
@@ -456,7 +452,8 @@ __device__ void decide(const VerifyArgs& a, SmemV& sm, int wi, int i, int lane) 
 }
 
 // =============================================================================
-// Bookkeeper warp
+// Bookkeeper warp (stream kernel): merges the eight warp partials of a unit
+// and stores the unit's partial
 // =============================================================================
 
 // Warp reductions within aligned groups of 8 lanes.
@@ -480,15 +477,12 @@ __device__ __forceinline__ void group8_merge_arg(float& M, int& I) {
 }
 
 // Records are taken in batches of up to four that are already complete; lane
-// group g (8 lanes, one per consumer warp) handles record r + g, so the
-// device-scope counts of a batch overlap in one round trip.
-__device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
+// group g (8 lanes, one per consumer warp) handles record r + g.
+__device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
     const int g = lane >> 3, wl = lane & 7;
     for (long long r = 0;;) {
-        // Consumers may idle until other CTAs finish, hence the long bound.
         const bool ok = __all_sync(0xffffffffu, mbar_wait_ns(&sm.rec_full[r % kRecs],
-                                                             static_cast<uint32_t>(r / kRecs) & 1u,
-                                                             kDrainWaitNs + kWaitNs));
+                                                             static_cast<uint32_t>(r / kRecs) & 1u, kWaitNs));
         if (!ok) {
             if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
             break;
@@ -498,14 +492,13 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
             ++nb;
         const bool mine = g < nb;
         const Rec& rc = sm.rec[(r + (mine ? g : 0)) % kRecs];
-        const int kind = rc.kind, seq = rc.seq, rslot = rc.slot, chunk = rc.chunk, expect = rc.expect, arg = rc.arg;
+        const int kind = rc.kind, rslot = rc.slot, chunk = rc.chunk, arg = rc.arg;
         const float2 v = rc.wp[wl];
         __syncwarp();
         if (lane < nb) mbar_arrive(&sm.rec_empty[(r + lane) % kRecs]);
         // An end marker is the last record: the batch stops there.
         const unsigned end_mask = __ballot_sync(0xffffffffu, mine && wl == 0 && kind == kEnd);
         const int n_real = end_mask ? (__ffs(end_mask) - 1) / 8 : nb;
-        const bool act = g < n_real;
         // Both merges run on every lane (shuffles need the whole warp); each
         // group keeps the one its record asks for.
         float Mm = v.x, Sm = v.y;
@@ -513,15 +506,9 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
         float Ma = v.x;
         int Ia = __float_as_int(v.y);
         group8_merge_arg(Ma, Ia);
-        if (act && wl == 0) {
+        if (g < n_real && wl == 0)
             a.part[static_cast<size_t>(rslot) * a.nck + chunk] = arg ? make_float2(Ma, __int_as_float(Ia))
                                                                      : make_float2(Mm, Sm);
-            // The count that completes a sequence acquires every partial of
-            // it; the release of its ready word passes them on to whichever
-            // worker holds the sequence's decision ticket.
-            if (atomic_add_acq_rel(a.seq_count + seq, 1) == expect - 1)
-                st_release_u64(a.dready + seq, flagged(static_cast<uint32_t>(seq) + 1u, 0));
-        }
         __syncwarp();
         r += nb;
         if (end_mask) break;
@@ -529,10 +516,10 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemV& sm, int lane) {
 }
 
 // =============================================================================
-// Producer thread: streams this CTA's units into the stage ring
+// Producer thread (stream kernel): streams chunks into the stage ring
 // =============================================================================
 
-__device__ __forceinline__ int acquire_stage(SmemV& sm, long long n, int* err) {
+__device__ __forceinline__ int acquire_stage(SmemA& sm, long long n, int* err) {
     const int stage = static_cast<int>(n % kStagesV);
     const uint32_t parity = (static_cast<uint32_t>(n / kStagesV) & 1u) ^ 1u;
     if (!mbar_wait_ns(&sm.empty[stage], parity, kWaitNs)) {
@@ -543,19 +530,28 @@ __device__ __forceinline__ int acquire_stage(SmemV& sm, long long n, int* err) {
 }
 
 template <typename Elem>
-__device__ void producer(const VerifyArgs& a, SmemV& sm) {
+__device__ void producer(const VerifyArgs& a, SmemA& sm) {
     constexpr int E = sizeof(Elem);
-    const long long G = gridDim.x;
     long long n = 0;  // stages issued
     bool ok = true;
-    if (!sm.batch_bad) {
+    if (!sm.tb.batch_bad) {
         // Units in sequence order: sequence i owns [base, base + units);
-        // within it, row index ri in [0, rows_of), chunk c in [0, nck).
+        // within it, row index ri in [0, rows_of), chunk c in [0, nck).  A
+        // batch of kGrab units is taken from the global counter one batch
+        // ahead of its use, so a CTA that falls behind takes fewer.
         int i = -1;
         long long base = 0, units = 0;
         SeqInfo s{};
         float c2 = 0.0f;
-        for (long long U = blockIdx.x; ok; U += G) {
+        unsigned long long next = atomicAdd(&a.ctl->grab, static_cast<unsigned long long>(kGrab));
+        unsigned long long cur = 0, cur_end = 0;
+        while (ok) {
+            if (cur == cur_end) {
+                cur = next;
+                cur_end = next + kGrab;
+                next = atomicAdd(&a.ctl->grab, static_cast<unsigned long long>(kGrab));
+            }
+            const long long U = static_cast<long long>(cur++);
             bool more = true;
             while (U >= base + units) {
                 base += units;
@@ -563,7 +559,7 @@ __device__ void producer(const VerifyArgs& a, SmemV& sm) {
                     more = false;
                     break;
                 }
-                s = seq_lookup(a, sm, i);
+                s = seq_lookup(a, sm.tb, i);
                 units = s.ok ? static_cast<long long>(rows_of(s)) * a.nck : 0;
                 c2 = s.T > 0.0f ? inv_temp_log2e(s.T) : 0.0f;
             }
@@ -625,7 +621,7 @@ __device__ void producer(const VerifyArgs& a, SmemV& sm) {
 // =============================================================================
 
 // Hand this warp's partial of a unit to the bookkeeper.
-__device__ __forceinline__ void push_record(const VerifyArgs& a, SmemV& sm, long long& nrec, int warp, int lane,
+__device__ __forceinline__ void push_record(const VerifyArgs& a, SmemA& sm, long long& nrec, int warp, int lane,
                                             float2 part, int kind, int seq, int slot, int chunk, int expect,
                                             int arg) {
     const int rs = static_cast<int>(nrec % kRecs);
@@ -649,7 +645,7 @@ __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemV& sm, long
 }
 
 template <typename Elem>
-__device__ __forceinline__ void unit_stage(const VerifyArgs& a, SmemV& sm, int stage, const Desc& d, int tid,
+__device__ __forceinline__ void unit_stage(const VerifyArgs& a, SmemA& sm, int stage, const Desc& d, int tid,
                                            int warp, int lane, long long& nrec) {
     constexpr bool kBf16 = sizeof(Elem) == 2;
     constexpr uint32_t kNeg = kBf16 ? 0xff80ff80u : 0xff800000u;  // -inf pattern
@@ -757,7 +753,7 @@ __device__ __forceinline__ void unit_stage(const VerifyArgs& a, SmemV& sm, int s
 }
 
 template <typename Elem>
-__device__ void consumer(const VerifyArgs& a, SmemV& sm, int tid, int warp, int lane) {
+__device__ void consumer(const VerifyArgs& a, SmemA& sm, int tid, int warp, int lane) {
     long long nrec = 0;
     for (long long n = 0;; ++n) {
         const int stage = static_cast<int>(n % kStagesV);
@@ -848,15 +844,14 @@ __device__ __forceinline__ void staged_vec(const unsigned char* st, int e, int n
 // fallback for a residual that rounds to zero everywhere.  Returns true for
 // the piece that completes its tail.
 template <typename Elem>
-__device__ bool run_piece(const VerifyArgs& a, SmemV& sm, int wi, const Tail& t, int slot, int k, int lane) {
+__device__ bool run_piece(const VerifyArgs& a, unsigned char* sp, unsigned char* sq, const Tail& t, int slot, int k,
+                          int lane) {
     constexpr int E = sizeof(Elem), VEC = 16 / E;
     constexpr int kPerLane = kPieceBytes / E / 32;
     const int e0 = k * a.ps;
     const int n = min(a.ps, a.vocab - e0);
     const bool res = t.mode == kTailRes;
     const bool gum = a.sampler == kSamplerGumbel && t.mode != kTailArg;
-    unsigned char* sp = sm.piece[wi][0];
-    unsigned char* sq = sm.piece[wi][1];
     stage_piece<Elem>(sp, sq, tail_prow<Elem>(a, t) + static_cast<size_t>(e0) * E,
                       a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes + static_cast<size_t>(e0) * E, n, res, lane);
     const int b = lane * kPerLane;  // this lane's block of ids
@@ -1163,12 +1158,12 @@ __device__ __forceinline__ int piece_icdf(const unsigned char* sp, const unsigne
 // most), draws, writes the token, and clears the tail's words and count for
 // the next call.  False if a wait ran out.
 template <typename Elem>
-__device__ bool select_draw(const VerifyArgs& a, SmemV& sm, int wi, const Tail& t, int slot, int lane) {
+__device__ bool select_draw(const VerifyArgs& a, unsigned char* sp, unsigned char* sq, float4* pr, const Tail& t,
+                            int slot, int lane) {
     constexpr int E = sizeof(Elem);
     const int np = a.np;
     const uint32_t f = static_cast<uint32_t>(slot) + 1u;
     const uint64_t* src = a.tpart + static_cast<size_t>(slot) * np * kPartWords;
-    float4* pr = sm.ppart[wi];  // this worker's copy of the piece results
     const bool gum = a.sampler == kSamplerGumbel && t.mode != kTailArg;
     // The draw's uniform, while the results are on their way.
     const float rnd = (gum || t.mode == kTailArg) ? 0.0f : decision_uniform(a.seed, a.offset, t.seq, t.pos, t.tag);
@@ -1236,8 +1231,6 @@ __device__ bool select_draw(const VerifyArgs& a, SmemV& sm, int wi, const Tail& 
             // A residual that rounded to zero everywhere draws from p_j: no
             // block weights of p were kept, so the piece is staged and
             // scanned whole (a path that rounding alone can reach).
-            unsigned char* sp = sm.piece[wi][0];
-            unsigned char* sq = sm.piece[wi][1];
             stage_piece<Elem>(sp, sq, gp, gq, len, res, lane);
             const DrawW id_w{kind, t.c2, MC, t.nz0, t.nz1};
             token = lo + piece_icdf<Elem>(sp, sq, res, len, tloc, id_w, lane);
@@ -1334,56 +1327,48 @@ __device__ bool select_draw(const VerifyArgs& a, SmemV& sm, int wi, const Tail& 
 // A worker holds one decision ticket (a sequence index: sequences complete
 // roughly in index order, as the units are dealt) and one tail-piece ticket
 // (a queue slot and a piece), and serves whichever comes ready first.
+// =============================================================================
+// Draw kernel workers: every warp takes decision tickets (sequence indices),
+// then tail-piece tickets, and draws the tails whose last piece it finishes
+// =============================================================================
+
 template <typename Elem>
-__device__ void worker(const VerifyArgs& a, SmemV& sm, int wi, int lane) {
+__device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, int lane) {
     const unsigned long long cap = static_cast<unsigned long long>(a.n_tail) * static_cast<unsigned long long>(a.np);
-    const unsigned long long ndec = sm.batch_bad ? 0ull : static_cast<unsigned long long>(a.num_seqs);
-    const int n_valid = sm.n_valid;
+    const unsigned long long ndec = sm.tb.batch_bad ? 0ull : static_cast<unsigned long long>(a.num_seqs);
+    const int n_valid = sm.tb.n_valid;
+    unsigned char* sp = sm.piece[wi][0];
+    unsigned char* sq = sm.piece[wi][1];
     unsigned long long raw = 0, rawd = 0;
-    if (lane == 0) {
-        raw = cap > 0 ? atomicAdd(&a.ctl->claim, 1ull) : cap;
-        rawd = ndec > 0 ? atomicAdd(&a.ctl->dclaim, 1ull) : ndec;
-    }
-    unsigned long long ticket = __shfl_sync(0xffffffffu, raw, 0);
+    if (lane == 0) rawd = ndec > 0 ? atomicAdd(&a.ctl->dclaim, 1ull) : ndec;
     unsigned long long dtk = __shfl_sync(0xffffffffu, rawd, 0);
+    // Decisions first: every sequence is ready, its partials complete.
+    while (dtk < ndec) {
+        if (lane == 0) rawd = atomicAdd(&a.ctl->dclaim, 1ull);
+        if (seq_lookup(a, sm.tb, static_cast<int>(dtk)).ok)
+            decide<Elem>(a, sm.tb, reinterpret_cast<float2*>(sp), static_cast<int>(dtk), lane);
+        dtk = __shfl_sync(0xffffffffu, rawd, 0);
+    }
+    if (lane == 0) raw = cap > 0 ? atomicAdd(&a.ctl->claim, 1ull) : cap;
+    unsigned long long ticket = __shfl_sync(0xffffffffu, raw, 0);
     uint64_t t_mark = global_timer_ns();
     for (;;) {
-        // A decision ticket of a sequence that has nothing to stream (invalid
-        // as laid out) is passed over.
-        if (dtk < ndec && !seq_lookup(a, sm, static_cast<int>(dtk)).ok) {
-            if (lane == 0) rawd = atomicAdd(&a.ctl->dclaim, 1ull);
-            dtk = __shfl_sync(0xffffffffu, rawd, 0);
-            continue;
-        }
         const bool have = ticket < cap;
         const int slot = have ? static_cast<int>(ticket / static_cast<unsigned long long>(a.np)) : 0;
         const int k = have ? static_cast<int>(ticket % static_cast<unsigned long long>(a.np)) : 0;
-        // One round trip: the decision's ready word, the piece's descriptor
-        // and the completion count.
-        uint64_t w = 0, dw = 0;
+        // One round trip: the held ticket's descriptor and the completion count.
+        uint64_t w = 0;
         if (have && lane < kTailWords) w = ld_volatile_u64(a.tdesc + static_cast<size_t>(slot) * kTailWords + lane);
-        if (lane == 30 && dtk < ndec) dw = ld_acquire_u64(a.dready + dtk);
         int fin = 0;
         if (lane == 31) fin = ld_volatile(&a.ctl->finalized);
-        dw = __shfl_sync(0xffffffffu, dw, 30);
-        if (dtk < ndec && static_cast<uint32_t>(dw >> 32) == static_cast<uint32_t>(dtk) + 1u) {
-            const int seq = static_cast<int>(dtk);
-            if (lane == 0) {
-                st_volatile_u64(a.dready + seq, 0);  // cleared for the next call
-                rawd = atomicAdd(&a.ctl->dclaim, 1ull);
-            }
-            decide<Elem>(a, sm, wi, seq, lane);
-            dtk = __shfl_sync(0xffffffffu, rawd, 0);
-            t_mark = global_timer_ns();
-            continue;
-        }
-        const bool ready =
-            have && __all_sync(0xffffffffu, lane >= kTailWords || static_cast<uint32_t>(w >> 32) == static_cast<uint32_t>(slot) + 1u);
+        const bool ready = have && __all_sync(0xffffffffu, lane >= kTailWords ||
+                                                               static_cast<uint32_t>(w >> 32) == static_cast<uint32_t>(slot) + 1u);
         if (ready) {
             const Tail t = decode_tail(w, lane);
             // The next ticket is claimed now; its round trip overlaps the piece.
             if (lane == 0) raw = atomicAdd(&a.ctl->claim, 1ull);
-            if (run_piece<Elem>(a, sm, wi, t, slot, k, lane) && !select_draw<Elem>(a, sm, wi, t, slot, lane)) return;
+            if (run_piece<Elem>(a, sp, sq, t, slot, k, lane) && !select_draw<Elem>(a, sp, sq, sm.ppart[wi], t, slot, lane))
+                return;
             ticket = __shfl_sync(0xffffffffu, raw, 0);
             t_mark = global_timer_ns();
             continue;
@@ -1394,21 +1379,55 @@ __device__ void worker(const VerifyArgs& a, SmemV& sm, int wi, int lane) {
             if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
             return;
         }
-        __nanosleep(100);
+        __nanosleep(64);
     }
 }
 
 // =============================================================================
-// Kernel
+// Kernels
 // =============================================================================
 
-template <typename Elem>
-__global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(const VerifyArgs a) {
-    extern __shared__ unsigned char smem_raw[];
-    SmemV& sm = *reinterpret_cast<SmemV*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// Both kernels' prologue: every CTA counts the valid sequences (the draw
+// kernel's exit condition) and checks that the offsets never decrease; small
+// batches keep the offsets, temperatures and tokens in shared memory.
+template <int kThreads>
+__device__ __forceinline__ bool load_tables(const VerifyArgs& a, Tables& tb, int tid) {
+    if (tid == 0) tb.n_valid = 0;
+    int nv = 0;
+    bool bad = false;
+    const bool small = a.num_seqs <= kSmemSeqs;
+    for (int i = tid; i < a.num_seqs; i += kThreads) {
+        const SeqInfo s = seq_info(a.seq_offsets, a.temperature, i, a.total);
+        nv += s.ok ? 1 : 0;
+        const int end = __ldg(a.seq_offsets + i + 1);
+        bad = bad || end < s.start;
+        if (small) {
+            tb.offs[i] = s.start;
+            tb.temp[i] = s.T;
+            if (i == a.num_seqs - 1) tb.offs[i + 1] = end;
+        }
+    }
+    if (a.total <= kSmemToks)
+        for (int r = tid; r < a.total; r += kThreads) tb.tok[r] = __ldg(a.tokens + r);
+    __syncthreads();
+    if (nv) atomicAdd(&tb.n_valid, nv);
+    bad = __syncthreads_or(bad);
+    if (tid == 0) {
+        tb.batch_bad = bad;
+        if (bad) tb.n_valid = 0;
+    }
+    __syncthreads();
+    return bad;
+}
 
+template <typename Elem>
+__global__ void __launch_bounds__(kThreadsA, kVerifyCtasPerSm) stream_kernel(const VerifyArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    SmemA& sm = *reinterpret_cast<SmemA*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_wait();
+    // The draw kernel's CTAs may be scheduled as soon as SMs free up; they
+    // wait for this grid to complete before reading anything it writes.
     pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < kStagesV; ++s) {
@@ -1420,42 +1439,12 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
             mbar_init(&sm.rec_empty[s], 1);
         }
         fence_mbarrier_init();
-        sm.n_valid = 0;
     }
-    // Every CTA counts the valid sequences (the grid's exit condition) and
-    // checks that the offsets never decrease; small batches keep the offsets
-    // and temperatures in shared memory.
-    int nv = 0;
-    bool bad = false;
-    const bool small = a.num_seqs <= kSmemSeqs;
-    for (int i = tid; i < a.num_seqs; i += kThreadsV) {
-        const SeqInfo s = seq_info(a.seq_offsets, a.temperature, i, a.total);
-        nv += s.ok ? 1 : 0;
-        const int end = __ldg(a.seq_offsets + i + 1);
-        bad = bad || end < s.start;
-        if (small) {
-            sm.offs[i] = s.start;
-            sm.temp[i] = s.T;
-            if (i == a.num_seqs - 1) sm.offs[i + 1] = end;
-        }
-    }
-    if (a.total <= kSmemToks)  // the decisions read the proposed tokens from here
-        for (int r = tid; r < a.total; r += kThreadsV) sm.tok[r] = __ldg(a.tokens + r);
-    __syncthreads();
-    if (nv) atomicAdd(&sm.n_valid, nv);
-    bad = __syncthreads_or(bad);
-    if (tid == 0) {
-        sm.batch_bad = bad;
-        if (bad) sm.n_valid = 0;
-    }
-    __syncthreads();
-
+    const bool bad = load_tables<kThreadsA>(a, sm.tb, tid);
     if (warp == kProdWarp) {
         if (lane == 0) producer<Elem>(a, sm);
     } else if (warp == kBookWarp) {
         bookkeeper(a, sm, lane);
-    } else if (warp >= kWorkWarp) {
-        worker<Elem>(a, sm, warp - kWorkWarp, lane);
     } else {
         // This CTA's share of the sequences that are invalid as laid out.
         for (long long i = blockIdx.x + static_cast<long long>(warp) * gridDim.x; i < a.num_seqs;
@@ -1465,6 +1454,16 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
         }
         consumer<Elem>(a, sm, tid, warp, lane);
     }
+}
+
+template <typename Elem>
+__global__ void __launch_bounds__(kThreadsB, kCtasPerSmB) draw_kernel(const VerifyArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    SmemB& sm = *reinterpret_cast<SmemB*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();  // the stream kernel has completed and its partials are visible
+    load_tables<kThreadsB>(a, sm.tb, tid);
+    worker<Elem>(a, sm, warp, lane);
     __syncthreads();
     if (tid == 0) {
         __threadfence();
@@ -1475,6 +1474,7 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
                     a.accept_len[i] = -2;
                     if (a.fused) a.valid[i] = 0;
                 }
+            a.ctl->grab = 0;
             a.ctl->tail_reserve = 0;
             a.ctl->claim = 0;
             a.ctl->dclaim = 0;
@@ -1484,25 +1484,38 @@ __global__ void __launch_bounds__(kThreadsV, kVerifyCtasPerSm) verify_kernel(con
     }
 }
 
-static_assert(sizeof(SmemV) + 128 <= 113 * 1024, "two CTAs per SM");
+static_assert(sizeof(SmemA) + 128 <= 113 * 1024, "two stream CTAs per SM");
+static_assert(kCtasPerSmB * (sizeof(SmemB) + 128) <= 227 * 1024, "draw CTAs per SM");
 
 template <typename Elem>
 cudaError_t launch_verify_t(const VerifyArgs& a, int grid, cudaStream_t stream) {
-    const size_t smem = sizeof(SmemV) + 128;
-    cudaError_t err = cudaFuncSetAttribute(verify_kernel<Elem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+    const size_t smem_a = sizeof(SmemA) + 128, smem_b = sizeof(SmemB) + 128;
+    cudaError_t err = cudaFuncSetAttribute(stream_kernel<Elem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem_a));
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreadsV);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
+    err = cudaFuncSetAttribute(draw_kernel<Elem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem_b));
+    if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsA);
+    cfg.dynamicSmemBytes = smem_a;
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, verify_kernel<Elem>, a);
+    err = cudaLaunchKernelEx(&cfg, stream_kernel<Elem>, a);
+    if (err != cudaSuccess) return err;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorUnknown;
+    cudaLaunchConfig_t cfg_b = cfg;
+    cfg_b.gridDim = dim3(sms * kCtasPerSmB);
+    cfg_b.blockDim = dim3(kThreadsB);
+    cfg_b.dynamicSmemBytes = smem_b;
+    return cudaLaunchKernelEx(&cfg_b, draw_kernel<Elem>, a);
 }
 
 }  // namespace
