@@ -24,15 +24,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Workspace of isd_verify (stream kernel, then draw kernel):
 //   [control block | per-sequence draw counts | per-tail piece counts |
-//    tail descriptors | tail piece results | piece block sums |
-//    per (row slot, chunk) partials]
+//    tail descriptors | tail piece records | per (row slot, chunk) partials]
 struct VerifyPlan {
     int ck, nck, ps, np;
 };
 
 VerifyPlan verify_plan(int vocab, int esz) {
     VerifyPlan pl;
-    const Chunking main = isd::make_chunking(vocab, esz);
+    const Chunking main = isd::make_chunking(vocab, esz, isd::kVerifyStageBytes);
     pl.ck = main.chunk;
     pl.nck = main.nchunks;
     pl.ps = isd::kPieceBytes / esz;
@@ -41,7 +40,7 @@ VerifyPlan verify_plan(int vocab, int esz) {
 }
 
 struct VerifyLayout {
-    size_t ctl, seq_done, tcount, tdesc, tpart, tbsum, part, bytes;
+    size_t ctl, seq_done, tcount, tdesc, tpart, part, bytes;
 };
 
 // Tails: one per sequence (its correction or bonus), plus one per qnew row
@@ -60,9 +59,7 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl, bool f
     l.tdesc = off;
     off = align_up(off + sizeof(uint64_t) * isd::kTailWords * NT);
     l.tpart = off;
-    off = align_up(off + sizeof(uint64_t) * 4 * NT * static_cast<size_t>(pl.np));  // four words per piece
-    l.tbsum = off;
-    off = align_up(off + sizeof(float) * 32 * NT * static_cast<size_t>(pl.np));  // a block sum per lane and piece
+    off = align_up(off + sizeof(uint64_t) * 20 * NT * static_cast<size_t>(pl.np));  // a record of 20 words per piece
     l.part = off;
     off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * pl.nck);
     l.bytes = off;
@@ -183,7 +180,6 @@ isd_status verify_run(const void* p_logits, int64_t ld_p, const void* q_logits, 
     va.tdesc = reinterpret_cast<uint64_t*>(ws + lay.tdesc);
     va.tpart = reinterpret_cast<uint64_t*>(ws + lay.tpart);
     va.tcount = reinterpret_cast<int*>(ws + lay.tcount);
-    va.tbsum = reinterpret_cast<float*>(ws + lay.tbsum);
     va.part = reinterpret_cast<float2*>(ws + lay.part);
     va.fused = o.fused ? 1 : 0;
     va.qnew = static_cast<const char*>(o.qnew);

@@ -9,21 +9,23 @@
 
 namespace isd {
 
-// One pipeline stage of the streaming kernel holds one chunk of one row.
+// One pipeline stage of the propose kernel holds one chunk of one row; a
+// stage of the verify step's stream kernel holds twice as much.
 constexpr int kStageBytes = 16384;
+constexpr int kVerifyStageBytes = 32768;
 
 // Chunking of a vocabulary row: nchunks pieces of `chunk` elements (the last
 // may be shorter).  `chunk` is a multiple of the 16-byte vector width and,
-// with up to one vector of alignment slack, fits one stage.
+// with up to one vector of alignment slack, fits one stage of stage_bytes.
 struct Chunking {
     int elem_bytes;
     int chunk;
     int nchunks;
 };
 
-inline Chunking make_chunking(int vocab, int elem_bytes) {
+inline Chunking make_chunking(int vocab, int elem_bytes, int stage_bytes = kStageBytes) {
     const int vec = 16 / elem_bytes;
-    const int chunk_max = ((kStageBytes - 16) / elem_bytes) / vec * vec;
+    const int chunk_max = ((stage_bytes - 16) / elem_bytes) / vec * vec;
     Chunking c;
     c.elem_bytes = elem_bytes;
     c.nchunks = (vocab + chunk_max - 1) / chunk_max;
@@ -73,6 +75,7 @@ struct VerifyCtl {
     alignas(128) int tail_reserve;          // tail slots reserved by decisions
     alignas(128) unsigned long long claim;  // tail-piece tickets handed to workers
     alignas(128) unsigned long long dclaim; // decision tickets (sequence indices) handed to workers
+    alignas(128) int ddone;                 // decisions made (their tail slots reserved)
     alignas(128) int finalized;             // sequences whose outputs are complete
     alignas(128) int exited;                // CTAs of the draw kernel that have finished
 };
@@ -129,9 +132,8 @@ struct VerifyArgs {
     // of a sequence that accepted its whole stride.
     int n_tail;        // capacity: C, or C + total when fused
     uint64_t* tdesc;   // [n_tail][kTailWords] flagged descriptor words
-    uint64_t* tpart;   // [n_tail][np][4] flagged piece results
+    uint64_t* tpart;   // [n_tail][np][20] flagged piece records: 4 result words, 16 block weights
     int* tcount;       // [n_tail] pieces finished
-    float* tbsum;      // [n_tail][np][32] per-lane block sums of each piece (published before its result)
     float2* part;      // [2 * total][nck] per (row slot, chunk) partials
     // The fused call (isd_verify_propose): the next stride's proposals of the
     // sequences that accept their whole stride, drawn from qnew rows.

@@ -54,30 +54,25 @@ constexpr int kCT = kCW * 32;          // consumer threads
 constexpr int kProdWarp = kCW;
 constexpr int kBookWarp = kCW + 1;
 constexpr int kThreadsA = 32 * (kCW + 2);
-constexpr int kStagesV = 4;
+constexpr int kStagesV = 3;
 constexpr int kRecs = 16;              // record ring between consumers and bookkeeper
-constexpr int kGrab = 4;               // units taken from the global counter at once
-constexpr int kVecPT = kStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
-constexpr int kWarpsB = 4;             // workers per CTA of the draw kernel
+constexpr int kGrab = 8;               // units taken from the global counter at once, away from the end
+constexpr int kVecPT = kVerifyStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
+constexpr int kWarpsB = 6;             // workers per CTA of the draw kernel
 constexpr int kThreadsB = 32 * kWarpsB;
-constexpr int kCtasPerSmB = 2;
+constexpr int kCtasPerSmB = 1;
 constexpr int kSmemSeqs = 512;         // batches up to this size keep offsets in shared memory
 constexpr int kSmemToks = 1024;        // batches up to this many positions keep their tokens there
 constexpr int kPartWords = 4;          // flagged words per piece result
-static_assert(kVecPT * 16 * kCT == kStageBytes, "stage split");
-// A staged piece row keeps 16 bytes of padding after every 256: a lane that
-// reads its own contiguous block of ids then meets no bank conflict.
-constexpr int kPieceRow = kPieceBytes + kPieceBytes / 16;
-__host__ __device__ constexpr int pad_off(int b) { return b + ((b >> 8) << 4); }
+static_assert(kVecPT * 16 * kCT == kVerifyStageBytes, "stage split");
 
 enum : int { kEnd = 0, kUnit = 1 };
 
 struct Desc {
     int kind;
-    int seq;
     int slot;        // row slot of the partial: 2 r + {0: p, 1: q}
     int chunk;
-    int expect;      // units of the sequence
+    int last;        // 1: the run of consecutive chunks of this row ends here
     int e0;          // first element of the chunk in its row
     int n;           // elements of the chunk
     int nvec;        // 16-byte vectors in shared memory
@@ -87,14 +82,17 @@ struct Desc {
     float c2;        // log2(e) / T, or 0 for an argmax
 };
 
+// A run: consecutive chunks [chunk, chunk + n) of one row slot, reduced by
+// one CTA in a row; its partial covers them all.
 struct Rec {
-    int kind, seq, slot, chunk, expect, arg;
+    int kind, slot, chunk, n, arg;
     float2 wp[kCW];  // one partial per consumer warp
 };
 
 // The batch layout both kernels read: offsets and temperatures of small
 // batches, proposed tokens, the valid count.
 struct Tables {
+    long long units;  // chunks the stream kernel reduces
     int n_valid;
     int batch_bad;
     int offs[kSmemSeqs + 1];
@@ -103,7 +101,7 @@ struct Tables {
 };
 
 struct SmemA {
-    alignas(128) unsigned char stage[kStagesV][kStageBytes];
+    alignas(128) unsigned char stage[kStagesV][kVerifyStageBytes];
     uint64_t full[kStagesV];
     uint64_t empty[kStagesV];
     uint64_t rec_full[kRecs];
@@ -114,8 +112,9 @@ struct SmemA {
 };
 
 struct SmemB {
-    alignas(16) unsigned char piece[kWarpsB][2][kPieceRow];  // each worker's staged piece of p and q
-    float4 ppart[kWarpsB][kMaxPieces];                       // each worker's piece results of one draw
+    alignas(128) unsigned char buf[kWarpsB][2][2][kPieceBytes];  // each worker's two piece buffers (rows p, q)
+    float4 ppart[kWarpsB][kMaxPieces];                            // each worker's piece results of one draw
+    uint64_t bar[kWarpsB][2];                                     // completion of each buffer's copies
     Tables tb;
 };
 
@@ -276,9 +275,47 @@ __device__ __forceinline__ void publish_tail(const VerifyArgs& a, int slot, cons
     for (int k = 0; k < kTailWords; k += 2) st_volatile_v2u64(d + k, flagged(f, w[k]), flagged(f, w[k + 1]));
 }
 
+// What a decision reads from its inputs alone (not from the stream kernel's
+// partials): the proposed tokens, their logits, the acceptance uniforms, and
+// the reservation of the sequence's queue slot.  A warp's first decision
+// takes these before the stream kernel has completed.
+struct DecPrep {
+    int x;       // this lane's proposed token x_{lane+1}
+    float zp;    // its logit in p_{lane+1}
+    float zq;    // its logit in q_{lane+1}
+    float u;     // its acceptance uniform
+    int tslot;   // lane 0: the queue slot of the sequence's correction or bonus draw
+    int bad;     // some proposed token is outside the vocabulary
+};
+
 template <typename Elem>
-__device__ void decide(const VerifyArgs& a, const Tables& tb, float2* sblk, int i, int lane) {
+__device__ __forceinline__ DecPrep decide_prep(const VerifyArgs& a, const Tables& tb, int i, int lane) {
     constexpr int E = sizeof(Elem);
+    const SeqInfo s = seq_lookup(a, tb, i);
+    const int L = s.len;
+    const float T = s.T;
+    const int r = s.start + lane;
+    const bool mine = lane < L;
+    DecPrep d;
+    d.x = mine ? (a.total <= kSmemToks ? tb.tok[r] : __ldg(a.tokens + r)) : 0;
+    d.bad = __any_sync(0xffffffffu, mine && (d.x < 0 || d.x >= a.vocab));
+    // A T > 0 sequence always makes one draw after its decision: its queue
+    // slot is reserved now, so that the round trip overlaps the loads below.
+    d.tslot = 0;
+    if (T > 0.0f && lane == 0 && !d.bad && i != a.stall_seq) d.tslot = atomicAdd(&a.ctl->tail_reserve, 1);
+    d.zp = 0.0f;
+    d.zq = 0.0f;
+    if (mine && T > 0.0f && !d.bad) {
+        d.zp = load_elem<Elem>(a.p + static_cast<int64_t>(r + i) * a.ldp_bytes + static_cast<size_t>(d.x) * E);
+        d.zq = load_elem<Elem>(a.q + static_cast<int64_t>(r) * a.ldq_bytes + static_cast<size_t>(d.x) * E);
+    }
+    d.u = (mine && T > 0.0f) ? decision_uniform(a.seed, a.offset, i, lane + 1, kTagAccept) : 0.0f;
+    return d;
+}
+
+template <typename Elem>
+__device__ __noinline__ void decide(const VerifyArgs& a, const Tables& tb, float2* sblk, int i, const DecPrep pre,
+                                    int lane) {
     // The stream kernel has completed: every partial of the sequence is in
     // place.
     const SeqInfo s = seq_lookup(a, tb, i);
@@ -287,33 +324,22 @@ __device__ void decide(const VerifyArgs& a, const Tables& tb, float2* sblk, int 
     const float c2 = T > 0.0f ? inv_temp_log2e(T) : 0.0f;
     const int r = s.start + lane;
     const bool mine = lane < L;
-    const int x = mine ? (a.total <= kSmemToks ? tb.tok[r] : __ldg(a.tokens + r)) : 0;
-    if (__any_sync(0xffffffffu, mine && (x < 0 || x >= a.vocab))) {
+    const int x = pre.x;
+    if (pre.bad) {
         write_invalid(a, i, s, lane, -1);
         if (lane == 0) finalize(a);
         return;
     }
     const bool stall = i == a.stall_seq;
-    // A T > 0 sequence always makes one draw after its decision: its queue
-    // slot is reserved now, so that the round trip overlaps the loads below.
-    int tslot = 0;
-    if (T > 0.0f && lane == 0 && !stall) tslot = atomicAdd(&a.ctl->tail_reserve, 1);
+    int tslot = pre.tslot;
     // The sequence's partials are one contiguous block, [2 L rows][nck]: it
-    // is staged in this warp's shared buffer in one round trip, together
-    // with the proposed tokens' logits, when it fits.
+    // is staged in this warp's shared buffer in one round trip when it fits.
     const float2* blk = a.part + static_cast<size_t>(2 * s.start) * a.nck;
     const int nblk = 2 * L * a.nck;
-    const bool staged = nblk * static_cast<int>(sizeof(float2)) <= 2 * kPieceRow;
+    const bool staged = nblk * static_cast<int>(sizeof(float2)) <= 2 * kPieceBytes;
     if (staged)
         for (int v = lane; v < nblk / 2; v += 32) cp_async16(sblk + 2 * v, blk + 2 * v);
-    float zp = 0.0f, zq = 0.0f;
-    if (mine && T > 0.0f) {  // the proposed token's logits, from rows read moments ago
-        zp = load_elem<Elem>(a.p + static_cast<int64_t>(r + i) * a.ldp_bytes + static_cast<size_t>(x) * E);
-        zq = load_elem<Elem>(a.q + static_cast<int64_t>(r) * a.ldq_bytes + static_cast<size_t>(x) * E);
-    }
-    // The accept uniform does not depend on the loads: it is drawn while
-    // they are in flight.
-    const float u_acc = (mine && T > 0.0f) ? decision_uniform(a.seed, a.offset, i, lane + 1, kTagAccept) : 0.0f;
+    const float zp = pre.zp, zq = pre.zq, u_acc = pre.u;
     if (staged) cp_async_wait_all();
     __syncwarp();
     const float2* part_of = staged ? sblk : blk;
@@ -477,7 +503,9 @@ __device__ __forceinline__ void group8_merge_arg(float& M, int& I) {
 }
 
 // Records are taken in batches of up to four that are already complete; lane
-// group g (8 lanes, one per consumer warp) handles record r + g.
+// group g (8 lanes, one per consumer warp) handles record r + g.  A run's
+// partial goes to its first chunk; its other chunks get a partial that holds
+// nothing (max -inf; sum 0, or index INT_MAX).
 __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
     const int g = lane >> 3, wl = lane & 7;
     for (long long r = 0;;) {
@@ -492,7 +520,7 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
             ++nb;
         const bool mine = g < nb;
         const Rec& rc = sm.rec[(r + (mine ? g : 0)) % kRecs];
-        const int kind = rc.kind, rslot = rc.slot, chunk = rc.chunk, arg = rc.arg;
+        const int kind = rc.kind, rslot = rc.slot, chunk = rc.chunk, nrun = rc.n, arg = rc.arg;
         const float2 v = rc.wp[wl];
         __syncwarp();
         if (lane < nb) mbar_arrive(&sm.rec_empty[(r + lane) % kRecs]);
@@ -506,9 +534,12 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
         float Ma = v.x;
         int Ia = __float_as_int(v.y);
         group8_merge_arg(Ma, Ia);
-        if (g < n_real && wl == 0)
-            a.part[static_cast<size_t>(rslot) * a.nck + chunk] = arg ? make_float2(Ma, __int_as_float(Ia))
-                                                                     : make_float2(Mm, Sm);
+        if (g < n_real) {
+            float2* dst = a.part + static_cast<size_t>(rslot) * a.nck + chunk;
+            if (wl == 0) *dst = arg ? make_float2(Ma, __int_as_float(Ia)) : make_float2(Mm, Sm);
+            const float2 none = make_float2(-INFINITY, arg ? __int_as_float(INT_MAX) : 0.0f);
+            for (int j = 1 + wl; j < nrun; j += 8) dst[j] = none;
+        }
         __syncwarp();
         r += nb;
         if (end_mask) break;
@@ -519,37 +550,56 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
 // Producer thread (stream kernel): streams chunks into the stage ring
 // =============================================================================
 
-__device__ __forceinline__ int acquire_stage(SmemA& sm, long long n, int* err) {
-    const int stage = static_cast<int>(n % kStagesV);
-    const uint32_t parity = (static_cast<uint32_t>(n / kStagesV) & 1u) ^ 1u;
-    if (!mbar_wait_ns(&sm.empty[stage], parity, kWaitNs)) {
+// The producer's position in the stage ring: the next stage and the phase
+// of its use.
+struct Ring {
+    int stage = 0;
+    uint32_t phase = 0;
+    __device__ void advance() {
+        if (++stage == kStagesV) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+__device__ __forceinline__ int acquire_stage(SmemA& sm, const Ring& rg, int* err) {
+    if (!mbar_wait_ns(&sm.empty[rg.stage], rg.phase ^ 1u, kWaitNs)) {
         atomicOr(err, kErrWaitTimeout);
         return -1;
     }
-    return stage;
+    return rg.stage;
 }
 
 template <typename Elem>
 __device__ void producer(const VerifyArgs& a, SmemA& sm) {
     constexpr int E = sizeof(Elem);
-    long long n = 0;  // stages issued
+    Ring rg;  // stages issued
     bool ok = true;
+    // Each chunk is read once: its lines are the first the L2 gives up, so
+    // that the stream leaves resident what the draw kernel reads next (its
+    // code, the partials) instead of the rows it has finished with.
+    const uint64_t stream_policy = l2_policy_evict_first();
     if (!sm.tb.batch_bad) {
         // Units in sequence order: sequence i owns [base, base + units);
         // within it, row index ri in [0, rows_of), chunk c in [0, nck).  A
-        // batch of kGrab units is taken from the global counter one batch
-        // ahead of its use, so a CTA that falls behind takes fewer.
+        // batch of units is taken from the global counter one batch ahead of
+        // its use, so a CTA that falls behind takes fewer; near the end the
+        // batches shrink to single units, so that CTAs finish together.
         int i = -1;
         long long base = 0, units = 0;
         SeqInfo s{};
         float c2 = 0.0f;
-        unsigned long long next = atomicAdd(&a.ctl->grab, static_cast<unsigned long long>(kGrab));
+        const long long fine = sm.tb.units - 2LL * kGrab * gridDim.x;  // single units from here on
+        unsigned long long g = fine > 0 ? kGrab : 1;
+        unsigned long long next = atomicAdd(&a.ctl->grab, g);
         unsigned long long cur = 0, cur_end = 0;
         while (ok) {
             if (cur == cur_end) {
                 cur = next;
-                cur_end = next + kGrab;
-                next = atomicAdd(&a.ctl->grab, static_cast<unsigned long long>(kGrab));
+                cur_end = next + g;
+                g = static_cast<long long>(next) >= fine ? 1 : kGrab;
+                next = atomicAdd(&a.ctl->grab, g);
             }
             const long long U = static_cast<long long>(cur++);
             bool more = true;
@@ -581,17 +631,19 @@ __device__ void producer(const VerifyArgs& a, SmemA& sm) {
             const int e0 = c * a.ck;
             const int nel = min(a.ck, a.vocab - e0);
             const Piece pc = make_piece<E>(row, e0, nel);
-            const int stage = acquire_stage(sm, n, &a.ctl->err);
+            const int stage = acquire_stage(sm, rg, &a.ctl->err);
             if (stage < 0) {
                 ok = false;
                 break;
             }
             Desc& d = sm.desc[stage];
             d.kind = kUnit;
-            d.seq = i;
             d.slot = slot;
             d.chunk = c;
-            d.expect = static_cast<int>(units);
+            // The run goes on while the next unit of this CTA is the next
+            // chunk of the same row.
+            d.last = c == a.nck - 1 ||
+                     (cur == cur_end && (next != cur_end || static_cast<long long>(next) >= sm.tb.units));
             d.e0 = e0;
             d.n = nel;
             d.nvec = pc.bytes >> 4;
@@ -601,15 +653,15 @@ __device__ void producer(const VerifyArgs& a, SmemA& sm) {
             d.c2 = c2;
             if (pc.bytes > 0) {
                 mbar_arrive_expect_tx(&sm.full[stage], static_cast<uint32_t>(pc.bytes));
-                bulk_copy_g2s(sm.stage[stage], reinterpret_cast<const void*>(pc.lo), static_cast<uint32_t>(pc.bytes),
-                              &sm.full[stage]);
+                bulk_copy_g2s_hint(sm.stage[stage], reinterpret_cast<const void*>(pc.lo),
+                                   static_cast<uint32_t>(pc.bytes), &sm.full[stage], stream_policy);
             } else {
                 mbar_arrive(&sm.full[stage]);
             }
-            ++n;
+            rg.advance();
         }
     }
-    const int stage = acquire_stage(sm, n, &a.ctl->err);
+    const int stage = acquire_stage(sm, rg, &a.ctl->err);
     if (stage >= 0) {
         sm.desc[stage].kind = kEnd;
         mbar_arrive(&sm.full[stage]);
@@ -620,10 +672,9 @@ __device__ void producer(const VerifyArgs& a, SmemA& sm) {
 // Consumer warps
 // =============================================================================
 
-// Hand this warp's partial of a unit to the bookkeeper.
+// Hand this warp's partial of a run to the bookkeeper.
 __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemA& sm, long long& nrec, int warp, int lane,
-                                            float2 part, int kind, int seq, int slot, int chunk, int expect,
-                                            int arg) {
+                                            float2 part, int kind, int slot, int chunk, int n, int arg) {
     const int rs = static_cast<int>(nrec % kRecs);
     const uint32_t parity = (static_cast<uint32_t>(nrec / kRecs) & 1u) ^ 1u;
     ++nrec;
@@ -633,10 +684,9 @@ __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemA& sm, long
         rc.wp[warp] = part;
         if (warp == 0) {
             rc.kind = kind;
-            rc.seq = seq;
             rc.slot = slot;
             rc.chunk = chunk;
-            rc.expect = expect;
+            rc.n = n;
             rc.arg = arg;
         }
         mbar_arrive(&sm.rec_full[rs]);
@@ -644,21 +694,90 @@ __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemA& sm, long
     __syncwarp();
 }
 
+// Largest of 2 kN bf16 (or kN fp32) values, as a tree.
+template <bool kBf16, int kN>
+__device__ __forceinline__ float tree_max(const uint32_t* w) {
+    if constexpr (kBf16) {
+        uint32_t m[kN];
+#pragma unroll
+        for (int j = 0; j < kN; ++j) m[j] = w[j];
+#pragma unroll
+        for (int h = kN / 2; h > 0; h >>= 1)
+#pragma unroll
+            for (int j = 0; j < h; ++j) m[j] = hmax2_bf16(m[j], m[j + h]);
+        return fmaxf(bf16lo(m[0]), bf16hi(m[0]));
+    } else {
+        float m[kN];
+#pragma unroll
+        for (int j = 0; j < kN; ++j) m[j] = __uint_as_float(w[j]);
+#pragma unroll
+        for (int h = kN / 2; h > 0; h >>= 1)
+#pragma unroll
+            for (int j = 0; j < h; ++j) m[j] = fmaxf(m[j], m[j + h]);
+        return m[0];
+    }
+}
+
+// The open run of a consumer thread: softmax partial (RM = largest x c2
+// so far, RS = sum of exp2(x c2 - RM)), or argmax partial (RM, RI: the
+// first position of the largest value).
+struct Run {
+    float RM;
+    float RS;
+    int RI;
+};
+
+// Sum over this thread's share of a chunk of exp2(x c2 - ref), in packed
+// pairs: one fused multiply-add and one addition per two elements.
+template <bool kBf16>
+__device__ __forceinline__ float chunk_sum(const uint32_t* w, float tv, float c2, float ref) {
+    const float2 C2 = make_float2(c2, c2), NMC = make_float2(-ref, -ref);
+    float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                     make_float2(0.0f, 0.0f)};
+#pragma unroll
+    for (int j = 0; j < kVecPT * 4; ++j) {
+        float2 x;
+        if constexpr (kBf16) {
+            x = make_float2(bf16lo(w[j]), bf16hi(w[j]));
+        } else {
+            if (j & 1) continue;
+            x = make_float2(__uint_as_float(w[j]), __uint_as_float(w[j + 1]));
+        }
+        const float2 y = __ffma2_rn(x, C2, NMC);
+        acc[j & 3] = __fadd2_rn(acc[j & 3], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
+    }
+    if (tv != -INFINITY) acc[1].x += soft_w(tv, c2, ref);
+    const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+    return t.x + t.y;
+}
+
+// One stage: this thread's share of the chunk (kVecPT 16-byte vectors, and
+// at most one element after the last whole vector) folded into its run.
 template <typename Elem>
-__device__ __forceinline__ void unit_stage(const VerifyArgs& a, SmemA& sm, int stage, const Desc& d, int tid,
-                                           int warp, int lane, long long& nrec) {
+__device__ __forceinline__ void unit_stage(SmemA& sm, int stage, const Desc& d, int tid, int lane, Run& r) {
     constexpr bool kBf16 = sizeof(Elem) == 2;
     constexpr uint32_t kNeg = kBf16 ? 0xff80ff80u : 0xff800000u;  // -inf pattern
     uint32_t w[kVecPT * 4];
     const uint4* sv = reinterpret_cast<const uint4*>(sm.stage[stage]);
+    if (d.nvec == kVecPT * kCT) {  // a full stage
 #pragma unroll
-    for (int k = 0; k < kVecPT; ++k) {
-        const int vi = tid + k * kCT;
-        const uint4 v = vi < d.nvec ? sv[vi] : make_uint4(kNeg, kNeg, kNeg, kNeg);
-        w[4 * k] = v.x;
-        w[4 * k + 1] = v.y;
-        w[4 * k + 2] = v.z;
-        w[4 * k + 3] = v.w;
+        for (int k = 0; k < kVecPT; ++k) {
+            const uint4 v = sv[tid + k * kCT];
+            w[4 * k] = v.x;
+            w[4 * k + 1] = v.y;
+            w[4 * k + 2] = v.z;
+            w[4 * k + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kVecPT; ++k) {
+            const int vi = tid + k * kCT;
+            const uint4 v = vi < d.nvec ? sv[vi] : make_uint4(kNeg, kNeg, kNeg, kNeg);
+            w[4 * k] = v.x;
+            w[4 * k + 1] = v.y;
+            w[4 * k + 2] = v.z;
+            w[4 * k + 3] = v.w;
+        }
     }
     if (d.skip != 0 && tid == 0) {  // elements before the chunk in the first vector
 #pragma unroll
@@ -677,97 +796,87 @@ __device__ __forceinline__ void unit_stage(const VerifyArgs& a, SmemA& sm, int s
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);
 
-    float cm;
-    if constexpr (kBf16) {
-        uint32_t mx = w[0];
-#pragma unroll
-        for (int j = 1; j < kVecPT * 4; ++j) mx = hmax2_bf16(mx, w[j]);
-        cm = fmaxf(bf16lo(mx), bf16hi(mx));
-    } else {
-        cm = __uint_as_float(w[0]);
-#pragma unroll
-        for (int j = 1; j < kVecPT * 4; ++j) cm = fmaxf(cm, __uint_as_float(w[j]));
-    }
-    cm = fmaxf(cm, tv);
     const float c2 = d.c2;
-    float2 part;
     if (c2 > 0.0f) {
-        float M = -INFINITY, S = 0.0f;
-        if (cm != -INFINITY) {
-            const float mc = cm * c2;
-            const uint64_t C2 = pack_f2(c2, c2), NMC = pack_f2(-mc, -mc);
-            uint64_t acc0 = 0, acc1 = 0;
-#pragma unroll
-            for (int j = 0; j < kVecPT * 4; j += 2) {
-                if constexpr (kBf16) {
-                    float y0, y1, y2, y3;
-                    unpack_f2(fma_f2(pack_f2(bf16lo(w[j]), bf16hi(w[j])), C2, NMC), y0, y1);
-                    unpack_f2(fma_f2(pack_f2(bf16lo(w[j + 1]), bf16hi(w[j + 1])), C2, NMC), y2, y3);
-                    acc0 = add_f2(acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
-                    acc1 = add_f2(acc1, pack_f2(ex2_approx(y2), ex2_approx(y3)));
-                } else {
-                    float y0, y1;
-                    unpack_f2(fma_f2(pack_f2(__uint_as_float(w[j]), __uint_as_float(w[j + 1])), C2, NMC), y0, y1);
-                    if (j & 2)
-                        acc1 = add_f2(acc1, pack_f2(ex2_approx(y0), ex2_approx(y1)));
-                    else
-                        acc0 = add_f2(acc0, pack_f2(ex2_approx(y0), ex2_approx(y1)));
-                }
-            }
-            if (tv != -INFINITY) acc1 = add_f2(acc1, pack_f2(soft_w(tv, c2, mc), 0.0f));
-            float s0, s1, s2, s3;
-            unpack_f2(acc0, s0, s1);
-            unpack_f2(acc1, s2, s3);
-            M = mc;
-            S = (s0 + s1) + (s2 + s3);
+        // The chunk is summed against the run's largest value so far; the
+        // first chunk of a run takes the largest of its first four words.
+        // A sum past 2^64 (a value far above the reference) is summed again
+        // against the chunk's own largest value.
+        float ref = r.RM;
+        if (ref == -INFINITY) ref = fmaxf(tree_max<kBf16, 4>(w), tv) * c2;
+        float sc = ref == -INFINITY ? INFINITY : chunk_sum<kBf16>(w, tv, c2, ref);
+        if (!(sc <= 18446744073709551616.0f)) {
+            ref = fmaxf(tree_max<kBf16, kVecPT * 4>(w), tv) * c2;
+            sc = ref == -INFINITY ? 0.0f : chunk_sum<kBf16>(w, tv, c2, ref);
         }
-        warp_merge_mc(M, S);
-        part = make_float2(M, S);
-    } else {
-        // First position of the maximum in this thread's (ascending) elements.
-        constexpr int kPer = kBf16 ? 8 : 4;
-        int idx = INT_MAX;
-        if (cm != -INFINITY) {  // a chunk of -inf alone has no maximum to offer
-            if (tv == cm) idx = d.nsm + tid;
-#pragma unroll
-            for (int k = kVecPT - 1; k >= 0; --k) {
-#pragma unroll
-                for (int j = 3; j >= 0; --j) {
-                    const uint32_t x = w[4 * k + j];
-                    const int base = (tid + k * kCT) * kPer - d.skip;
-                    if constexpr (kBf16) {
-                        if (bf16hi(x) == cm) idx = base + 2 * j + 1;
-                        if (bf16lo(x) == cm) idx = base + 2 * j;
-                    } else {
-                        if (__uint_as_float(x) == cm) idx = base + j;
-                    }
-                }
-            }
+        if (ref > r.RM) {  // a new reference: rescale the run's sum
+            r.RS = r.RS * ex2_approx(r.RM - ref) + sc;
+            r.RM = ref;
+        } else {
+            r.RS += sc;
         }
-        float M = cm;
-        int I = idx == INT_MAX ? INT_MAX : d.e0 + idx;
-        warp_merge_arg(M, I);
-        part = make_float2(M, __int_as_float(I));
+        return;
     }
-    push_record(a, sm, nrec, warp, lane, part, kUnit, d.seq, d.slot, d.chunk, d.expect, c2 > 0.0f ? 0 : 1);
+    const float cm = fmaxf(tree_max<kBf16, kVecPT * 4>(w), tv);
+    if (cm > r.RM) {
+        // First position of the maximum in this thread's (ascending)
+        // elements; a later chunk of the run takes over only if larger.
+        constexpr int kPer = kBf16 ? 8 : 4;
+        int idx = d.nsm + tid;  // the element after the vectors, unless a vector holds the maximum
+#pragma unroll
+        for (int k = kVecPT - 1; k >= 0; --k) {
+#pragma unroll
+            for (int j = 3; j >= 0; --j) {
+                const uint32_t x = w[4 * k + j];
+                const int base = (tid + k * kCT) * kPer - d.skip;
+                if constexpr (kBf16) {
+                    if (bf16hi(x) == cm) idx = base + 2 * j + 1;
+                    if (bf16lo(x) == cm) idx = base + 2 * j;
+                } else {
+                    if (__uint_as_float(x) == cm) idx = base + j;
+                }
+            }
+        }
+        r.RM = cm;
+        r.RI = d.e0 + idx;
+    }
 }
 
 template <typename Elem>
 __device__ void consumer(const VerifyArgs& a, SmemA& sm, int tid, int warp, int lane) {
     long long nrec = 0;
-    for (long long n = 0;; ++n) {
-        const int stage = static_cast<int>(n % kStagesV);
-        const uint32_t parity = static_cast<uint32_t>(n / kStagesV) & 1u;
+    Run r{-INFINITY, 0.0f, INT_MAX};
+    int run_chunk = -1;  // first chunk of the open run
+    int stage = 0;
+    uint32_t parity = 0;
+    for (;; stage = stage + 1 == kStagesV ? (parity ^= 1u, 0) : stage + 1) {
         if (!__all_sync(0xffffffffu, mbar_wait_ns(&sm.full[stage], parity, kDrainWaitNs + kWaitNs))) {
             if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
             break;
         }
         const Desc d = sm.desc[stage];
         if (d.kind == kEnd) break;
-        unit_stage<Elem>(a, sm, stage, d, tid, warp, lane, nrec);
+        if (run_chunk < 0) run_chunk = d.chunk;
+        unit_stage<Elem>(sm, stage, d, tid, lane, r);
+        if (d.last) {
+            const bool arg = d.c2 == 0.0f;
+            float M = r.RM, S = r.RS;
+            int I = r.RI;
+            float2 part;
+            if (arg) {
+                warp_merge_arg(M, I);
+                part = make_float2(M, __int_as_float(I));
+            } else {
+                warp_merge_mc(M, S);
+                part = make_float2(M, S);
+            }
+            push_record(a, sm, nrec, warp, lane, part, kUnit, d.slot, run_chunk, d.chunk - run_chunk + 1, arg);
+            r = Run{-INFINITY, 0.0f, INT_MAX};
+            run_chunk = -1;
+        }
     }
     // Tell the bookkeeper there is no more work (a record of kind kEnd).
-    push_record(a, sm, nrec, warp, lane, make_float2(0.0f, 0.0f), kEnd, 0, 0, 0, 0, 0);
+    push_record(a, sm, nrec, warp, lane, make_float2(0.0f, 0.0f), kEnd, 0, 0, 0, 0);
 }
 
 // =============================================================================
@@ -799,72 +908,204 @@ __device__ __forceinline__ const char* tail_prow(const VerifyArgs& a, const Tail
                   : a.p + static_cast<int64_t>(t.prow) * a.ldp_bytes;
 }
 
-// Stage elements [0, n) of a piece of one or two rows (from gp, and gq when
-// `two`) in shared memory (padded rows, pad_off), every load in flight at
-// once: 16-byte cp.async where both rows allow them, the elements left one
-// by one.
-template <typename Elem>
-__device__ __forceinline__ void stage_piece(unsigned char* sp, unsigned char* sq, const char* gp, const char* gq,
-                                            int n, bool two, int lane) {
-    constexpr int E = sizeof(Elem), VEC = 16 / E;
-    const bool v16 = aligned16(gp) && (!two || aligned16(gq));
-    const int nv16 = v16 ? (n * E) >> 4 : 0;
-    for (int v = lane; v < nv16; v += 32) {
-        cp_async16(sp + pad_off(16 * v), gp + 16 * v);
-        if (two) cp_async16(sq + pad_off(16 * v), gq + 16 * v);
-    }
-    using Raw = typename std::conditional<E == 2, uint16_t, uint32_t>::type;
-    for (int e = nv16 * VEC + lane; e < n; e += 32) {
-        *reinterpret_cast<Raw*>(sp + pad_off(e * E)) = reinterpret_cast<const Raw*>(gp)[e];
-        if (two) *reinterpret_cast<Raw*>(sq + pad_off(e * E)) = reinterpret_cast<const Raw*>(gq)[e];
-    }
-    cp_async_wait_all();
-    __syncwarp();
-}
+// ---- tail pieces ----------------------------------------------------------------
+// A piece is ids [k ps, k ps + ps) of a tail's row or row pair (kPieceBytes
+// of each row).  A worker double-buffers its pieces: while it reduces one,
+// the bulk copies of the next are in flight.  Its lanes read a staged piece
+// as 16-byte vectors in lane order, so that step j (vectors 32 j .. 32 j +
+// 31, 512 bytes of ids) is block j of the piece: the unit a draw walks after
+// choosing the piece.
 
-// Ids e .. e + 16/E - 1 of a staged (padded) piece row, -inf past n.
+constexpr int kBlk = kPieceBytes / 512;       // blocks per piece
+constexpr int kRecWords = kPartWords + kBlk;  // flagged words per piece record: result, then block weights
+static_assert(kBlk % 4 == 0, "blocks are reduced four at a time");
+
+// A piece a worker holds: its ticket and tail, where its ids are, and how
+// much of each row its buffer stages.
+struct Held {
+    unsigned long long ticket;
+    int state;          // kHeldNone, kHeldWait (descriptor not yet seen), kHeldLoad (copies issued)
+    int slot, k;
+    Tail t;
+    const char* gp;     // first id of the piece in the drawn row
+    const char* gq;     // the same in q_j (residual)
+    int len;            // ids in the piece
+    int nbytes;         // staged bytes of each row: whole 16-byte vectors, 0 when the rows are read in place
+};
+enum : int { kHeldNone = 0, kHeldWait = 1, kHeldLoad = 2 };
+
+// Ids v VEC .. v VEC + VEC - 1 of one row of a piece (-inf past len) from
+// global memory (a draw's block).
 template <typename Elem>
-__device__ __forceinline__ void staged_vec(const unsigned char* st, int e, int n, float x[16 / sizeof(Elem)]) {
+__device__ __forceinline__ void piece_vec_global(const char* g, int len, int v, float x[16 / sizeof(Elem)]) {
     constexpr int E = sizeof(Elem), VEC = 16 / E;
-    const uint4 v = *reinterpret_cast<const uint4*>(st + pad_off(e * E));
+    if (aligned16(g) && (v + 1) * VEC <= len) {
+        const uint4 u = __ldcg(reinterpret_cast<const uint4*>(g) + v);
 #pragma unroll
-    for (int jv = 0; jv < VEC; ++jv) x[jv] = e + jv < n ? vec_elem<E>(v, jv) : -INFINITY;
+        for (int jv = 0; jv < VEC; ++jv) x[jv] = vec_elem<E>(u, jv);
+    } else {
+#pragma unroll
+        for (int jv = 0; jv < VEC; ++jv) {
+            const int e = v * VEC + jv;
+            x[jv] = e < len ? load_elem<Elem>(g + static_cast<size_t>(e) * E) : -INFINITY;
+        }
+    }
 }
 
-// One piece (ids [k ps, k ps + ps) of the tail's row or row pair), staged in
-// this worker's buffer, then reduced.  Lane l takes the contiguous block of
-// ids [l q, l q + q), q = ps / 32, and publishes its block's weight (inverse
-// CDF), so that a draw can find its block without scanning the piece.  The
-// piece's result follows as four flagged words:
+// The same from a staged buffer row (every vector of it is there: copied,
+// or filled by stage_rows).
+template <typename Elem>
+__device__ __forceinline__ void piece_vec(const unsigned char* st, int v, float x[16 / sizeof(Elem)]) {
+    constexpr int E = sizeof(Elem), VEC = 16 / E;
+    const uint4 u = *reinterpret_cast<const uint4*>(st + 16 * v);
+#pragma unroll
+    for (int jv = 0; jv < VEC; ++jv) x[jv] = vec_elem<E>(u, jv);
+}
+
+// Block sums of four blocks: lane l holds v[i], its share of block i; every
+// lane returns the warp's sum for block (l >> 3) & 3 (a reduce-scatter: each
+// of the first two exchanges halves the blocks a lane keeps).
+__device__ __forceinline__ float block_sums4(const float (&v)[4], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8;
+    float w2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        w2[i] = (b4 ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[i + 2], 16);
+    float w1 = (b3 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b3 ? w2[0] : w2[1], 8);
+    w1 += __shfl_xor_sync(0xffffffffu, w1, 4);
+    w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+    w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+    return w1;
+}
+
+// Stage a piece's rows in buffer b: bulk copies of the whole 16-byte vectors
+// (completing on bar[b]) while the lanes fill the rest of each buffer row,
+// the last ids of the row from global memory and -inf past them (rows whose
+// piece does not start on a 16-byte boundary are filled whole), so that a
+// reduction reads every vector from shared memory.
+template <typename Elem>
+__device__ __noinline__ void fill_rows(SmemB& sm, int wi, int b, const char* gp, const char* gq, int len, int nbytes,
+                                      bool two, int lane) {
+    constexpr int E = sizeof(Elem), VEC = 16 / E;
+    using Raw = typename std::conditional<E == 2, uint16_t, uint32_t>::type;
+    constexpr Raw kNegInf = E == 2 ? static_cast<Raw>(0xff80u) : static_cast<Raw>(0xff800000u);
+    for (int r = 0; r < (two ? 2 : 1); ++r) {
+        const Raw* g = reinterpret_cast<const Raw*>(r ? gq : gp);
+        unsigned char* row = sm.buf[wi][b][r];
+        for (int off = nbytes + 16 * lane; off < kPieceBytes; off += 512) {
+            Raw v[VEC];
+#pragma unroll
+            for (int jv = 0; jv < VEC; ++jv) {
+                const int e = off / E + jv;
+                v[jv] = e < len ? g[e] : kNegInf;
+            }
+            *reinterpret_cast<uint4*>(row + off) = *reinterpret_cast<const uint4*>(v);
+        }
+    }
+}
+
+template <typename Elem>
+__device__ __forceinline__ void stage_rows(SmemB& sm, int wi, int b, Held& h, bool two, int lane) {
+    constexpr int E = sizeof(Elem);
+    const bool ok = aligned16(h.gp) && (!two || aligned16(h.gq));
+    h.nbytes = ok ? ((h.len * E) & ~15) : 0;
+    __syncwarp();
+    if (h.nbytes < kPieceBytes) fill_rows<Elem>(sm, wi, b, h.gp, h.gq, h.len, h.nbytes, two, lane);
+    if (lane == 0) {
+        uint64_t* bar = &sm.bar[wi][b];
+        if (h.nbytes > 0) {
+            fence_proxy_async();  // this buffer's earlier reads come before the copy's writes
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(h.nbytes * (two ? 2 : 1)));
+            bulk_copy_g2s(sm.buf[wi][b][0], h.gp, static_cast<uint32_t>(h.nbytes), bar);
+            if (two) bulk_copy_g2s(sm.buf[wi][b][1], h.gq, static_cast<uint32_t>(h.nbytes), bar);
+        } else {
+            mbar_arrive(bar);
+        }
+    }
+    __syncwarp();  // the filled vectors are visible to every lane
+}
+
+// Look for the descriptor of a held ticket; once it is there, issue the
+// piece's copies.  A ticket past the last tail (every decision made, its
+// slot beyond the reserved ones) is dropped.
+template <typename Elem>
+__device__ __forceinline__ void try_start(const VerifyArgs& a, SmemB& sm, int wi, int b, Held& h, int n_valid,
+                                          int lane) {
+    constexpr int E = sizeof(Elem);
+    uint64_t w = 0;
+    if (lane < kTailWords) w = ld_volatile_u64(a.tdesc + static_cast<size_t>(h.slot) * kTailWords + lane);
+    const bool ready = __all_sync(0xffffffffu, lane >= kTailWords ||
+                                                   static_cast<uint32_t>(w >> 32) == static_cast<uint32_t>(h.slot) + 1u);
+    if (!ready) {
+        int gone = 0;
+        if (lane == 0 && ld_acquire(&a.ctl->ddone) >= n_valid) gone = h.slot >= ld_volatile(&a.ctl->tail_reserve);
+        if (__shfl_sync(0xffffffffu, gone, 0)) h.state = kHeldNone;
+        return;
+    }
+    h.t = decode_tail(w, lane);
+    const int e0 = h.k * a.ps;
+    h.len = min(a.ps, a.vocab - e0);
+    h.gp = tail_prow<Elem>(a, h.t) + static_cast<size_t>(e0) * E;
+    h.gq = a.q + static_cast<int64_t>(h.t.qrow) * a.ldq_bytes + static_cast<size_t>(e0) * E;
+    stage_rows<Elem>(sm, wi, b, h, h.t.mode == kTailRes, lane);
+    h.state = kHeldLoad;
+}
+
+// A claimed tail-piece ticket into h.
+__device__ __forceinline__ void take_ticket(const VerifyArgs& a, Held& h, unsigned long long ticket,
+                                            unsigned long long cap) {
+    h.ticket = ticket;
+    if (ticket >= cap) {
+        h.state = kHeldNone;
+        return;
+    }
+    h.slot = static_cast<int>(ticket / static_cast<unsigned long long>(a.np));
+    h.k = static_cast<int>(ticket % static_cast<unsigned long long>(a.np));
+    h.state = kHeldWait;
+}
+
+// Claim the next tail-piece ticket into h.
+__device__ __forceinline__ void claim_piece(const VerifyArgs& a, Held& h, unsigned long long cap, int lane) {
+    unsigned long long raw = 0;
+    if (lane == 0) raw = atomicAdd(&a.ctl->claim, 1ull);
+    take_ticket(a, h, __shfl_sync(0xffffffffu, raw, 0), cap);
+}
+
+// Reduce one staged piece and publish its record: the result as four
+// flagged words,
 //   inverse CDF, residual:  (sum of max(0, p - q), sum of p)
 //   inverse CDF, softmax:   (mc, sum exp2(x c2 - mc)), mc = the piece's largest logit times c2
 //   argmax (T = 0):         (max, lowest id)
 //   Gumbel-max:             (best score, its id, best score of p alone, its id)
-// where a Gumbel score is log2 w_v - log2(-ln u_v); the last pair is the
-// fallback for a residual that rounds to zero everywhere.  Returns true for
-// the piece that completes its tail.
-template <typename Elem>
-__device__ bool run_piece(const VerifyArgs& a, unsigned char* sp, unsigned char* sq, const Tail& t, int slot, int k,
-                          int lane) {
-    constexpr int E = sizeof(Elem), VEC = 16 / E;
-    constexpr int kPerLane = kPieceBytes / E / 32;
-    const int e0 = k * a.ps;
-    const int n = min(a.ps, a.vocab - e0);
+// (a Gumbel score is log2 w_v - log2(-ln u_v); the last pair is the fallback
+// for a residual that rounds to zero everywhere), then, for the inverse CDF,
+// the 16 block weights in the piece's own scale.  Returns, on lane 0, the
+// tail's count of finished pieces before this one (np - 1: this piece
+// completes the tail).
+template <typename Elem, bool kGum>
+__device__ __forceinline__ int reduce_piece(const VerifyArgs& a, const unsigned char* sp, const unsigned char* sq,
+                                             const Held h, int lane) {
+    constexpr int VEC = 16 / sizeof(Elem);
+    const Tail t = h.t;
+    // Everything the loops read, in registers.
+    const float c2 = t.c2, nz0 = t.nz0, nz1 = t.nz1;
+    const int e0 = h.k * a.ps;
+    const int n = h.len;
     const bool res = t.mode == kTailRes;
-    const bool gum = a.sampler == kSamplerGumbel && t.mode != kTailArg;
-    stage_piece<Elem>(sp, sq, tail_prow<Elem>(a, t) + static_cast<size_t>(e0) * E,
-                      a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes + static_cast<size_t>(e0) * E, n, res, lane);
-    const int b = lane * kPerLane;  // this lane's block of ids
+    const bool gum = kGum && t.mode != kTailArg;
+    const uint32_t f = static_cast<uint32_t>(h.slot) + 1u;
+    uint64_t* rec = a.tpart + (static_cast<size_t>(h.slot) * a.np + h.k) * kRecWords;
     uint32_t out[kPartWords] = {0, 0, 0, 0};
     if (gum || t.mode == kTailArg) {
         float best = -INFINITY, best_p = -INFINITY;
         int bid = INT_MAX, bid_p = INT_MAX;
-        for (int j = 0; j < kPerLane; j += VEC) {
-            const int e = b + j;
+        for (int j = 0; j < kBlk; ++j) {
+            const int v = 32 * j + lane;
+            const int e = v * VEC;
             if (e >= n) break;
             float xp[VEC], xq[VEC];
-            staged_vec<Elem>(sp, e, n, xp);
-            if (res) staged_vec<Elem>(sq, e, n, xq);
+            piece_vec<Elem>(sp, v, xp);
+            if (res) piece_vec<Elem>(sq, v, xq);
             if (gum) {
                 // One Philox block (four ids) at a time keeps the live
                 // registers of the uniforms and logarithms few.
@@ -880,11 +1121,11 @@ __device__ bool run_piece(const VerifyArgs& a, unsigned char* sp, unsigned char*
                         float lw, lpw = -INFINITY;
                         if (res) {
                             float pv;
-                            const float w = resid_w(xp[jv], xq[jv], t.c2, t.nz0, t.nz1, pv);
+                            const float w = resid_w(xp[jv], xq[jv], c2, nz0, nz1, pv);
                             lw = w > 0.0f ? lg2_approx(w) : -INFINITY;
                             lpw = pv > 0.0f ? lg2_approx(pv) : -INFINITY;
                         } else {
-                            lw = xp[jv] * t.c2;
+                            lw = xp[jv] * c2;
                         }
                         const float sc = lw - g, scp = lpw - g;
                         if (lw != -INFINITY && sc > best) {
@@ -897,7 +1138,7 @@ __device__ bool run_piece(const VerifyArgs& a, unsigned char* sp, unsigned char*
                         }
                     }
                 }
-            } else {  // argmax: the first maximum is kept
+            } else {  // argmax: the first maximum of this lane's ids is kept
 #pragma unroll
                 for (int jv = 0; jv < VEC; ++jv)
                     if (xp[jv] > best) {
@@ -918,61 +1159,66 @@ __device__ bool run_piece(const VerifyArgs& a, unsigned char* sp, unsigned char*
             out[3] = static_cast<uint32_t>(Ip);
         }
     } else {
-        // Inverse CDF: the block's weight and the piece's sums, independent
-        // exponentials summed as small trees.
+        // Inverse CDF: each block's weight, stored as soon as its group of
+        // four is reduced, and the piece's sums.
         float mc = 0.0f;
-        if (!res) {  // the softmax partial's reference: the piece's largest logit times c2
+        if (!res) {  // the softmax reference: the piece's largest logit times c2
             float m = -INFINITY;
 #pragma unroll 4
-            for (int j = 0; j < kPerLane; j += VEC) {
+            for (int j = 0; j < kBlk; ++j) {
                 float xp[VEC];
-                staged_vec<Elem>(sp, b + j, n, xp);
+                piece_vec<Elem>(sp, 32 * j + lane, xp);
 #pragma unroll
                 for (int jv = 0; jv < VEC; ++jv) m = fmaxf(m, xp[jv]);
             }
             m = warp_max(m);
-            mc = m == -INFINITY ? -INFINITY : m * t.c2;
+            mc = m == -INFINITY ? -INFINITY : m * c2;
         }
-        float bw = 0.0f, bp = 0.0f;
-        if (res || mc != -INFINITY) {
-#pragma unroll 2
-            for (int j = 0; j < kPerLane; j += VEC) {
-                float xp[VEC], w[VEC], pv[VEC];
-                staged_vec<Elem>(sp, b + j, n, xp);
-                if (res) {
-                    float xq[VEC];
-                    staged_vec<Elem>(sq, b + j, n, xq);
+        const bool any = res || mc != -INFINITY;
+        float tot = 0.0f, bp = 0.0f;
+#pragma unroll 1
+        for (int g = 0; g < kBlk / 4; ++g) {
+            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (any) {
 #pragma unroll
-                    for (int jv = 0; jv < VEC; ++jv) w[jv] = resid_w(xp[jv], xq[jv], t.c2, t.nz0, t.nz1, pv[jv]);
-                    bp += tree_sum<VEC>(pv);
-                } else {
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int vi = 32 * (4 * g + jj) + lane;
+                    float xp[VEC], w[VEC];
+                    piece_vec<Elem>(sp, vi, xp);
+                    if (res) {
+                        float xq[VEC], pv[VEC];
+                        piece_vec<Elem>(sq, vi, xq);
 #pragma unroll
-                    for (int jv = 0; jv < VEC; ++jv) w[jv] = soft_w(xp[jv], t.c2, mc);
+                        for (int jv = 0; jv < VEC; ++jv) w[jv] = resid_w(xp[jv], xq[jv], c2, nz0, nz1, pv[jv]);
+                        bp += tree_sum<VEC>(pv);
+                    } else {
+#pragma unroll
+                        for (int jv = 0; jv < VEC; ++jv) w[jv] = soft_w(xp[jv], c2, mc);
+                    }
+                    v[jj] = tree_sum<VEC>(w);
                 }
-                bw += tree_sum<VEC>(w);
+            }
+            const float sg = block_sums4(v, lane);
+            if ((lane & 7) == 0) {
+                st_volatile_u64(rec + kPartWords + 4 * g + (lane >> 3), flagged(f, __float_as_uint(sg)));
+                tot += sg;
             }
         }
-        a.tbsum[(static_cast<size_t>(slot) * a.np + k) * 32 + lane] = bw;
+        // The piece's total is the sum of its block weights, as a draw sees them.
+        tot = warp_sum(tot);
         if (res) {
-            out[0] = __float_as_uint(warp_sum(bw));
+            out[0] = __float_as_uint(tot);
             out[1] = __float_as_uint(warp_sum(bp));
         } else {
             out[0] = __float_as_uint(mc);
-            out[1] = __float_as_uint(mc == -INFINITY ? 0.0f : warp_sum(bw));
+            out[1] = __float_as_uint(mc == -INFINITY ? 0.0f : tot);
         }
-        __syncwarp();
-        if (lane == 0) __threadfence();  // the block weights are visible before the result
     }
-    int last = 0;
-    if (lane == 0) {
-        const uint32_t f = static_cast<uint32_t>(slot) + 1u;
-        uint64_t* dst = a.tpart + (static_cast<size_t>(slot) * a.np + k) * kPartWords;
-        st_volatile_v2u64(dst, flagged(f, out[0]), flagged(f, out[1]));
-        st_volatile_v2u64(dst + 2, flagged(f, out[2]), flagged(f, out[3]));
-        // The results carry their flags, so the count needs no ordering.
-        last = atomicAdd(a.tcount + slot, 1) == a.np - 1;
-    }
-    return __shfl_sync(0xffffffffu, last, 0) != 0;
+    if (lane < kPartWords) st_volatile_u64(rec + lane, flagged(f, out[lane]));
+    // The words carry their flags, so the count needs no ordering.
+    int cnt = 0;
+    if (lane == 0) cnt = atomicAdd(a.tcount + h.slot, 1);
+    return cnt;
 }
 
 // The weight of one id in a draw, from its p (and q) logit: the softmax
@@ -1064,107 +1310,20 @@ __device__ __forceinline__ int warp_icdf(int n, int q, float target, const F& w,
     return found;
 }
 
-// Inverse-CDF position of `target` in the running weight of a staged piece
-// of `len` ids (weights w(xp, xq) of its staged, padded p and q logits), in
-// vocabulary order.  Lane l sums ids [l q, l q + q) from 16-byte vectors;
-// the lane whose block holds the target is then walked by the whole warp, a
-// few ids per lane.  Rounding that leaves the target past the block's end
-// gives the block's last id of positive weight, past every weight the
-// piece's last one.
-template <typename Elem, typename F>
-__device__ __forceinline__ int piece_icdf(const unsigned char* sp, const unsigned char* sq, bool two, int len,
-                                          float target, const F& w, int lane) {
-    constexpr int E = sizeof(Elem), VEC = 16 / E;
-    constexpr int kPerLane = kPieceBytes / E / 32;
-    constexpr int kSub = kPerLane / 32;
-    const int b = lane * kPerLane;
-    float own = 0.0f;
-    int lp = -1;
-    // A whole vector's weights at a time, independent of each other (ids
-    // past the piece read as -inf, weight 0), summed as a small tree.
-#pragma unroll 2
-    for (int j = 0; j < kPerLane; j += VEC) {
-        const int e = b + j;
-        const uint4 vp = *reinterpret_cast<const uint4*>(sp + pad_off(e * E));
-        const uint4 vq = two ? *reinterpret_cast<const uint4*>(sq + pad_off(e * E)) : make_uint4(0, 0, 0, 0);
-        float wv[VEC];
-#pragma unroll
-        for (int jv = 0; jv < VEC; ++jv) {
-            const bool in = e + jv < len;
-            wv[jv] = w(in ? vec_elem<E>(vp, jv) : -INFINITY, in ? vec_elem<E>(vq, jv) : -INFINITY);
-        }
-#pragma unroll
-        for (int jv = 0; jv < VEC; ++jv)
-            if (wv[jv] > 0.0f) lp = e + jv;
-        own += tree_sum<VEC>(wv);
-    }
-    float incl = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, b < len && incl > target);
-    int found = -1;
-    if (hit) {
-        const int owner = __ffs(hit) - 1;
-        const float before = __shfl_sync(0xffffffffu, incl - own, owner);
-        const int olp = __shfl_sync(0xffffffffu, lp, owner);  // the block's last id of positive weight
-        const int ob = owner * kPerLane + lane * kSub;          // this lane's ids of the owner's block
-        float sub = 0.0f;
-#pragma unroll
-        for (int e = 0; e < kSub; ++e)
-            if (ob + e < len)
-                sub += w(load_elem<Elem>(sp + pad_off((ob + e) * E)),
-                         two ? load_elem<Elem>(sq + pad_off((ob + e) * E)) : 0.0f);
-        float c = sub;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, c, o);
-            if (lane >= o) c += y;
-        }
-        const unsigned h = __ballot_sync(0xffffffffu, ob < len && before + c > target);
-        if (h) {
-            const int hl = __ffs(h) - 1;
-            if (lane == hl) {
-                float cum = before + c - sub;
-                int last = -1;
-#pragma unroll
-                for (int e = 0; e < kSub; ++e) {
-                    if (found < 0 && ob + e < len) {
-                        const float x = w(load_elem<Elem>(sp + pad_off((ob + e) * E)),
-                                          two ? load_elem<Elem>(sq + pad_off((ob + e) * E)) : 0.0f);
-                        cum += x;
-                        if (x > 0.0f) last = ob + e;
-                        if (cum > target) found = ob + e;
-                    }
-                }
-                if (found < 0) found = last >= 0 ? last : olp;  // rounding inside the lane
-            }
-            found = __shfl_sync(0xffffffffu, found, hl);
-        } else {
-            found = olp;  // rounding inside the block
-        }
-    }
-    if (found < 0) {
-        const int last = warp_max_int(lp);
-        found = last >= 0 ? last : 0;
-    }
-    return found;
-}
-
-// The draw of tail `slot`, by the worker whose piece completed it: reads every
+// The draw of a tail, by the worker whose piece completed it: reads every
 // piece result (all counted, their flagged words land moments later at
 // most), draws, writes the token, and clears the tail's words and count for
 // the next call.  False if a wait ran out.
-template <typename Elem>
-__device__ bool select_draw(const VerifyArgs& a, unsigned char* sp, unsigned char* sq, float4* pr, const Tail& t,
-                            int slot, int lane) {
-    constexpr int E = sizeof(Elem);
+template <typename Elem, bool kGum>
+__device__ __noinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi, const Held hd, int lane) {
+    constexpr int VEC = 16 / sizeof(Elem);
+    const Tail& t = hd.t;
+    const int slot = hd.slot;
     const int np = a.np;
+    float4* pr = sm.ppart[wi];
     const uint32_t f = static_cast<uint32_t>(slot) + 1u;
-    const uint64_t* src = a.tpart + static_cast<size_t>(slot) * np * kPartWords;
-    const bool gum = a.sampler == kSamplerGumbel && t.mode != kTailArg;
+    const uint64_t* src = a.tpart + static_cast<size_t>(slot) * np * kRecWords;
+    const bool gum = kGum && t.mode != kTailArg;
     // The draw's uniform, while the results are on their way.
     const float rnd = (gum || t.mode == kTailArg) ? 0.0f : decision_uniform(a.seed, a.offset, t.seq, t.pos, t.tag);
     // Wait for every piece: each lane polls pieces lane, lane + 32, ...
@@ -1173,8 +1332,8 @@ __device__ bool select_draw(const VerifyArgs& a, unsigned char* sp, unsigned cha
         bool mine = true;
         for (int kp = lane; kp < np; kp += 32) {
             uint64_t w0, w1, w2, w3;
-            ld_volatile_v2u64(src + static_cast<size_t>(kp) * kPartWords, w0, w1);
-            ld_volatile_v2u64(src + static_cast<size_t>(kp) * kPartWords + 2, w2, w3);
+            ld_volatile_v2u64(src + static_cast<size_t>(kp) * kRecWords, w0, w1);
+            ld_volatile_v2u64(src + static_cast<size_t>(kp) * kRecWords + 2, w2, w3);
             mine = mine && (w0 >> 32) == f && (w1 >> 32) == f && (w2 >> 32) == f && (w3 >> 32) == f;
             pr[kp] = make_float4(__uint_as_float(static_cast<uint32_t>(w0)), __uint_as_float(static_cast<uint32_t>(w1)),
                                  __uint_as_float(static_cast<uint32_t>(w2)), __uint_as_float(static_cast<uint32_t>(w3)));
@@ -1205,7 +1364,7 @@ __device__ bool select_draw(const VerifyArgs& a, unsigned char* sp, unsigned cha
         token = I == INT_MAX ? 0 : I;
     } else {
         // Inverse CDF: piece weights in one scale, the target u * total, its
-        // piece, then its id within the piece, every sum in vocabulary order.
+        // piece, its block, then its id, every sum in vocabulary order.
         const bool soft = t.mode == kTailSoft;
         float MC = -INFINITY, W = 0.0f;
         for (int kp = lane; kp < np; kp += 32) {
@@ -1222,93 +1381,116 @@ __device__ bool select_draw(const VerifyArgs& a, unsigned char* sp, unsigned cha
         total = warp_sum(total);
         float tloc = INFINITY;
         const int chosen = warp_icdf(np, (np + 31) / 32, rnd * total, piece_w, lane, &tloc);
+        Held h = hd;
         const int lo = chosen * a.ps;
-        const int len = min(a.ps, a.vocab - lo);
-        const bool res = t.mode == kTailRes;
-        const char* gp = tail_prow<Elem>(a, t) + static_cast<size_t>(lo) * E;
-        const char* gq = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes + static_cast<size_t>(lo) * E;
+        h.k = chosen;
+        h.len = min(a.ps, a.vocab - lo);
+        h.gp = tail_prow<Elem>(a, t) + static_cast<size_t>(lo) * sizeof(Elem);
+        h.gq = a.q + static_cast<int64_t>(t.qrow) * a.ldq_bytes + static_cast<size_t>(lo) * sizeof(Elem);
+        h.nbytes = 0;
+        const float mc_k = soft ? pr[chosen].x : 0.0f;
+        const DrawW id_w{kind, t.c2, soft ? mc_k : MC, t.nz0, t.nz1};
+        float bw = 0.0f;  // lane j < 16: the weight of block j of the chosen piece
         if (kind == 2) {
             // A residual that rounded to zero everywhere draws from p_j: no
-            // block weights of p were kept, so the piece is staged and
-            // scanned whole (a path that rounding alone can reach).
-            stage_piece<Elem>(sp, sq, gp, gq, len, res, lane);
-            const DrawW id_w{kind, t.c2, MC, t.nz0, t.nz1};
-            token = lo + piece_icdf<Elem>(sp, sq, res, len, tloc, id_w, lane);
-        } else {
-            // The block: its weight per lane, published before the piece's
-            // result (acquired by the fence), in the piece's own scale.
-            __threadfence();
-            const float mc_k = soft ? pr[chosen].x : 0.0f;
-            const float tpiece = soft ? tloc * ex2_approx(MC - mc_k) : tloc;
-            const float bw = __ldcg(a.tbsum + (static_cast<size_t>(slot) * np + chosen) * 32 + lane);
-            constexpr int kPerLane = kPieceBytes / E / 32;
-            constexpr int kSub = kPerLane / 32;
-            float incl = bw;
+            // block weights of p were kept, so its blocks are summed here
+            // from the row (a path that rounding alone can reach).
+#pragma unroll 1
+            for (int g = 0; g < kBlk / 4; ++g) {
+                float v[4];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, incl > tpiece);
-            int bb;
-            float tb;
-            if (hit) {
-                bb = __ffs(hit) - 1;
-                tb = tpiece - __shfl_sync(0xffffffffu, incl - bw, bb);
-            } else {  // rounding left the target past the piece: its last block of positive weight
-                bb = 31 - __clz(static_cast<int>(__ballot_sync(0xffffffffu, bw > 0.0f)) | 1);
-                tb = INFINITY;
-            }
-            // The block's ids straight from the rows: kSub per lane, in order.
-            const DrawW id_w{kind, t.c2, soft ? mc_k : MC, t.nz0, t.nz1};
-            const int ib = bb * kPerLane + lane * kSub;  // this lane's ids in the piece
-            float wv[kSub];
-            float own = 0.0f;
-            int lp = -1;
+                for (int jj = 0; jj < 4; ++jj) {
+                    float xp[VEC], w[VEC];
+                    piece_vec_global<Elem>(h.gp, h.len, 32 * (4 * g + jj) + lane, xp);
 #pragma unroll
-            for (int e = 0; e < kSub; ++e) {
-                const bool in = ib + e < len;
-                const float xp = in ? load_elem<Elem>(gp + static_cast<size_t>(ib + e) * E) : -INFINITY;
-                const float xq = (in && res) ? load_elem<Elem>(gq + static_cast<size_t>(ib + e) * E) : -INFINITY;
-                wv[e] = id_w(xp, xq);
-                own += wv[e];
-                if (wv[e] > 0.0f) lp = ib + e;
-            }
-            float c = own;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, c, o);
-                if (lane >= o) c += y;
-            }
-            const unsigned h = __ballot_sync(0xffffffffu, c > tb);
-            int found = -1;
-            if (h) {
-                const int hl = __ffs(h) - 1;
-                if (lane == hl) {
-                    float cum = c - own;
-#pragma unroll
-                    for (int e = 0; e < kSub; ++e) {
-                        cum += wv[e];
-                        if (found < 0 && cum > tb) found = ib + e;
-                    }
-                    if (found < 0) found = lp;  // rounding inside the lane
+                    for (int jv = 0; jv < VEC; ++jv) w[jv] = id_w(xp[jv], 0.0f);
+                    v[jj] = tree_sum<VEC>(w);
                 }
-                found = __shfl_sync(0xffffffffu, found, hl);
+                // Lane l < 16 keeps block l = 4 g + (l & 3), reduced on lane (l & 3) * 8.
+                const float sg = __shfl_sync(0xffffffffu, block_sums4(v, lane), (lane & 3) << 3);
+                if ((lane >> 2) == g) bw = sg;
             }
-            if (found < 0) {  // rounding inside the block: its last id of positive weight
-                const int lastp = warp_max_int(lp);
-                found = lastp >= 0 ? lastp : bb * kPerLane;
+            if (lane >= kBlk) bw = 0.0f;
+        } else {
+            // The chosen piece's block weights, published with its result.
+            const uint64_t* bsrc = src + static_cast<size_t>(chosen) * kRecWords + kPartWords;
+            for (;;) {
+                uint64_t w = 0;
+                if (lane < kBlk) w = ld_volatile_u64(bsrc + lane);
+                if (__all_sync(0xffffffffu, lane >= kBlk || (w >> 32) == f)) {
+                    bw = lane < kBlk ? __uint_as_float(static_cast<uint32_t>(w)) : 0.0f;
+                    break;
+                }
+                if (global_timer_ns() - t0 > a.wait_ns) {
+                    if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+                    return false;
+                }
             }
-            token = lo + found;
         }
+        // The block: the first whose running weight passes the target, in
+        // the piece's own scale.
+        const float tpiece = soft ? tloc * ex2_approx(MC - mc_k) : tloc;
+        float incl = bw;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < kBlk && incl > tpiece);
+        int bb;
+        float tb;
+        if (hit) {
+            bb = __ffs(hit) - 1;
+            tb = tpiece - __shfl_sync(0xffffffffu, incl - bw, bb);
+        } else {  // rounding left the target past the piece: its last block of positive weight
+            bb = 31 - __clz(static_cast<int>(__ballot_sync(0xffffffffu, bw > 0.0f)) | 1);
+            tb = INFINITY;
+        }
+        // The block's ids: one vector of VEC ids per lane, in order.
+        const int v = 32 * bb + lane;
+        float xp[VEC], xq[VEC], wv[VEC];
+        const bool two = kind == 1;  // the residual's own weights need q_j
+        piece_vec_global<Elem>(h.gp, h.len, v, xp);
+        if (two) piece_vec_global<Elem>(h.gq, h.len, v, xq);
+        float own = 0.0f;
+        int lp = -1;
+#pragma unroll
+        for (int jv = 0; jv < VEC; ++jv) {
+            wv[jv] = id_w(xp[jv], two ? xq[jv] : 0.0f);
+            if (wv[jv] > 0.0f) lp = v * VEC + jv;
+        }
+        own = tree_sum<VEC>(wv);
+        float c = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, c, o);
+            if (lane >= o) c += y;
+        }
+        const unsigned hv = __ballot_sync(0xffffffffu, c > tb);
+        int found = -1;
+        if (hv) {
+            const int hl = __ffs(hv) - 1;
+            if (lane == hl) {
+                float cum = c - own;
+#pragma unroll
+                for (int jv = 0; jv < VEC; ++jv) {
+                    cum += wv[jv];
+                    if (found < 0 && cum > tb) found = v * VEC + jv;
+                }
+                if (found < 0) found = lp;  // rounding inside the lane
+            }
+            found = __shfl_sync(0xffffffffu, found, hl);
+        }
+        if (found < 0) {  // rounding inside the block: its last id of positive weight
+            const int lastp = warp_max_int(lp);
+            found = lastp >= 0 ? lastp : 32 * bb * VEC;
+        }
+        token = lo + found;
     }
     // Clear the tail's words for the next call (every piece has been read),
     // write the draw, and finalise the sequence with its last draw.
-    uint64_t* dst = a.tpart + static_cast<size_t>(slot) * np * kPartWords;
-    for (int kk = lane; kk < np; kk += 32) {
-        st_volatile_v2u64(dst + static_cast<size_t>(kk) * kPartWords, 0, 0);
-        st_volatile_v2u64(dst + static_cast<size_t>(kk) * kPartWords + 2, 0, 0);
-    }
+    uint64_t* dst = a.tpart + static_cast<size_t>(slot) * np * kRecWords;
+    for (int kk = lane; kk < np * kRecWords / 2; kk += 32) st_volatile_v2u64(dst + 2 * kk, 0, 0);
     if (lane < kTailWords) st_volatile_u64(a.tdesc + static_cast<size_t>(slot) * kTailWords + lane, 0);
     if (lane == 0) {
         a.tcount[slot] = 0;
@@ -1324,62 +1506,107 @@ __device__ bool select_draw(const VerifyArgs& a, unsigned char* sp, unsigned cha
     return true;
 }
 
-// A worker holds one decision ticket (a sequence index: sequences complete
-// roughly in index order, as the units are dealt) and one tail-piece ticket
-// (a queue slot and a piece), and serves whichever comes ready first.
 // =============================================================================
 // Draw kernel workers: every warp takes decision tickets (sequence indices),
-// then tail-piece tickets, and draws the tails whose last piece it finishes
+// then tail-piece tickets, two pieces in flight at a time, and draws the
+// tails whose last piece it finishes
 // =============================================================================
 
+// A warp's first decision ticket, with the part of its decision that needs
+// inputs only, taken before the stream kernel has completed.
+struct FirstDecision {
+    unsigned long long ticket;
+    DecPrep pre;
+};
+
 template <typename Elem>
-__device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, int lane) {
+__device__ __forceinline__ FirstDecision first_decision(const VerifyArgs& a, const Tables& tb, int lane) {
+    const unsigned long long ndec = tb.batch_bad ? 0ull : static_cast<unsigned long long>(a.num_seqs);
+    unsigned long long raw = ndec;
+    if (lane == 0 && ndec > 0) raw = atomicAdd(&a.ctl->dclaim, 1ull);
+    FirstDecision f;
+    f.ticket = __shfl_sync(0xffffffffu, raw, 0);
+    f.pre = DecPrep{0, 0.0f, 0.0f, 0.0f, 0, 0};
+    if (f.ticket < ndec && seq_lookup(a, tb, static_cast<int>(f.ticket)).ok)
+        f.pre = decide_prep<Elem>(a, tb, static_cast<int>(f.ticket), lane);
+    return f;
+}
+
+template <typename Elem, bool kGum>
+__device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecision& first, int lane) {
     const unsigned long long cap = static_cast<unsigned long long>(a.n_tail) * static_cast<unsigned long long>(a.np);
     const unsigned long long ndec = sm.tb.batch_bad ? 0ull : static_cast<unsigned long long>(a.num_seqs);
     const int n_valid = sm.tb.n_valid;
-    unsigned char* sp = sm.piece[wi][0];
-    unsigned char* sq = sm.piece[wi][1];
-    unsigned long long raw = 0, rawd = 0;
-    if (lane == 0) rawd = ndec > 0 ? atomicAdd(&a.ctl->dclaim, 1ull) : ndec;
-    unsigned long long dtk = __shfl_sync(0xffffffffu, rawd, 0);
     // Decisions first: every sequence is ready, its partials complete.
+    unsigned long long dtk = first.ticket, rawd = 0;
+    bool is_first = true;
     while (dtk < ndec) {
         if (lane == 0) rawd = atomicAdd(&a.ctl->dclaim, 1ull);
-        if (seq_lookup(a, sm.tb, static_cast<int>(dtk)).ok)
-            decide<Elem>(a, sm.tb, reinterpret_cast<float2*>(sp), static_cast<int>(dtk), lane);
+        if (seq_lookup(a, sm.tb, static_cast<int>(dtk)).ok) {
+            const DecPrep pre = is_first ? first.pre : decide_prep<Elem>(a, sm.tb, static_cast<int>(dtk), lane);
+            decide<Elem>(a, sm.tb, reinterpret_cast<float2*>(sm.buf[wi][0][0]), static_cast<int>(dtk), pre, lane);
+            // Every tail slot of the decision is reserved before it counts.
+            if (lane == 0) atomic_add_acq_rel(&a.ctl->ddone, 1);
+        }
+        is_first = false;
         dtk = __shfl_sync(0xffffffffu, rawd, 0);
     }
-    if (lane == 0) raw = cap > 0 ? atomicAdd(&a.ctl->claim, 1ull) : cap;
-    unsigned long long ticket = __shfl_sync(0xffffffffu, raw, 0);
+    // Two pieces in flight: hc in buffer bc (reduced next), hn in the other.
+    Held hc, hn;
+    int bc = 0;
+    uint32_t pc = 0u, pn = 0u;  // each buffer's barrier phase
+    claim_piece(a, hc, cap, lane);
+    claim_piece(a, hn, cap, lane);
     uint64_t t_mark = global_timer_ns();
     for (;;) {
-        const bool have = ticket < cap;
-        const int slot = have ? static_cast<int>(ticket / static_cast<unsigned long long>(a.np)) : 0;
-        const int k = have ? static_cast<int>(ticket % static_cast<unsigned long long>(a.np)) : 0;
-        // One round trip: the held ticket's descriptor and the completion count.
-        uint64_t w = 0;
-        if (have && lane < kTailWords) w = ld_volatile_u64(a.tdesc + static_cast<size_t>(slot) * kTailWords + lane);
-        int fin = 0;
-        if (lane == 31) fin = ld_volatile(&a.ctl->finalized);
-        const bool ready = have && __all_sync(0xffffffffu, lane >= kTailWords ||
-                                                               static_cast<uint32_t>(w >> 32) == static_cast<uint32_t>(slot) + 1u);
-        if (ready) {
-            const Tail t = decode_tail(w, lane);
-            // The next ticket is claimed now; its round trip overlaps the piece.
-            if (lane == 0) raw = atomicAdd(&a.ctl->claim, 1ull);
-            if (run_piece<Elem>(a, sp, sq, t, slot, k, lane) && !select_draw<Elem>(a, sp, sq, sm.ppart[wi], t, slot, lane))
-                return;
-            ticket = __shfl_sync(0xffffffffu, raw, 0);
-            t_mark = global_timer_ns();
-            continue;
+        if (hc.state == kHeldWait) try_start<Elem>(a, sm, wi, bc, hc, n_valid, lane);
+        if (hn.state == kHeldWait) try_start<Elem>(a, sm, wi, bc ^ 1, hn, n_valid, lane);
+        if (hc.state != kHeldLoad) {
+            if (hn.state == kHeldLoad || (hc.state == kHeldNone && hn.state != kHeldNone)) {
+                const Held tmp = hc;
+                hc = hn;
+                hn = tmp;
+                const uint32_t tp = pc;
+                pc = pn;
+                pn = tp;
+                bc ^= 1;
+                if (hc.state != kHeldLoad) continue;
+            } else if (hc.state == kHeldNone && hn.state == kHeldNone) {
+                return;  // no tickets left
+            } else {
+                if (global_timer_ns() - t_mark > a.wait_ns) {
+                    if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+                    return;
+                }
+                __nanosleep(64);
+                continue;
+            }
         }
-        fin = __shfl_sync(0xffffffffu, fin, 31);
-        if (fin >= n_valid) return;  // every sequence is final
-        if (global_timer_ns() - t_mark > a.wait_ns) {
+        // The current piece: wait for its copies; the next ticket for this
+        // buffer is claimed while the piece is reduced.
+        if (!__all_sync(0xffffffffu, mbar_wait_ns(&sm.bar[wi][bc], pc, kWaitNs))) {
             if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
             return;
         }
-        __nanosleep(64);
+        pc ^= 1u;
+        unsigned long long raw = 0;
+        if (lane == 0) raw = atomicAdd(&a.ctl->claim, 1ull);
+        const int cnt = reduce_piece<Elem, kGum>(a, sm.buf[wi][bc][0], sm.buf[wi][bc][1], hc, lane);
+        const Held done = hc;
+        // The freed buffer starts its next piece before the count comes
+        // back: the descriptor's round trip overlaps the count's.
+        take_ticket(a, hc, __shfl_sync(0xffffffffu, raw, 0), cap);
+        if (hc.state == kHeldWait) try_start<Elem>(a, sm, wi, bc, hc, n_valid, lane);
+        if (__shfl_sync(0xffffffffu, cnt, 0) == a.np - 1 && !select_draw<Elem, kGum>(a, sm, wi, done, lane)) return;
+        // The other buffer's piece goes next.
+        const Held tmp = hc;
+        hc = hn;
+        hn = tmp;
+        const uint32_t tp = pc;
+        pc = pn;
+        pn = tp;
+        bc ^= 1;
+        t_mark = global_timer_ns();
     }
 }
 
@@ -1388,17 +1615,23 @@ __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, int lane) {
 // =============================================================================
 
 // Both kernels' prologue: every CTA counts the valid sequences (the draw
-// kernel's exit condition) and checks that the offsets never decrease; small
-// batches keep the offsets, temperatures and tokens in shared memory.
+// kernel's exit condition) and the chunks to stream, and checks that the
+// offsets never decrease; small batches keep the offsets, temperatures and
+// tokens in shared memory.
 template <int kThreads>
 __device__ __forceinline__ bool load_tables(const VerifyArgs& a, Tables& tb, int tid) {
-    if (tid == 0) tb.n_valid = 0;
+    if (tid == 0) {
+        tb.n_valid = 0;
+        tb.units = 0;
+    }
     int nv = 0;
+    long long nu = 0;
     bool bad = false;
     const bool small = a.num_seqs <= kSmemSeqs;
     for (int i = tid; i < a.num_seqs; i += kThreads) {
         const SeqInfo s = seq_info(a.seq_offsets, a.temperature, i, a.total);
         nv += s.ok ? 1 : 0;
+        nu += s.ok ? static_cast<long long>(rows_of(s)) * a.nck : 0;
         const int end = __ldg(a.seq_offsets + i + 1);
         bad = bad || end < s.start;
         if (small) {
@@ -1411,6 +1644,7 @@ __device__ __forceinline__ bool load_tables(const VerifyArgs& a, Tables& tb, int
         for (int r = tid; r < a.total; r += kThreads) tb.tok[r] = __ldg(a.tokens + r);
     __syncthreads();
     if (nv) atomicAdd(&tb.n_valid, nv);
+    if (nu) atomicAdd(reinterpret_cast<unsigned long long*>(&tb.units), static_cast<unsigned long long>(nu));
     bad = __syncthreads_or(bad);
     if (tid == 0) {
         tb.batch_bad = bad;
@@ -1456,14 +1690,25 @@ __global__ void __launch_bounds__(kThreadsA, kVerifyCtasPerSm) stream_kernel(con
     }
 }
 
-template <typename Elem>
+// The draw kernel is compiled once per sampler: each launch carries only
+// the code its draws run, which keeps the instruction footprint small.
+template <typename Elem, bool kGum>
 __global__ void __launch_bounds__(kThreadsB, kCtasPerSmB) draw_kernel(const VerifyArgs a) {
     extern __shared__ unsigned char smem_raw[];
     SmemB& sm = *reinterpret_cast<SmemB*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_wait();  // the stream kernel has completed and its partials are visible
+    if (lane == 0) {
+        mbar_init(&sm.bar[warp][0], 1);
+        mbar_init(&sm.bar[warp][1], 1);
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+    // Inputs only until the wait: the batch layout and each warp's first
+    // decision's tokens, logits, uniforms and queue slot.
     load_tables<kThreadsB>(a, sm.tb, tid);
-    worker<Elem>(a, sm, warp, lane);
+    const FirstDecision first = first_decision<Elem>(a, sm.tb, lane);
+    pdl_wait();  // the stream kernel has completed and its partials are visible
+    worker<Elem, kGum>(a, sm, warp, first, lane);
     __syncthreads();
     if (tid == 0) {
         __threadfence();
@@ -1478,6 +1723,7 @@ __global__ void __launch_bounds__(kThreadsB, kCtasPerSmB) draw_kernel(const Veri
             a.ctl->tail_reserve = 0;
             a.ctl->claim = 0;
             a.ctl->dclaim = 0;
+            a.ctl->ddone = 0;
             a.ctl->finalized = 0;
             a.ctl->exited = 0;
         }
@@ -1493,8 +1739,8 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int grid, cudaStream_t stream) 
     cudaError_t err = cudaFuncSetAttribute(stream_kernel<Elem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem_a));
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(draw_kernel<Elem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem_b));
+    auto* draw = a.sampler == kSamplerGumbel ? draw_kernel<Elem, true> : draw_kernel<Elem, false>;
+    err = cudaFuncSetAttribute(draw, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_b));
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1515,7 +1761,7 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int grid, cudaStream_t stream) 
     cfg_b.gridDim = dim3(sms * kCtasPerSmB);
     cfg_b.blockDim = dim3(kThreadsB);
     cfg_b.dynamicSmemBytes = smem_b;
-    return cudaLaunchKernelEx(&cfg_b, draw_kernel<Elem>, a);
+    return cudaLaunchKernelEx(&cfg_b, draw, a);
 }
 
 }  // namespace
