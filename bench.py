@@ -2,9 +2,15 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c64]
 
-One step = isd_verify + isd_propose (every stage of the hot path) over one
-batch of synthetic logits resident in HBM: C=64 sequences, stride L=8,
-V=151936, bf16, T=1 by default.  Prints ONE JSON line (rank 0).
+One step = isd_verify_propose (every stage of the hot path: the verify
+decisions, the correction or bonus draws and the next stride's proposals, one
+call of two kernels) over one batch of synthetic logits resident in HBM: C=64
+sequences, stride L=8, V=151936, bf16, T=1 by default.  Prints ONE JSON line
+(rank 0).  At N=1 the line also carries, measured after the headline in the
+same run: the Gumbel-max sampler on the same batch, the other workloads
+(greedy, highconc, ragged) and the step under top-k 50 / top-p 0.95
+(`configs`), and the oracle's check of a sample of the headline's outputs
+(`parity`).
 
 Metric: verified stride-positions per second (sum of L_i per step / step
 time); the line also carries logit GB/s against the measured HBM peak.
@@ -30,7 +36,15 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "verified stride-positions/sec and logit GB/s (% of B300 HBM peak), C=64 V=151936"
+METRIC_BASE = "verified stride-positions/sec and logit GB/s (% of B300 HBM peak)"
+SUB_STEPS = 200  # timed steps of each sub-record
+
+
+def metric_for(batch):
+    """The metric's name with the workload's batch and vocabulary sizes."""
+    return f"{METRIC_BASE}, C={batch.num_seqs} V={batch.vocab}"
+
+
 UNIT = "positions/s"
 REFERENCE_BUDGET_S = 120.0  # seconds for a whole --impl reference run
 FALLBACK_HBM_GBS = 6400.0
@@ -389,7 +403,8 @@ def run_reference(args):
     desc = (f"{len(seqs)} of {batch.num_seqs} sequences" + (f", cut to {kp} positions" if kp < L0 else "")
             + f" ({positions} positions) per step, "
             + (f"verify+propose under top-k {FILTER_TOP_K} / top-p {FILTER_TOP_P}" if filtered else "verify+propose"))
-    metric = f"verified stride-positions/sec under top-k {FILTER_TOP_K} / top-p {FILTER_TOP_P}" if filtered else METRIC
+    metric = (f"verified stride-positions/sec under top-k {FILTER_TOP_K} / top-p {FILTER_TOP_P}, "
+              f"C={batch.num_seqs} V={batch.vocab}") if filtered else metric_for(batch)
     line = {"impl": "reference", "metric": metric, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -419,6 +434,131 @@ def slowest_rank(ms, device, distributed):
 def job_throughput(positions_per_rank, world, steps, ms):
     """Whole-job positions per second: every replica verifies its own batch."""
     return positions_per_rank * world * steps / (ms / 1e3)
+
+
+def time_calls(call, flush, stream, K):
+    """K calls, each bracketed by its own events on `stream`, the L2 flushed
+    before each outside them: the calls' durations in ms."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def sub_record(batch, ms, kernel_bytes, peak, accept_len=None):
+    """One workload's figures: step time, positions per second, the step's
+    algorithmic logit bytes over its average duration against the peak."""
+    avg_s = sum(ms) / len(ms) / 1e3
+    rec = {"workload": f"{batch.name}: {batch.meta['description']}", "step_us": 1e3 * statistics.median(ms),
+           "step_us_best": 1e3 * min(ms), "positions_per_s": batch.total / avg_s,
+           "roofline": {"achieved_gbs": kernel_bytes / avg_s / 1e9, "frac": kernel_bytes / avg_s / 1e9 / peak,
+                        "algorithmic_bytes": kernel_bytes},
+           "steps": len(ms)}
+    if accept_len is not None:
+        rec["accepted_share"] = accepted_share(batch, accept_len)
+    return rec
+
+
+def fused_sub_records(dev, stream, flush, peak, K, head_batch):
+    """The Gumbel-max sampler on the headline batch, then the other workloads
+    through the same fused call (inverse-CDF draws), each timed as the
+    headline (K steps, L2 flushed between them)."""
+    import torch
+    from speculative_verify_accept_02_b300 import isd_verify_propose, isd_verify_propose_workspace_bytes, workloads
+    from speculative_verify_accept_02_b300.api import workspace
+    out = {}
+    for key, name, sampler in (("gumbel", None, "gumbel"), ("greedy", "greedy", "icdf"),
+                               ("highconc", "highconc", "icdf"), ("ragged", "ragged", "icdf")):
+        b = head_batch if name is None else workloads.make(name, device=dev)
+        ws = workspace(isd_verify_propose_workspace_bytes(b.num_seqs, b.total, b.vocab, b.dtype), dev)
+        res = {}
+
+        def call():
+            res["out"] = isd_verify_propose(b.p, b.q, b.tokens, b.qnew, b.seq_offsets, b.temperature, b.seed,
+                                            b.offset, vocab=b.vocab, total=b.total, ws=ws, stream=stream,
+                                            sampler=sampler)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        v, pr = res["out"]
+        acc = v.accept_len.cpu().tolist()
+        vb, pb = algorithmic_bytes(b, acc, pr.valid.cpu().tolist())
+        rec = sub_record(b, time_calls(call, flush, stream, K), vb + pb, peak, acc)
+        rec["step"] = f"isd_verify_propose ({'Gumbel-max' if sampler == 'gumbel' else 'inverse-CDF'} draws)"
+        out[key] = rec
+        del b, ws, res
+        torch.cuda.empty_cache()
+    return out
+
+
+def filtered_sub_record(dev, stream, flush, peak, K, batch):
+    """The step under top-k 50 / top-p 0.95 on the headline batch:
+    isd_verify_filtered then isd_propose_filtered; the roofline is the verify
+    call's (every p and q row streamed once)."""
+    import torch
+    from speculative_verify_accept_02_b300 import (isd_propose_filtered, isd_propose_filtered_workspace_bytes,
+                                                   isd_verify_filtered, isd_verify_filtered_workspace_bytes)
+    from speculative_verify_accept_02_b300.api import workspace
+    C, total, V = batch.num_seqs, batch.total, batch.vocab
+    k, tp = FILTER_TOP_K, FILTER_TOP_P
+    vws = workspace(isd_verify_filtered_workspace_bytes(C, total, k), dev)
+    pws = workspace(isd_propose_filtered_workspace_bytes(C, total, k), dev)
+    res = {}
+
+    def verify():
+        res["v"] = isd_verify_filtered(batch.p, batch.q, batch.tokens, batch.seq_offsets, batch.temperature,
+                                       batch.seed, batch.offset, top_k=k, top_p=tp, vocab=V, total=total, ws=vws,
+                                       stream=stream)
+
+    def step():
+        verify()
+        isd_propose_filtered(batch.qnew, batch.seq_offsets, batch.temperature, batch.seed, batch.offset,
+                             res["v"].accept_len, top_k=k, top_p=tp, vocab=V, total=total, ws=pws, stream=stream)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    acc = res["v"].accept_len.cpu().tolist()
+    vbytes = filtered_verify_bytes(batch)
+    rec = sub_record(batch, time_calls(step, flush, stream, K), vbytes, peak, acc)
+    vms = time_calls(verify, flush, stream, K)
+    avg_s = sum(vms) / len(vms) / 1e3
+    rec["roofline"] = {"achieved_gbs": vbytes / avg_s / 1e9, "frac": vbytes / avg_s / 1e9 / peak,
+                       "algorithmic_bytes": vbytes, "kernel": "isd_verify_filtered (top-k lists, then decisions)",
+                       "avg_launch_us": avg_s * 1e6}
+    rec["step"] = f"isd_verify_filtered + isd_propose_filtered, top-k {k}, top-p {tp}"
+    return rec
+
+
+def oracle_parity(batch, vout, pout):
+    """The oracle's check of a sample of the headline's outputs (the first
+    sequence, the last four and eight at random), by the comparison the GPU
+    tests make: the counts of compared sequences and exempted decisions."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from parity import Report, compare_propose, compare_verify
+    h = _host_inputs(batch)
+    C = batch.num_seqs
+    rng = np.random.default_rng(11)
+    seqs = sorted(set([0] + list(range(max(0, C - 4), C)) + list(rng.choice(C, size=min(C, 8), replace=False))))
+    gv = dict(accept_len=vout.accept_len.cpu().numpy(), out_tokens=vout.out_tokens.cpu().numpy(),
+              ratio=vout.ratio.cpu().numpy(), alpha=vout.alpha.cpu().numpy())
+    gp = dict(proposals=pout.proposals.cpu().numpy(), valid=pout.valid.cpu().numpy())
+    ov = oracle.verify(h["p"], h["q"], batch.vocab, h["tokens"], h["offs"], h["temp"], batch.seed, batch.offset,
+                       seqs=seqs)
+    rep = compare_verify(ov, gv, h["offs"], seqs=seqs, report=Report())
+    agree = [i for i in seqs if ov["accept_len"][i] == gv["accept_len"][i]]
+    op = oracle.propose(h["qnew"], batch.vocab, h["offs"], h["temp"], batch.seed, batch.offset,
+                        accept_len=gv["accept_len"], seqs=agree)
+    compare_propose(op, gp, h["offs"], seqs=agree, report=rep)
+    out = {k: v for k, v in rep.summary().items() if k != "cut_skips"}
+    out["failures"] = len(rep.failures)
+    out["sample"] = [int(i) for i in seqs]
+    return out
 
 
 def run_ours(args):
@@ -549,7 +689,15 @@ def run_ours(args):
     if rank != 0:
         dist.destroy_process_group()
         return
+    configs = None
+    if not distributed and fused and args.workload == "c64":
+        # The other figures of the record, after the headline: the Gumbel-max
+        # sampler, the other workloads, the filtered step.
+        sub_k = min(K, SUB_STEPS)
+        configs = fused_sub_records(dev, stream, flush, peak, sub_k, batch)
+        configs["filtered"] = filtered_sub_record(dev, stream, flush, peak, sub_k, batch)
     cpu = None
+    parity = None
     if not distributed:  # the CPU baseline is taken at N=1 only
         rate, threads, reps, el, pos = time_oracle(batch, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -560,25 +708,31 @@ def run_ours(args):
         cpu["single_core"] = {"value": rate1, "unit": UNIT, "cores": 1,
                               "sample": f"{len(one)} sequences ({pos1} positions) verify+propose, "
                                         f"{reps1} repetition(s) in {el1:.1f} s"}
+        # the same oracle checks a sample of the headline's outputs (the timed
+        # steps' inputs, seed and offset)
+        parity = oracle_parity(batch, vout, pout)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "metric": metric_for(batch), "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": workload_config(batch, {
             "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write between timed steps",
-            "parallelism": f"replicas x{world}", "step": "isd_verify_propose (one launch)" if fused else "isd_verify + isd_propose",
+            "parallelism": f"replicas x{world}", "step": "isd_verify_propose (one call: stream kernel, draw kernel)" if fused else "isd_verify + isd_propose",
             "accepted_share": accepted_share(batch, acc_host)}),
         "logit_gbs": logit_gbs, "hbm_frac": logit_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
-                     "kernel": ("verify_kernel (isd_verify_propose: one persistent launch)" if fused
-                                else "verify_kernel (isd_verify: one persistent launch)"),
+                     "kernel": ("isd_verify_propose: stream_kernel, then draw_kernel launched behind it"
+                                if fused else "isd_verify: stream_kernel, then draw_kernel launched behind it"),
                      "algorithmic_bytes": kernel_bytes, "reread_bytes": rbytes,
                      "peak_source": f"{peak_kind} hbm_gbs", "avg_launch_us": verify_avg_s * 1e6},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "step_us": {"median": 1e3 * statistics.median(per_step_ms), "best": 1e3 * min(per_step_ms)},
-        "gpu_launches": (1 if fused else 2) * K,  # verify_kernel (+ propose_kernel) per step
+        "gpu_launches": (2 if fused else 3) * K,  # stream + draw kernels (+ propose_kernel) per step
+        "configs": configs,
+        "parity": parity,
         "clocks": sampler.summary(),
         "wall_s_timed": t_wall,
     }
@@ -758,7 +912,8 @@ def run_filtered(args):
     torch.cuda.synchronize(dev)
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e) / E
     line = {
-        "metric": f"verified stride-positions/sec under top-k {k} / top-p {tp}", "value": total / (step_ms / 1e3),
+        "metric": f"verified stride-positions/sec under top-k {k} / top-p {tp}, C={C} V={V}",
+        "value": total / (step_ms / 1e3),
         "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(batch, {"top_k": k, "top_p": tp, "kept_ids_arithmetic": "f64",

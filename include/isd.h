@@ -253,24 +253,26 @@ ISD_API isd_status isd_alpha(const float* ratio, const int32_t* seq_offsets, int
  *
  * Arguments, layout, outputs and results are those of isd_verify, without
  * the workspace.  The scratch is a fixed array of ISD_NOALLOC_SCRATCH_BYTES
- * inside the library, reserved on every device that loads the library until
- * the process exits.  The call allocates nothing: it clears the part of the
- * array the batch needs (cudaMemsetAsync on `stream`) and then runs
- * isd_verify's kernels on it.
+ * inside the library, reserved in every CUDA context that loads the library
+ * until that context is destroyed.  The call allocates nothing: every
+ * argument check of isd_verify comes first (a refused call touches neither
+ * the array nor the stream), then it clears the part of the array the batch
+ * needs (cudaMemsetAsync on `stream`) and runs isd_verify's kernels on it.
  *
  * Limits and rules:
  *   - a batch whose isd_verify_workspace_bytes() exceeds
  *     ISD_NOALLOC_SCRATCH_BYTES returns ISD_ERR_WORKSPACE and launches
- *     nothing (isd_verify_workspace_bytes() gives any batch's need; bf16
- *     rows of V = 151936 at C = 256, L = 16 need about a third of it);
- *   - the first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture;
+ *     nothing (isd_verify_workspace_bytes() gives any batch's need: rows of
+ *     V = 151936 at C = 256, L = 16 need 2,231,296 bytes in bf16, about 27 %
+ *     of the array, and 4,336,640 bytes in fp32, about 52 %);
+ *   - the array's device address is looked up once per CUDA context, on the
+ *     first call made in it; make that first call before any stream capture;
  *   - every call on a device shares the one array: two calls that can
  *     overlap on the GPU (different streams without an event between them)
  *     race and give wrong results.  Order them, or use isd_verify with
  *     workspaces of your own.
  */
-#define ISD_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define ISD_NOALLOC_SCRATCH_BYTES (8u << 20)
 ISD_API isd_status isd_verify_noalloc(const void* p_logits, int64_t ld_p, const void* q_logits, int64_t ld_q,
                                       isd_dtype dtype, int vocab, const int32_t* tokens,
                                       const int32_t* seq_offsets, int num_seqs, int total_positions,

@@ -32,10 +32,13 @@ ISD_API isd_status isd_decision_uniforms(uint64_t seed, uint64_t offset, const u
  * isd_debug_verify_stall — isd_verify_propose with one sequence's decision
  * held back, to test the verify kernel's bounded waits without a GPU fault
  * (failure detection).  The decision of sequence `stall_seq` writes its
- * outputs but publishes none of its draws and never marks the sequence
- * final, so the kernel's waits on other CTAs' work (the worker warps'
- * polls) run out after `wait_ns` nanoseconds of the global timer instead of
- * the usual 4 s.  The call then ends as a timeout does: the workspace's
+ * outputs and reserves the queue slot of its correction or bonus draw but
+ * never publishes that draw's descriptor, so the worker warps holding the
+ * draw's piece tickets poll for it until their bound on waits for other
+ * CTAs' work runs out: `wait_ns` nanoseconds of the global timer instead of
+ * the usual 4 s.  The hook takes effect on a sequence with T > 0 (a T = 0
+ * sequence that does not accept its whole stride has no draw to hold back).
+ * The call then ends as a timeout does: the workspace's
  * error word is set, every accept_len reads -2 and every valid 0, and the
  * workspace must be zero-filled again before its next use (include/isd.h,
  * Workspace).  Only waits on other CTAs' work can run out this way: every

@@ -70,7 +70,7 @@ SIGNATURES = {
 }
 
 # Size of the library's built-in scratch array (ISD_NOALLOC_SCRATCH_BYTES).
-NOALLOC_SCRATCH_BYTES = 4 << 20
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class IsdError(RuntimeError):

@@ -8,7 +8,8 @@
 // kept probabilities are renormalised over the kept ids, so the row's full
 // softmax normaliser cancels.  Each call therefore runs two kernels:
 //   topk_rows_kernel  one CTA per row streams the row once with 16-byte
-//                     loads; every warp keeps a sorted list of its 64 best
+//                     loads, four in flight per lane; every warp keeps a
+//                     sorted list of its 64 best
 //                     (logit, id) pairs in registers (two per lane) and
 //                     inserts the rare candidate that beats its k-th entry;
 //                     warp 0 merges the eight lists and writes the row's k
@@ -37,6 +38,7 @@ static_assert(kListMax == 64, "a warp list holds two entries per lane");
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkCtasPerSm = 4;
+constexpr int kInFlight = 4;  // 16-byte loads in flight per lane of topk_rows_kernel
 constexpr int kSeqThreads = 256;
 constexpr int kSeqWarps = kSeqThreads / 32;
 constexpr double kLog2eD = 1.4426950408889634;  // log2(e)
@@ -151,14 +153,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(TopkArgs a) {
         float tv = -INFINITY;
         int ti = INT_MAX;
         const uint4* body = reinterpret_cast<const uint4*>(row + static_cast<size_t>(head) * E);
-        for (int g0 = warp * 32; g0 < nvec; g0 += kTopkThreads) {
-            const int g = g0 + lane;
-            const bool has = g < nvec;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if (has) w = __ldg(body + g);
+        // kInFlight vectors per lane are loaded ahead of the one being
+        // offered: each slot is refilled with the vector kInFlight steps on
+        // as soon as it is taken.
+        uint4 ahead[kInFlight];
 #pragma unroll
-            for (int j = 0; j < VEC; ++j)
-                offer(wl, vec_elem<E>(w, j), head + g * VEC + j, has, k, tv, ti, lane);
+        for (int d = 0; d < kInFlight; ++d) {
+            const int g = warp * 32 + d * kTopkThreads + lane;
+            ahead[d] = g < nvec ? __ldg(body + g) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int g0 = warp * 32; g0 < nvec; g0 += kInFlight * kTopkThreads) {
+#pragma unroll
+            for (int d = 0; d < kInFlight; ++d) {
+                const int gs = g0 + d * kTopkThreads;  // the warp's first vector of this step
+                if (gs >= nvec) break;                // the same for every lane
+                const int g = gs + lane;
+                const bool has = g < nvec;
+                const uint4 w = ahead[d];
+                const int gn = g + kInFlight * kTopkThreads;
+                ahead[d] = gn < nvec ? __ldg(body + gn) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    offer(wl, vec_elem<E>(w, j), head + g * VEC + j, has, k, tv, ti, lane);
+            }
         }
         if (warp == 0) {  // the unaligned head and the tail: fewer than 2 * VEC ids
             const int e = lane < head ? lane : tail0 + (lane - head);

@@ -300,9 +300,11 @@ __device__ __forceinline__ DecPrep decide_prep(const VerifyArgs& a, const Tables
     d.x = mine ? (a.total <= kSmemToks ? tb.tok[r] : __ldg(a.tokens + r)) : 0;
     d.bad = __any_sync(0xffffffffu, mine && (d.x < 0 || d.x >= a.vocab));
     // A T > 0 sequence always makes one draw after its decision: its queue
-    // slot is reserved now, so that the round trip overlaps the loads below.
+    // slot is reserved now, so that the round trip overlaps the loads below
+    // (the check hook's held-back decision reserves it too, and the workers
+    // that take its pieces wait for a descriptor that never comes).
     d.tslot = 0;
-    if (T > 0.0f && lane == 0 && !d.bad && i != a.stall_seq) d.tslot = atomicAdd(&a.ctl->tail_reserve, 1);
+    if (T > 0.0f && lane == 0 && !d.bad) d.tslot = atomicAdd(&a.ctl->tail_reserve, 1);
     d.zp = 0.0f;
     d.zq = 0.0f;
     if (mine && T > 0.0f && !d.bad) {
@@ -428,7 +430,7 @@ __device__ __noinline__ void decide(const VerifyArgs& a, const Tables& tb, float
         }
         if (lane == 0) a.out_tokens[s.start + i + na] = tok;
     }
-    if (stall) return;  // check hook: nothing is published, the sequence never completes
+    if (stall) return;  // check hook: the reserved draw is never published, its pieces' workers wait
     // Draws left: the correction or bonus (T > 0), then one per proposal row.
     const int n_tok = T > 0.0f ? 1 : 0;
     const int n_prop = props ? L : 0;
@@ -1586,6 +1588,7 @@ __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecisi
         // buffer is claimed while the piece is reduced.
         if (!__all_sync(0xffffffffu, mbar_wait_ns(&sm.bar[wi][bc], pc, kWaitNs))) {
             if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+            if (hn.state == kHeldLoad) mbar_wait_ns(&sm.bar[wi][bc ^ 1], pn, kWaitNs);
             return;
         }
         pc ^= 1u;
@@ -1597,7 +1600,13 @@ __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecisi
         // back: the descriptor's round trip overlaps the count's.
         take_ticket(a, hc, __shfl_sync(0xffffffffu, raw, 0), cap);
         if (hc.state == kHeldWait) try_start<Elem>(a, sm, wi, bc, hc, n_valid, lane);
-        if (__shfl_sync(0xffffffffu, cnt, 0) == a.np - 1 && !select_draw<Elem, kGum>(a, sm, wi, done, lane)) return;
+        if (__shfl_sync(0xffffffffu, cnt, 0) == a.np - 1 && !select_draw<Elem, kGum>(a, sm, wi, done, lane)) {
+            // Leaving on an error: this warp's own copies land first, so that
+            // none is still writing into the CTA's shared memory at exit.
+            if (hc.state == kHeldLoad) mbar_wait_ns(&sm.bar[wi][bc], pc, kWaitNs);
+            if (hn.state == kHeldLoad) mbar_wait_ns(&sm.bar[wi][bc ^ 1], pn, kWaitNs);
+            return;
+        }
         // The other buffer's piece goes next.
         const Held tmp = hc;
         hc = hn;

@@ -17,9 +17,14 @@ RTOL = 1e-4
 
 @dataclass
 class Report:
+    """What a comparison covered: the sequences compared, the decisions
+    exempted for an oracle margin below MARGIN (accept tests, draws), and the
+    sequences left out of a filtered comparison because the oracle's top-p
+    cut lies within its own rounding of moving (cut_skips)."""
     sequences: int = 0
     exempt_accept: int = 0
     exempt_token: int = 0
+    cut_skips: int = 0
     failures: list = field(default_factory=list)
 
     def fail(self, msg):
@@ -27,6 +32,18 @@ class Report:
 
     def check(self):
         assert not self.failures, "\n".join(self.failures[:20])
+
+    def summary(self):
+        return {"compared": self.sequences, "exempt_accept": self.exempt_accept,
+                "exempt_token": self.exempt_token, "cut_skips": self.cut_skips}
+
+    def merge(self, other):
+        self.sequences += other.sequences
+        self.exempt_accept += other.exempt_accept
+        self.exempt_token += other.exempt_token
+        self.cut_skips += other.cut_skips
+        self.failures += other.failures
+        return self
 
 
 def _close(a, b, rtol=RTOL):

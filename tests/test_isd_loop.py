@@ -152,6 +152,35 @@ def test_loop_kv_on_cuda():
     _kv_loop(CudaBackend(), 4096, "cuda")
 
 
+def _filtered_extremes(backend, device):
+    """Closed forms of the loop under the evaluation setting's filters (see
+    test_loop_under_filters_on_oracle): top-10 of a 32-id support, and top-50
+    then top-p 0.95 of a 64-id support (both filtered rows uniform on the
+    same 48 ids, the cut 0.01 from moving).  Returns the loop statistics."""
+    n, C, S = 4, 3, 7
+    out = []
+    for filters, support in (((10, 1.0), 32), ((50, 0.95), 64)):
+        for alpha, all_pass in ((0.6, True), (0.4, False)):
+            model = TableModel(256, alpha, entries=5, support=support, seed=8, device=device)
+            st = ISDLoop(model, C, n, backend, filters=filters).run(S)
+            if all_pass:
+                assert st.per_seq_tokens == [1 + n * (S - 1)] * C and st.accepted == st.verified
+            else:
+                assert st.per_seq_tokens == [S] * C and st.accepted == 0
+            out.append((st.per_seq_tokens, st.accepted, st.rejected, st.verified, st.forwards))
+    return out
+
+
+@pytest.mark.gpu
+def test_loop_under_filters_on_cuda():
+    """The decode loop on the CUDA backend under top-k / top-p (Summary §4.1:
+    top-k 50, top-p 0.95), through isd_verify_filtered and
+    isd_propose_filtered: the closed forms hold, and the step statistics equal
+    the oracle backend's."""
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    assert _filtered_extremes(CudaBackend(), "cuda") == _filtered_extremes(OracleBackend(), "cpu")
+
+
 def test_loop_under_filters_on_oracle():
     """The evaluation setting's filters change what the table model accepts,
     exactly: q is uniform on a support S and p puts alpha/s on S, (1-alpha)/s

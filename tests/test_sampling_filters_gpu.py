@@ -75,6 +75,7 @@ def compare_step(batch, seed, offset, top_k, top_p, rep):
     tp = f32(top_p)
     ov = oracle.verify_filtered(h["p"], h["q"], V, h["tokens"], h["offs"], h["temp"], seed, offset, top_k, tp)
     keep = [i for i in range(batch.num_seqs) if ov["cut_margin"][i] >= CUT_MARGIN]
+    rep.cut_skips += batch.num_seqs - len(keep)
     compare_verify(ov, gv, h["offs"], seqs=keep, report=rep)
     op = oracle.propose_filtered(h["qnew"], V, h["offs"], h["temp"], seed, offset, top_k, tp,
                                  accept_len=gv["accept_len"])

@@ -39,6 +39,20 @@ def test_rejects_a_batch_larger_than_its_array():
     assert status == _lib.ISD_ERR_WORKSPACE
     assert lib.isd_verify_noalloc(fake, V, fake, V, 0, V, fake, fake, 0, 0, fake, 0, 0,
                                   fake, fake, fake, fake, None) == _lib.ISD_OK
+    # Every argument check comes before the array is touched: a refused call
+    # returns its status and queues nothing (here no CUDA call is made at all).
+    C_, total = 4, 16
+    args = [fake, V, fake, V, 0, V, fake, fake, C_, total, fake, 0, 0, fake, fake, fake, fake, None]
+    for i in (0, 2, 6, 7, 10, 13, 14, 15, 16):  # p, q, tokens, offsets, temperature and the four outputs
+        bad = list(args)
+        bad[i] = None
+        assert lib.isd_verify_noalloc(*bad) == _lib.ISD_ERR_INVALID_ARG, i
+    bad = list(args)
+    bad[1] = V - 1                                 # ld_p below the vocabulary
+    assert lib.isd_verify_noalloc(*bad) == _lib.ISD_ERR_INVALID_ARG
+    bad = list(args)
+    bad[0] = fake + 2                              # p not on a 16-byte boundary
+    assert lib.isd_verify_noalloc(*bad) == _lib.ISD_ERR_UNSUPPORTED
 
 
 @pytest.mark.gpu
