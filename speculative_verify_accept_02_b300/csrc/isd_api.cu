@@ -23,7 +23,7 @@ bool dtype_ok(int dtype) { return dtype == ISD_DTYPE_BF16 || dtype == ISD_DTYPE_
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Workspace of isd_verify (stream kernel, then draw kernel):
-//   [control block | per-sequence draw counts | per-tail piece counts |
+//   [control block | per-sequence draw counts | per-tail piece counts | draw queue |
 //    tail descriptors | tail piece records | per (row slot, chunk) partials]
 struct VerifyPlan {
     int ck, nck, ps, np;
@@ -40,7 +40,7 @@ VerifyPlan verify_plan(int vocab, int esz) {
 }
 
 struct VerifyLayout {
-    size_t ctl, seq_done, tcount, tdesc, tpart, part, bytes;
+    size_t ctl, seq_done, tcount, dqueue, tdesc, tpart, part, bytes;
 };
 
 // Tails: one per sequence (its correction or bonus), plus one per qnew row
@@ -55,6 +55,8 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl, bool f
     l.seq_done = off;
     off = align_up(off + sizeof(int) * C);
     l.tcount = off;
+    off = align_up(off + sizeof(int) * NT);
+    l.dqueue = off;
     off = align_up(off + sizeof(int) * NT);
     l.tdesc = off;
     off = align_up(off + sizeof(uint64_t) * isd::kTailWords * NT);
@@ -180,6 +182,7 @@ isd_status verify_run(const void* p_logits, int64_t ld_p, const void* q_logits, 
     va.tdesc = reinterpret_cast<uint64_t*>(ws + lay.tdesc);
     va.tpart = reinterpret_cast<uint64_t*>(ws + lay.tpart);
     va.tcount = reinterpret_cast<int*>(ws + lay.tcount);
+    va.dqueue = reinterpret_cast<int*>(ws + lay.dqueue);
     va.part = reinterpret_cast<float2*>(ws + lay.part);
     va.fused = o.fused ? 1 : 0;
     va.qnew = static_cast<const char*>(o.qnew);

@@ -77,6 +77,8 @@ struct VerifyCtl {
     alignas(128) unsigned long long dclaim; // decision tickets (sequence indices) handed to workers
     alignas(128) int ddone;                 // decisions made (their tail slots reserved)
     alignas(128) int finalized;             // sequences whose outputs are complete
+    alignas(128) int draw_tail;             // tails queued for their draw
+    alignas(128) int draw_claim;            // queued draws handed to drawing warps
     alignas(128) int exited;                // CTAs of the draw kernel that have finished
 };
 
@@ -134,6 +136,7 @@ struct VerifyArgs {
     uint64_t* tdesc;   // [n_tail][kTailWords] flagged descriptor words
     uint64_t* tpart;   // [n_tail][np][20] flagged piece records: 4 result words, 16 block weights
     int* tcount;       // [n_tail] pieces finished
+    int* dqueue;       // [n_tail] tails whose pieces are all finished, in completion order (slot + 1; 0: not yet)
     float2* part;      // [2 * total][nck] per (row slot, chunk) partials
     // The fused call (isd_verify_propose): the next stride's proposals of the
     // sequences that accept their whole stride, drawn from qnew rows.

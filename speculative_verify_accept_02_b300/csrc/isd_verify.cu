@@ -1534,6 +1534,64 @@ __device__ __forceinline__ FirstDecision first_decision(const VerifyArgs& a, con
     return f;
 }
 
+// A warp with no piece tickets left draws queued tails: it claims queue
+// positions in order and waits for each to be filled (every tail's pieces
+// are held by warps that finish them without waiting on a draw).  It stops
+// once every sequence is final, or at a claim past the queue's capacity.
+template <typename Elem, bool kGum>
+__device__ void drawer(const VerifyArgs& a, SmemB& sm, int wi, int n_valid, int lane) {
+    for (;;) {
+        int raw = 0;
+        if (lane == 0) raw = atomicAdd(&a.ctl->draw_claim, 1);
+        const int dk = __shfl_sync(0xffffffffu, raw, 0);
+        if (dk >= a.n_tail) return;
+        const uint64_t t0 = global_timer_ns();
+        int slot = -1;
+        for (;;) {
+            int v = 0, fin = 0;
+            if (lane == 0) {
+                v = ld_volatile(a.dqueue + dk);
+                fin = ld_volatile(&a.ctl->finalized);
+            }
+            v = __shfl_sync(0xffffffffu, v, 0);
+            if (v != 0) {
+                slot = v - 1;
+                break;
+            }
+            if (__shfl_sync(0xffffffffu, fin, 0) >= n_valid) return;  // every draw is made
+            if (global_timer_ns() - t0 > a.wait_ns) {
+                if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+                return;
+            }
+            __nanosleep(128);
+        }
+        if (lane == 0) a.dqueue[dk] = 0;  // zero again for the next call
+        // The tail's descriptor (published before any of its pieces ran).
+        uint64_t w = 0;
+        for (;;) {
+            if (lane < kTailWords) w = ld_volatile_u64(a.tdesc + static_cast<size_t>(slot) * kTailWords + lane);
+            if (__all_sync(0xffffffffu, lane >= kTailWords ||
+                                            static_cast<uint32_t>(w >> 32) == static_cast<uint32_t>(slot) + 1u))
+                break;
+            if (global_timer_ns() - t0 > a.wait_ns) {
+                if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
+                return;
+            }
+        }
+        Held hd;
+        hd.ticket = 0;
+        hd.state = kHeldNone;
+        hd.slot = slot;
+        hd.k = 0;
+        hd.t = decode_tail(w, lane);
+        hd.gp = nullptr;
+        hd.gq = nullptr;
+        hd.len = 0;
+        hd.nbytes = 0;
+        if (!select_draw<Elem, kGum>(a, sm, wi, hd, lane)) return;
+    }
+}
+
 template <typename Elem, bool kGum>
 __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecision& first, int lane) {
     const unsigned long long cap = static_cast<unsigned long long>(a.n_tail) * static_cast<unsigned long long>(a.np);
@@ -1574,7 +1632,8 @@ __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecisi
                 bc ^= 1;
                 if (hc.state != kHeldLoad) continue;
             } else if (hc.state == kHeldNone && hn.state == kHeldNone) {
-                return;  // no tickets left
+                drawer<Elem, kGum>(a, sm, wi, n_valid, lane);  // no piece tickets left: draw queued tails
+                return;
             } else {
                 if (global_timer_ns() - t_mark > a.wait_ns) {
                     if (lane == 0) atomicOr(&a.ctl->err, kErrWaitTimeout);
@@ -1600,13 +1659,10 @@ __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecisi
         // back: the descriptor's round trip overlaps the count's.
         take_ticket(a, hc, __shfl_sync(0xffffffffu, raw, 0), cap);
         if (hc.state == kHeldWait) try_start<Elem>(a, sm, wi, bc, hc, n_valid, lane);
-        if (__shfl_sync(0xffffffffu, cnt, 0) == a.np - 1 && !select_draw<Elem, kGum>(a, sm, wi, done, lane)) {
-            // Leaving on an error: this warp's own copies land first, so that
-            // none is still writing into the CTA's shared memory at exit.
-            if (hc.state == kHeldLoad) mbar_wait_ns(&sm.bar[wi][bc], pc, kWaitNs);
-            if (hn.state == kHeldLoad) mbar_wait_ns(&sm.bar[wi][bc ^ 1], pn, kWaitNs);
-            return;
-        }
+        // A tail whose pieces are all finished is queued for its draw: the
+        // warps that run out of pieces take the draws, so that no piece
+        // waits behind one.
+        if (lane == 0 && cnt == a.np - 1) st_volatile(a.dqueue + atomicAdd(&a.ctl->draw_tail, 1), done.slot + 1);
         // The other buffer's piece goes next.
         const Held tmp = hc;
         hc = hn;
@@ -1734,6 +1790,8 @@ __global__ void __launch_bounds__(kThreadsB, kCtasPerSmB) draw_kernel(const Veri
             a.ctl->dclaim = 0;
             a.ctl->ddone = 0;
             a.ctl->finalized = 0;
+            a.ctl->draw_tail = 0;
+            a.ctl->draw_claim = 0;
             a.ctl->exited = 0;
         }
     }
