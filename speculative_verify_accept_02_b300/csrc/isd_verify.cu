@@ -277,8 +277,8 @@ __device__ __forceinline__ void publish_tail(const VerifyArgs& a, int slot, cons
 
 // What a decision reads from its inputs alone (not from the stream kernel's
 // partials): the proposed tokens, their logits, the acceptance uniforms, and
-// the reservation of the sequence's queue slot.  A warp's first decision
-// takes these before the stream kernel has completed.
+// the reservation of the sequence's queue slot.  Its loads are issued before
+// the partials are staged, so that the two round trips overlap.
 struct DecPrep {
     int x;       // this lane's proposed token x_{lane+1}
     float zp;    // its logit in p_{lane+1}
@@ -1514,11 +1514,10 @@ __device__ __noinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi,
 // tails whose last piece it finishes
 // =============================================================================
 
-// A warp's first decision ticket, with the part of its decision that needs
-// inputs only, taken before the stream kernel has completed.
+// A warp's first decision ticket, claimed before the stream kernel has
+// completed (the control block is the previous call's, zeroed).
 struct FirstDecision {
     unsigned long long ticket;
-    DecPrep pre;
 };
 
 template <typename Elem>
@@ -1528,9 +1527,6 @@ __device__ __forceinline__ FirstDecision first_decision(const VerifyArgs& a, con
     if (lane == 0 && ndec > 0) raw = atomicAdd(&a.ctl->dclaim, 1ull);
     FirstDecision f;
     f.ticket = __shfl_sync(0xffffffffu, raw, 0);
-    f.pre = DecPrep{0, 0.0f, 0.0f, 0.0f, 0, 0};
-    if (f.ticket < ndec && seq_lookup(a, tb, static_cast<int>(f.ticket)).ok)
-        f.pre = decide_prep<Elem>(a, tb, static_cast<int>(f.ticket), lane);
     return f;
 }
 
@@ -1599,16 +1595,14 @@ __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecisi
     const int n_valid = sm.tb.n_valid;
     // Decisions first: every sequence is ready, its partials complete.
     unsigned long long dtk = first.ticket, rawd = 0;
-    bool is_first = true;
     while (dtk < ndec) {
         if (lane == 0) rawd = atomicAdd(&a.ctl->dclaim, 1ull);
         if (seq_lookup(a, sm.tb, static_cast<int>(dtk)).ok) {
-            const DecPrep pre = is_first ? first.pre : decide_prep<Elem>(a, sm.tb, static_cast<int>(dtk), lane);
+            const DecPrep pre = decide_prep<Elem>(a, sm.tb, static_cast<int>(dtk), lane);
             decide<Elem>(a, sm.tb, reinterpret_cast<float2*>(sm.buf[wi][0][0]), static_cast<int>(dtk), pre, lane);
             // Every tail slot of the decision is reserved before it counts.
             if (lane == 0) atomic_add_acq_rel(&a.ctl->ddone, 1);
         }
-        is_first = false;
         dtk = __shfl_sync(0xffffffffu, rawd, 0);
     }
     // Two pieces in flight: hc in buffer bc (reduced next), hn in the other.
@@ -1768,8 +1762,8 @@ __global__ void __launch_bounds__(kThreadsB, kCtasPerSmB) draw_kernel(const Veri
         fence_mbarrier_init();
     }
     __syncwarp();
-    // Inputs only until the wait: the batch layout and each warp's first
-    // decision's tokens, logits, uniforms and queue slot.
+    // Before the wait: the batch layout (inputs only) and each warp's first
+    // decision ticket.
     load_tables<kThreadsB>(a, sm.tb, tid);
     const FirstDecision first = first_decision<Elem>(a, sm.tb, lane);
     pdl_wait();  // the stream kernel has completed and its partials are visible
