@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c64", choices=["c64", "greedy", "highconc", "ragged"])
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="the workload's recipe at another batch size C (a sweep point; no sub-records)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--separate", action="store_true",
@@ -370,7 +372,7 @@ def run_reference(args):
     from speculative_verify_accept_02_b300 import workloads
     filtered = args.row == "filtered"
     stepper = _oracle_filtered_step if filtered else _oracle_step
-    batch = workloads.make(args.workload, device="cpu")
+    batch = workloads.make(args.workload, device="cpu", num_seqs=args.num_seqs)
     # The sample per step is sized so that the whole run (warm-up and timed
     # steps) takes about REFERENCE_BUDGET_S: up to 8 whole sequences, or one
     # sequence cut to fewer positions when a whole one is already too slow.
@@ -585,7 +587,7 @@ def run_ours(args):
         dist.barrier()
     _lib.load()
 
-    batch = workloads.make(args.workload, device=dev)
+    batch = workloads.make(args.workload, device=dev, num_seqs=args.num_seqs)
     C, total, V = batch.num_seqs, batch.total, batch.vocab
     i32, f32 = torch.int32, torch.float32
     vout = VerifyOut(torch.empty(C, dtype=i32, device=dev), torch.empty(total + C, dtype=i32, device=dev),
@@ -690,7 +692,7 @@ def run_ours(args):
         dist.destroy_process_group()
         return
     configs = None
-    if not distributed and fused and args.workload == "c64":
+    if not distributed and fused and args.workload == "c64" and args.num_seqs is None:
         # The other figures of the record, after the headline: the Gumbel-max
         # sampler, the other workloads, the filtered step.
         sub_k = min(K, SUB_STEPS)
@@ -849,7 +851,7 @@ def run_filtered(args):
     torch.cuda.set_device(dev)
     build.build()
     _lib.load()
-    batch = workloads.make(args.workload, device=dev)
+    batch = workloads.make(args.workload, device=dev, num_seqs=args.num_seqs)
     C, total, V = batch.num_seqs, batch.total, batch.vocab
     k, tp = FILTER_TOP_K, FILTER_TOP_P
     i32, f32 = torch.int32, torch.float32
