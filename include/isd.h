@@ -158,15 +158,15 @@ ISD_API isd_status isd_verify_relaxed(const void* p_logits, int64_t ld_p, const 
 ISD_API size_t isd_verify_propose_workspace_bytes(int num_seqs, int total_positions, int vocab, isd_dtype dtype);
 
 /*
- * isd_verify_propose — one launch that does isd_verify_relaxed (tau = 0:
+ * isd_verify_propose — one call that does isd_verify_relaxed (tau = 0:
  * isd_verify) and then isd_propose with this call's accept lengths: the
  * fused step of Summary §3.2, where one forward verifies the pending
  * proposals and its mask positions propose the next stride.  Proposals are
  * drawn only for sequences that accept their whole stride (valid[i] = 1);
  * the others get valid[i] = 0 and proposals -1, as isd_propose with
  * accept_len_or_null does.  Every output equals that of the two separate
- * calls on the same arguments (same uniforms); the proposal draws run inside
- * the verify kernel, right after the decision that keeps them.
+ * calls on the same arguments (same uniforms); the proposal draws run in the
+ * verify call's draw kernel, right after the decision that keeps them.
  *
  * Arguments: those of isd_verify_relaxed, then
  * qnew_logits, ld_qnew  [total, ld_qnew] this forward's mask-position logits
