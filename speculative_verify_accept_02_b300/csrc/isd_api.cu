@@ -2,6 +2,7 @@
 // workspace layout, kernel launches.  No allocation, no synchronisation.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -40,7 +41,7 @@ VerifyPlan verify_plan(int vocab, int esz) {
 }
 
 struct VerifyLayout {
-    size_t ctl, seq_done, tcount, dqueue, tdesc, tpart, part, bytes;
+    size_t ctl, seq_count, dready, seq_done, tcount, dqueue, tdesc, tpart, part, bytes;
 };
 
 // Tails: one per sequence (its correction or bonus), plus one per qnew row
@@ -52,6 +53,10 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl, bool f
     size_t off = 0;
     l.ctl = off;
     off = align_up(off + sizeof(isd::VerifyCtl));
+    l.seq_count = off;
+    off = align_up(off + sizeof(int) * C);
+    l.dready = off;
+    off = align_up(off + sizeof(uint64_t) * C);
     l.seq_done = off;
     off = align_up(off + sizeof(int) * C);
     l.tcount = off;
@@ -177,6 +182,8 @@ isd_status verify_run(const void* p_logits, int64_t ld_p, const void* q_logits, 
     va.relax_log2 = o.tau > 0.0f ? std::log2(1.0f + o.tau) : 0.0f;
     va.sampler = o.sampler;
     va.ctl = reinterpret_cast<VerifyCtl*>(ws + lay.ctl);
+    va.seq_count = reinterpret_cast<int*>(ws + lay.seq_count);
+    va.dready = reinterpret_cast<uint64_t*>(ws + lay.dready);
     va.seq_done = reinterpret_cast<int*>(ws + lay.seq_done);
     va.n_tail = num_seqs + (o.fused ? total_positions : 0);
     va.tdesc = reinterpret_cast<uint64_t*>(ws + lay.tdesc);
@@ -200,6 +207,12 @@ isd_status verify_run(const void* p_logits, int64_t ld_p, const void* q_logits, 
     int grid = 1;
     const isd_status gs = resident_grid(units, kVerifyCtasPerSm, &grid);
     if (gs != ISD_OK) return gs;
+    // Some SMs keep room for a draw-kernel CTA beside their one stream CTA,
+    // so that decisions and draws of finished sequences run during the stream.
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ISD_ERR_CUDA;
+    grid = std::max(1, std::min(grid, kVerifyCtasPerSm * sms - std::min(kDrawRoomSms, sms / 2)));
     if (launch_verify(va, esz, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ISD_ERR_CUDA;
     return ISD_OK;
 }

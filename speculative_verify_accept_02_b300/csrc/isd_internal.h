@@ -128,6 +128,8 @@ struct VerifyArgs {
     float relax_log2;  // log2(1 + tau) of relaxed acceptance, 0 for strict
     int sampler;       // Sampler of the draws after a decision
     VerifyCtl* ctl;
+    int* seq_count;    // [C] chunks of the sequence reduced (stream kernel)
+    uint64_t* dready;  // [C] flagged word: every chunk of the sequence is reduced
     int* seq_done;     // [C] draws after the decision finished
     // Tails are queued in the order decisions reserve them: a sequence's
     // correction or bonus draw, and in the fused call one draw per qnew row
@@ -163,6 +165,10 @@ constexpr int kMaxPieces = 128;
 
 // Resident CTAs of the verify step's stream kernel per SM.
 constexpr int kVerifyCtasPerSm = 2;
+
+// SMs the stream kernel leaves with one CTA, where a draw-kernel CTA fits
+// beside it from the start.
+constexpr int kDrawRoomSms = 32;
 
 cudaError_t launch_verify(const VerifyArgs& a, int elem_bytes, int grid, cudaStream_t stream);
 

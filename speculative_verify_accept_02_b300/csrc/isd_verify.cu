@@ -58,9 +58,9 @@ constexpr int kStagesV = 3;
 constexpr int kRecs = 16;              // record ring between consumers and bookkeeper
 constexpr int kGrab = 8;               // units taken from the global counter at once, away from the end
 constexpr int kVecPT = kVerifyStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
-constexpr int kWarpsB = 6;             // workers per CTA of the draw kernel
+constexpr int kWarpsB = 3;             // workers per CTA of the draw kernel
 constexpr int kThreadsB = 32 * kWarpsB;
-constexpr int kCtasPerSmB = 1;
+constexpr int kCtasPerSmB = 2;
 constexpr int kSmemSeqs = 512;         // batches up to this size keep offsets in shared memory
 constexpr int kSmemToks = 1024;        // batches up to this many positions keep their tokens there
 constexpr int kPartWords = 4;          // flagged words per piece result
@@ -70,6 +70,8 @@ enum : int { kEnd = 0, kUnit = 1 };
 
 struct Desc {
     int kind;
+    int seq;         // the sequence
+    int expect;      // chunks of the sequence
     int slot;        // row slot of the partial: 2 r + {0: p, 1: q}
     int chunk;
     int last;        // 1: the run of consecutive chunks of this row ends here
@@ -85,7 +87,7 @@ struct Desc {
 // A run: consecutive chunks [chunk, chunk + n) of one row slot, reduced by
 // one CTA in a row; its partial covers them all.
 struct Rec {
-    int kind, slot, chunk, n, arg;
+    int kind, seq, expect, slot, chunk, n, arg;
     float2 wp[kCW];  // one partial per consumer warp
 };
 
@@ -507,7 +509,10 @@ __device__ __forceinline__ void group8_merge_arg(float& M, int& I) {
 // Records are taken in batches of up to four that are already complete; lane
 // group g (8 lanes, one per consumer warp) handles record r + g.  A run's
 // partial goes to its first chunk; its other chunks get a partial that holds
-// nothing (max -inf; sum 0, or index INT_MAX).
+// nothing (max -inf; sum 0, or index INT_MAX).  Each run's chunks then count
+// toward its sequence (the stores first, then the count: release); the count
+// that completes a sequence publishes its ready word, on which the draw
+// kernel's decision waits while the stream goes on.
 __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
     const int g = lane >> 3, wl = lane & 7;
     for (long long r = 0;;) {
@@ -522,7 +527,8 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
             ++nb;
         const bool mine = g < nb;
         const Rec& rc = sm.rec[(r + (mine ? g : 0)) % kRecs];
-        const int kind = rc.kind, rslot = rc.slot, chunk = rc.chunk, nrun = rc.n, arg = rc.arg;
+        const int kind = rc.kind, rseq = rc.seq, rexpect = rc.expect, rslot = rc.slot, chunk = rc.chunk,
+                  nrun = rc.n, arg = rc.arg;
         const float2 v = rc.wp[wl];
         __syncwarp();
         if (lane < nb) mbar_arrive(&sm.rec_empty[(r + lane) % kRecs]);
@@ -541,6 +547,14 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
             if (wl == 0) *dst = arg ? make_float2(Ma, __int_as_float(Ia)) : make_float2(Mm, Sm);
             const float2 none = make_float2(-INFINITY, arg ? __int_as_float(INT_MAX) : 0.0f);
             for (int j = 1 + wl; j < nrun; j += 8) dst[j] = none;
+        }
+        __syncwarp();
+        if (g < n_real && wl == 0) {
+            __threadfence();
+            if (atomicAdd(a.seq_count + rseq, nrun) + nrun == rexpect) {
+                __threadfence();
+                st_volatile_u64(a.dready + rseq, flagged(static_cast<uint32_t>(rseq) + 1u, 0u));
+            }
         }
         __syncwarp();
         r += nb;
@@ -640,6 +654,8 @@ __device__ void producer(const VerifyArgs& a, SmemA& sm) {
             }
             Desc& d = sm.desc[stage];
             d.kind = kUnit;
+            d.seq = i;
+            d.expect = static_cast<int>(units);
             d.slot = slot;
             d.chunk = c;
             // The run goes on while the next unit of this CTA is the next
@@ -676,7 +692,8 @@ __device__ void producer(const VerifyArgs& a, SmemA& sm) {
 
 // Hand this warp's partial of a run to the bookkeeper.
 __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemA& sm, long long& nrec, int warp, int lane,
-                                            float2 part, int kind, int slot, int chunk, int n, int arg) {
+                                            float2 part, int kind, int seq, int expect, int slot, int chunk, int n,
+                                            int arg) {
     const int rs = static_cast<int>(nrec % kRecs);
     const uint32_t parity = (static_cast<uint32_t>(nrec / kRecs) & 1u) ^ 1u;
     ++nrec;
@@ -686,6 +703,8 @@ __device__ __forceinline__ void push_record(const VerifyArgs& a, SmemA& sm, long
         rc.wp[warp] = part;
         if (warp == 0) {
             rc.kind = kind;
+            rc.seq = seq;
+            rc.expect = expect;
             rc.slot = slot;
             rc.chunk = chunk;
             rc.n = n;
@@ -872,13 +891,14 @@ __device__ void consumer(const VerifyArgs& a, SmemA& sm, int tid, int warp, int 
                 warp_merge_mc(M, S);
                 part = make_float2(M, S);
             }
-            push_record(a, sm, nrec, warp, lane, part, kUnit, d.slot, run_chunk, d.chunk - run_chunk + 1, arg);
+            push_record(a, sm, nrec, warp, lane, part, kUnit, d.seq, d.expect, d.slot, run_chunk,
+                        d.chunk - run_chunk + 1, arg);
             r = Run{-INFINITY, 0.0f, INT_MAX};
             run_chunk = -1;
         }
     }
     // Tell the bookkeeper there is no more work (a record of kind kEnd).
-    push_record(a, sm, nrec, warp, lane, make_float2(0.0f, 0.0f), kEnd, 0, 0, 0, 0);
+    push_record(a, sm, nrec, warp, lane, make_float2(0.0f, 0.0f), kEnd, 0, 0, 0, 0, 0, 0);
 }
 
 // =============================================================================
@@ -1514,8 +1534,32 @@ __device__ __noinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi,
 // tails whose last piece it finishes
 // =============================================================================
 
-// A warp's first decision ticket, claimed before the stream kernel has
-// completed (the control block is the previous call's, zeroed).
+// Wait (bounded) for sequence i's ready word: every chunk of the sequence
+// reduced and stored by the stream kernel.  The word and the count are
+// zeroed for the next call.  False if the wait ran out.
+__device__ __forceinline__ bool decide_wait(const VerifyArgs& a, int i, int lane) {
+    const uint64_t t0 = global_timer_ns();
+    int ok = 1;
+    if (lane == 0) {
+        while (static_cast<uint32_t>(ld_volatile_u64(a.dready + i) >> 32) != static_cast<uint32_t>(i) + 1u) {
+            if (global_timer_ns() - t0 > a.wait_ns) {
+                atomicOr(&a.ctl->err, kErrWaitTimeout);
+                ok = 0;
+                break;
+            }
+            __nanosleep(128);
+        }
+        __threadfence();  // the sequence's partials are read after its ready word
+        if (ok) {
+            st_volatile_u64(a.dready + i, 0);
+            a.seq_count[i] = 0;
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// A warp's first decision ticket (the control block is the previous call's,
+// zeroed).
 struct FirstDecision {
     unsigned long long ticket;
 };
@@ -1593,11 +1637,12 @@ __device__ void worker(const VerifyArgs& a, SmemB& sm, int wi, const FirstDecisi
     const unsigned long long cap = static_cast<unsigned long long>(a.n_tail) * static_cast<unsigned long long>(a.np);
     const unsigned long long ndec = sm.tb.batch_bad ? 0ull : static_cast<unsigned long long>(a.num_seqs);
     const int n_valid = sm.tb.n_valid;
-    // Decisions first: every sequence is ready, its partials complete.
+    // Decisions first, each once its sequence's partials are all stored.
     unsigned long long dtk = first.ticket, rawd = 0;
     while (dtk < ndec) {
         if (lane == 0) rawd = atomicAdd(&a.ctl->dclaim, 1ull);
         if (seq_lookup(a, sm.tb, static_cast<int>(dtk)).ok) {
+            if (!decide_wait(a, static_cast<int>(dtk), lane)) return;
             const DecPrep pre = decide_prep<Elem>(a, sm.tb, static_cast<int>(dtk), lane);
             decide<Elem>(a, sm.tb, reinterpret_cast<float2*>(sm.buf[wi][0][0]), static_cast<int>(dtk), pre, lane);
             // Every tail slot of the decision is reserved before it counts.
@@ -1719,8 +1764,9 @@ __global__ void __launch_bounds__(kThreadsA, kVerifyCtasPerSm) stream_kernel(con
     SmemA& sm = *reinterpret_cast<SmemA*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_wait();
-    // The draw kernel's CTAs may be scheduled as soon as SMs free up; they
-    // wait for this grid to complete before reading anything it writes.
+    // The draw kernel's CTAs may be scheduled from here on, where an SM has
+    // room; they run beside this grid and read a sequence's partials once
+    // its ready word is published.
     pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < kStagesV; ++s) {
@@ -1762,12 +1808,14 @@ __global__ void __launch_bounds__(kThreadsB, kCtasPerSmB) draw_kernel(const Veri
         fence_mbarrier_init();
     }
     __syncwarp();
-    // Before the wait: the batch layout (inputs only) and each warp's first
-    // decision ticket.
+    // The draw kernel runs beside the stream kernel: it reads a sequence's
+    // partials only after that sequence's ready word (decide_wait).
     load_tables<kThreadsB>(a, sm.tb, tid);
     const FirstDecision first = first_decision<Elem>(a, sm.tb, lane);
-    pdl_wait();  // the stream kernel has completed and its partials are visible
     worker<Elem, kGum>(a, sm, warp, first, lane);
+    // Every CTA outlasts the stream kernel: the next call's kernels wait for
+    // this grid only, and the control block is zeroed below for both.
+    pdl_wait();
     __syncthreads();
     if (tid == 0) {
         __threadfence();
