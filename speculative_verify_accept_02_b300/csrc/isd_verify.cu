@@ -56,7 +56,7 @@ constexpr int kBookWarp = kCW + 1;
 constexpr int kThreadsA = 32 * (kCW + 2);
 constexpr int kStagesV = 3;
 constexpr int kRecs = 16;              // record ring between consumers and bookkeeper
-constexpr int kGrab = 8;               // units taken from the global counter at once, away from the end
+constexpr int kGrab = 4;               // units taken from the global counter at once, away from the end
 constexpr int kVecPT = kVerifyStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
 constexpr int kWarpsB = 3;             // workers per CTA of the draw kernel
 constexpr int kThreadsB = 32 * kWarpsB;
