@@ -13,9 +13,6 @@ constexpr int kMaxStride = 32;
 constexpr uint64_t kTagAccept = 0, kTagCorrect = 1, kTagBonus = 2, kTagPropose = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Bound on every spin-wait (mbarrier polls with back-off): a wait that never
-// completes ends after roughly a second instead of hanging the device.
-constexpr uint32_t kWaitLimit = 1u << 22;
 // Time bounds of the persistent verify kernel's waits, in nanoseconds of the
 // global timer: far above any legitimate wait, far below a hang.
 constexpr uint64_t kWaitNs = 1000000000ull;       // stage barriers, task flags
@@ -108,23 +105,6 @@ __device__ __forceinline__ int warp_max_int(int v) {
     return v;
 }
 
-// Softmax partial (running max m, sum s of exp2((x - m) * c2)) merged into
-// (M, S); a partial with m = -inf holds no mass.
-__device__ __forceinline__ void merge_softmax(float& M, float& S, float m, float s, float c2) {
-    if (m == -INFINITY) return;
-    if (M == -INFINITY) {
-        M = m;
-        S = s;
-        return;
-    }
-    if (m > M) {
-        S = S * exp2f((M - m) * c2) + s;
-        M = m;
-    } else {
-        S += s * exp2f((m - M) * c2);
-    }
-}
-
 // Argmax partial: larger value wins, equal values go to the lower index.
 __device__ __forceinline__ void merge_argmax(float& M, int& I, float m, int i) {
     if (m > M || (m == M && i < I)) {
@@ -198,11 +178,6 @@ __device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 
 // ---------------------------------------------------------------------------
 // Global-memory communication between CTAs of one grid
@@ -233,17 +208,6 @@ __device__ __forceinline__ void st_volatile_v2u64(uint64_t* p, uint64_t v0, uint
 }
 __device__ __forceinline__ void ld_volatile_v2u64(const uint64_t* p, uint64_t& v0, uint64_t& v1) {
     asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(v0), "=l"(v1) : "l"(p) : "memory");
-}
-
-// A flagged word published with release semantics (cumulative: it also
-// publishes what this thread acquired before), and its acquiring read.
-__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
 }
 
 // Loads that bypass L1 (data written by other CTAs of the running grid).
@@ -312,15 +276,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait for the phase of `parity` to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (it > 64) __nanosleep(128);
-    }
-    return false;
-}
-
 // Non-blocking check whether the phase of `parity` has completed.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     uint32_t done;
@@ -380,34 +335,11 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, u
         : "memory");
 }
 
-// L2 policies: lines loaded under evict_last outlive evict_first ones.
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
+// L2 policy for lines read once: the first the L2 gives up.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
-}
-
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Named barrier that also ORs a predicate over the participating threads.
-__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t threads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
 }
 
 // Programmatic dependent launch: wait for the grids this one depends on, and
