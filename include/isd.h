@@ -263,8 +263,8 @@ ISD_API isd_status isd_alpha(const float* ratio, const int32_t* seq_offsets, int
  *   - a batch whose isd_verify_workspace_bytes() exceeds
  *     ISD_NOALLOC_SCRATCH_BYTES returns ISD_ERR_WORKSPACE and launches
  *     nothing (isd_verify_workspace_bytes() gives any batch's need: rows of
- *     V = 151936 at C = 256, L = 16 need 2,231,296 bytes in bf16, about 27 %
- *     of the array, and 4,336,640 bytes in fp32, about 52 %);
+ *     V = 151936 at C = 256, L = 16 need 2,522,368 bytes in bf16, about 30 %
+ *     of the array, and 4,930,816 bytes in fp32, about 59 %);
  *   - the array's device address is looked up once per CUDA context, on the
  *     first call made in it; make that first call before any stream capture;
  *   - every call on a device shares the one array: two calls that can

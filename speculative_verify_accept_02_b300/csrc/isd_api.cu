@@ -66,7 +66,7 @@ VerifyLayout verify_layout(int num_seqs, int total, const VerifyPlan& pl, bool f
     l.tdesc = off;
     off = align_up(off + sizeof(uint64_t) * isd::kTailWords * NT);
     l.tpart = off;
-    off = align_up(off + sizeof(uint64_t) * 20 * NT * static_cast<size_t>(pl.np));  // a record of 20 words per piece
+    off = align_up(off + sizeof(uint64_t) * isd::kPieceRecWords * NT * static_cast<size_t>(pl.np));  // a record per piece
     l.part = off;
     off = align_up(off + sizeof(float2) * 2 * static_cast<size_t>(total) * pl.nck);
     l.bytes = off;

@@ -136,7 +136,7 @@ struct VerifyArgs {
     // of a sequence that accepted its whole stride.
     int n_tail;        // capacity: C, or C + total when fused
     uint64_t* tdesc;   // [n_tail][kTailWords] flagged descriptor words
-    uint64_t* tpart;   // [n_tail][np][20] flagged piece records: 4 result words, 16 block weights
+    uint64_t* tpart;   // [n_tail][np][kPieceRecWords] flagged piece records: 4 result words, block weights
     int* tcount;       // [n_tail] pieces finished
     int* dqueue;       // [n_tail] tails whose pieces are all finished, in completion order (slot + 1; 0: not yet)
     float2* part;      // [2 * total][nck] per (row slot, chunk) partials
@@ -160,8 +160,14 @@ struct VerifyArgs {
 
 // Bytes of a tail piece per row, and the most pieces per row the verify
 // kernel supports (vocabularies up to 524,288 bf16 or 262,144 fp32 ids).
-constexpr int kPieceBytes = 8192;
-constexpr int kMaxPieces = 128;
+constexpr int kPieceBytes = 4096;
+constexpr int kMaxPieces = 256;
+// A piece record: four flagged result words, then the flagged weight of each
+// 512-byte block of the piece (an even count: records are read in 16-byte
+// pairs).
+constexpr int kPieceBlocks = kPieceBytes / 512;
+constexpr int kPieceRecWords = 4 + kPieceBlocks;
+static_assert(kPieceRecWords % 2 == 0, "records of whole 16-byte pairs");
 
 // Resident CTAs of the verify step's stream kernel per SM.
 constexpr int kVerifyCtasPerSm = 2;

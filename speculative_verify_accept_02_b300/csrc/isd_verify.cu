@@ -5,33 +5,37 @@
 // correction work), optionally with the next stride's proposal draws of the
 // fused step (§3.2: one forward verifies and proposes).
 //
-// stream kernel  every chunk (at most 16 KB) of every row a decision needs:
+// stream kernel  every chunk (at most 32 KB) of every row a decision needs:
 //                p_k and q_k for k <= L_i (T > 0), or p_1 .. p_{L+1}
 //                (T = 0).  Chunks are taken in small batches from a global
-//                counter, staged with 1-D bulk copies into a 4-stage ring
+//                counter, staged with 1-D bulk copies into a 3-stage ring
 //                (mbarrier completion) by one producer thread, and reduced by
 //                eight consumer warps to a softmax partial (max, sum) or an
-//                argmax per warp; a bookkeeper warp merges the eight and
-//                stores the chunk's partial.  Nothing else runs beside the
-//                stream: it keeps the HBM busy from its first chunk to its
-//                last.
-// draw kernel    launched behind it (programmatic dependent launch: its CTAs
-//                take the SMs as the stream's retire).  Every warp is a
-//                worker:
-//                  decisions   by ticket (a sequence index): ratio_k =
+//                argmax per warp; a bookkeeper warp merges the eight, stores
+//                the chunk's partial and counts the sequence's chunks, and
+//                the CTA that stores a sequence's last chunk publishes its
+//                ready word.
+// draw kernel    launched behind it (programmatic dependent launch, released
+//                as soon as the stream kernel starts): its CTAs run on the
+//                SMs the stream leaves room on, then take the SMs as the
+//                stream's CTAs retire.  Every warp is a worker:
+//                  decisions   by ticket (a sequence index), once the
+//                              sequence's ready word is published: ratio_k =
 //                              min(1, p_k(x_k) / q_k(x_k)), alpha, the accept
 //                              prefix (Philox uniforms, one warp ballot;
 //                              relaxed acceptance tests min(1, (1 + tau) p/q))
 //                              and the emitted prefix; a greedy correction or
 //                              bonus.  The draws left are published as tails;
-//                  pieces      by ticket: 8 KB of a tail's row or row pair (the
+//                  pieces      by ticket: 4 KB of a tail's row or row pair (the
 //                              residual max(0, p_j - q_j) of the one rejected
 //                              row pair, the final anchor p_{L+1}, or a qnew
 //                              row of the fused call), staged in padded shared
-//                              memory and reduced, each lane's 128-id block
-//                              weight published before the piece's result;
-//                  draws       by the worker that finishes a tail's last
-//                              piece: by inverse CDF (the piece from the piece
+//                              memory and reduced; the weight of every 512-byte
+//                              block of the piece is published with the
+//                              piece's result;
+//                  draws       queued when a tail's last piece is finished and
+//                              taken by the workers that run out of pieces:
+//                              by inverse CDF (the piece from the piece
 //                              weights, the block from its block weights, the
 //                              id from the block's logits) or, with the
 //                              Gumbel-max sampler, the largest perturbed score.
@@ -58,7 +62,7 @@ constexpr int kStagesV = 3;
 constexpr int kRecs = 16;              // record ring between consumers and bookkeeper
 constexpr int kGrab = 4;               // units taken from the global counter at once, away from the end
 constexpr int kVecPT = kVerifyStageBytes / 16 / kCT;  // 16-byte vectors per consumer thread per stage
-constexpr int kWarpsB = 3;             // workers per CTA of the draw kernel
+constexpr int kWarpsB = 6;             // workers per CTA of the draw kernel
 constexpr int kThreadsB = 32 * kWarpsB;
 constexpr int kCtasPerSmB = 2;
 constexpr int kSmemSeqs = 512;         // batches up to this size keep offsets in shared memory
@@ -114,9 +118,11 @@ struct SmemA {
 };
 
 struct SmemB {
-    alignas(128) unsigned char buf[kWarpsB][2][2][kPieceBytes];  // each worker's two piece buffers (rows p, q)
-    float4 ppart[kWarpsB][kMaxPieces];                            // each worker's piece results of one draw
-    uint64_t bar[kWarpsB][2];                                     // completion of each buffer's copies
+    // Each worker's two piece buffers (rows p, q).  A worker's draws come
+    // after its last piece, with no copy in flight, so the piece results a
+    // draw reads live in its first buffer.
+    alignas(128) unsigned char buf[kWarpsB][2][2][kPieceBytes];
+    uint64_t bar[kWarpsB][2];  // completion of each buffer's copies
     Tables tb;
 };
 
@@ -938,8 +944,9 @@ __device__ __forceinline__ const char* tail_prow(const VerifyArgs& a, const Tail
 // 31, 512 bytes of ids) is block j of the piece: the unit a draw walks after
 // choosing the piece.
 
-constexpr int kBlk = kPieceBytes / 512;       // blocks per piece
-constexpr int kRecWords = kPartWords + kBlk;  // flagged words per piece record: result, then block weights
+constexpr int kBlk = kPieceBlocks;        // blocks per piece
+constexpr int kRecWords = kPieceRecWords;  // flagged words per piece record: result, then block weights
+static_assert(kRecWords == kPartWords + kBlk, "record layout");
 static_assert(kBlk % 4 == 0, "blocks are reduced four at a time");
 
 // A piece a worker holds: its ticket and tail, where its ids are, and how
@@ -1101,7 +1108,7 @@ __device__ __forceinline__ void claim_piece(const VerifyArgs& a, Held& h, unsign
 //   Gumbel-max:             (best score, its id, best score of p alone, its id)
 // (a Gumbel score is log2 w_v - log2(-ln u_v); the last pair is the fallback
 // for a residual that rounds to zero everywhere), then, for the inverse CDF,
-// the 16 block weights in the piece's own scale.  Returns, on lane 0, the
+// the kBlk block weights in the piece's own scale.  Returns, on lane 0, the
 // tail's count of finished pieces before this one (np - 1: this piece
 // completes the tail).
 template <typename Elem, bool kGum>
@@ -1342,7 +1349,7 @@ __device__ __noinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi,
     const Tail& t = hd.t;
     const int slot = hd.slot;
     const int np = a.np;
-    float4* pr = sm.ppart[wi];
+    float4* pr = reinterpret_cast<float4*>(sm.buf[wi][0][0]);  // the buffers are idle during draws
     const uint32_t f = static_cast<uint32_t>(slot) + 1u;
     const uint64_t* src = a.tpart + static_cast<size_t>(slot) * np * kRecWords;
     const bool gum = kGum && t.mode != kTailArg;
@@ -1412,7 +1419,7 @@ __device__ __noinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi,
         h.nbytes = 0;
         const float mc_k = soft ? pr[chosen].x : 0.0f;
         const DrawW id_w{kind, t.c2, soft ? mc_k : MC, t.nz0, t.nz1};
-        float bw = 0.0f;  // lane j < 16: the weight of block j of the chosen piece
+        float bw = 0.0f;  // lane j < kBlk: the weight of block j of the chosen piece
         if (kind == 2) {
             // A residual that rounded to zero everywhere draws from p_j: no
             // block weights of p were kept, so its blocks are summed here
@@ -1428,7 +1435,7 @@ __device__ __noinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi,
                     for (int jv = 0; jv < VEC; ++jv) w[jv] = id_w(xp[jv], 0.0f);
                     v[jj] = tree_sum<VEC>(w);
                 }
-                // Lane l < 16 keeps block l = 4 g + (l & 3), reduced on lane (l & 3) * 8.
+                // Lane l < kBlk keeps block l = 4 g + (l & 3), reduced on lane (l & 3) * 8.
                 const float sg = __shfl_sync(0xffffffffu, block_sums4(v, lane), (lane & 3) << 3);
                 if ((lane >> 2) == g) bw = sg;
             }
@@ -1841,6 +1848,7 @@ __global__ void __launch_bounds__(kThreadsB, kCtasPerSmB) draw_kernel(const Veri
 
 static_assert(sizeof(SmemA) + 128 <= 113 * 1024, "two stream CTAs per SM");
 static_assert(kCtasPerSmB * (sizeof(SmemB) + 128) <= 227 * 1024, "draw CTAs per SM");
+static_assert(kMaxPieces * sizeof(float4) <= 2 * kPieceBytes, "a draw's piece results fit in a worker's first buffer");
 
 template <typename Elem>
 cudaError_t launch_verify_t(const VerifyArgs& a, int grid, cudaStream_t stream) {
