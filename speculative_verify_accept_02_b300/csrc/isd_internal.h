@@ -174,7 +174,7 @@ constexpr int kVerifyCtasPerSm = 2;
 
 // SMs the stream kernel leaves with one CTA, where a draw-kernel CTA fits
 // beside it from the start.
-constexpr int kDrawRoomSms = 32;
+constexpr int kDrawRoomSms = 16;
 
 cudaError_t launch_verify(const VerifyArgs& a, int elem_bytes, int grid, cudaStream_t stream);
 

@@ -323,10 +323,13 @@ __device__ __forceinline__ DecPrep decide_prep(const VerifyArgs& a, const Tables
     return d;
 }
 
+// Inlined into the worker, so that the arguments are read as kernel
+// parameters (an out-of-line call would reach them through a generic pointer,
+// reloaded after every store).
 template <typename Elem>
-__device__ __noinline__ void decide(const VerifyArgs& a, const Tables& tb, float2* sblk, int i, const DecPrep pre,
-                                    int lane) {
-    // The stream kernel has completed: every partial of the sequence is in
+__device__ __forceinline__ void decide(const VerifyArgs& a, const Tables& tb, float2* sblk, int i, const DecPrep pre,
+                                       int lane) {
+    // The sequence's ready word is published: every partial of it is in
     // place.
     const SeqInfo s = seq_lookup(a, tb, i);
     const int L = s.len;
@@ -1339,12 +1342,12 @@ __device__ __forceinline__ int warp_icdf(int n, int q, float target, const F& w,
     return found;
 }
 
-// The draw of a tail, by the worker whose piece completed it: reads every
-// piece result (all counted, their flagged words land moments later at
-// most), draws, writes the token, and clears the tail's words and count for
-// the next call.  False if a wait ran out.
+// The draw of a queued tail: reads every piece result (all counted, their
+// flagged words land moments later at most), draws, writes the token, and
+// clears the tail's words and count for the next call.  False if a wait ran
+// out.  Inlined for the same reason as decide.
 template <typename Elem, bool kGum>
-__device__ __noinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi, const Held hd, int lane) {
+__device__ __forceinline__ bool select_draw(const VerifyArgs& a, SmemB& sm, int wi, const Held hd, int lane) {
     constexpr int VEC = 16 / sizeof(Elem);
     const Tail& t = hd.t;
     const int slot = hd.slot;
