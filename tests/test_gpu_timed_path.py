@@ -174,3 +174,60 @@ def test_bounded_wait_runs_out_then_recovers():
     torch.cuda.synchronize()
     assert np.array_equal(v2.accept_len.cpu().numpy(), gv["accept_len"])
     assert np.array_equal(v2.out_tokens.cpu().numpy(), gv["out_tokens"])
+
+
+def test_fused_step_replays_from_a_cuda_graph():
+    """isd_verify_propose captured once in a CUDA graph (both launches and the
+    programmatic dependency between them) and replayed on new inputs copied
+    into the captured buffers: the call allocates nothing and never
+    synchronises, and every call leaves the workspace ready for the next (its
+    counters, queue and tail words re-zeroed; its partials rewritten by the
+    next stream), so every replay equals the oracle on the inputs it saw."""
+    from speculative_verify_accept_02_b300.api import ProposeOut, VerifyOut
+    a = workloads.make("c64", num_seqs=6, vocab=20000, seed=1)
+    b = workloads.make("c64", num_seqs=6, vocab=20000, seed=2)
+    assert torch.equal(a.seq_offsets, b.seq_offsets) and torch.equal(a.temperature, b.temperature)
+    assert not torch.equal(a.p, b.p)
+    x = a.to("cuda")  # the buffers the graph reads
+    dev = x.p.device
+    C, total, V = x.num_seqs, x.total, x.vocab
+    i32 = torch.int32
+    out = VerifyOut(torch.empty(C, dtype=i32, device=dev), torch.empty(total + C, dtype=i32, device=dev),
+                    torch.empty(total, dtype=torch.float32, device=dev), torch.empty(C, dtype=torch.float32, device=dev))
+    pout = ProposeOut(torch.empty(total, dtype=i32, device=dev), torch.empty(C, dtype=torch.uint8, device=dev))
+    ws = workspace(isd_verify_propose_workspace_bytes(C, total, V, x.dtype), dev)
+    seed, offset = 3, 5
+
+    def step():
+        isd_verify_propose(x.p, x.q, x.tokens, x.qnew, x.seq_offsets, x.temperature, seed, offset,
+                           vocab=V, total=total, out=out, pout=pout, ws=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # one ordinary call first, outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    rep = Report()
+    for batch in (b, a, b):
+        for dst, src in ((x.p, batch.p), (x.q, batch.q), (x.qnew, batch.qnew), (x.tokens, batch.tokens)):
+            dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        gv = dict(accept_len=out.accept_len.cpu().numpy(), out_tokens=out.out_tokens.cpu().numpy(),
+                  ratio=out.ratio.cpu().numpy(), alpha=out.alpha.cpu().numpy())
+        gp = dict(proposals=pout.proposals.cpu().numpy(), valid=pout.valid.cpu().numpy())
+        h = host(batch)
+        check_layout(gv, gp, h, V)
+        ov = oracle.verify(h["p"], h["q"], V, h["tokens"], h["offs"], h["temp"], seed, offset)
+        compare_verify(ov, gv, h["offs"], report=rep)
+        agree = [i for i in range(C) if ov["accept_len"][i] == gv["accept_len"][i]]
+        op = oracle.propose(h["qnew"], V, h["offs"], h["temp"], seed, offset, accept_len=gv["accept_len"])
+        compare_propose(op, gp, h["offs"], seqs=agree, report=rep)
+        assert int(ws[:4].view(torch.int32)[0]) == 0  # no wait ran out (the error word leads the workspace)
+    print(f"\ngraph replays: {rep.summary()}")
+    rep.check()
+    assert rep.exempt_accept + rep.exempt_token <= max(1, rep.sequences // 20), rep.summary()
