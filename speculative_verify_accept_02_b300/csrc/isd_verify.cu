@@ -559,11 +559,12 @@ __device__ void bookkeeper(const VerifyArgs& a, SmemA& sm, int lane) {
         }
         __syncwarp();
         if (g < n_real && wl == 0) {
-            __threadfence();
-            if (atomicAdd(a.seq_count + rseq, nrun) + nrun == rexpect) {
-                __threadfence();
-                st_volatile_u64(a.dready + rseq, flagged(static_cast<uint32_t>(rseq) + 1u, 0u));
-            }
+            // The count releases this run's partials (the group's stores,
+            // ordered by the warp barrier above); the count that completes
+            // the sequence also acquires the other runs' and publishes the
+            // ready word with a release store.
+            if (atomic_add_acq_rel(a.seq_count + rseq, nrun) + nrun == rexpect)
+                st_release_u64(a.dready + rseq, flagged(static_cast<uint32_t>(rseq) + 1u, 0u));
         }
         __syncwarp();
         r += nb;
@@ -1551,7 +1552,7 @@ __device__ __forceinline__ bool decide_wait(const VerifyArgs& a, int i, int lane
     const uint64_t t0 = global_timer_ns();
     int ok = 1;
     if (lane == 0) {
-        while (static_cast<uint32_t>(ld_volatile_u64(a.dready + i) >> 32) != static_cast<uint32_t>(i) + 1u) {
+        while (static_cast<uint32_t>(ld_acquire_u64(a.dready + i) >> 32) != static_cast<uint32_t>(i) + 1u) {
             if (global_timer_ns() - t0 > a.wait_ns) {
                 atomicOr(&a.ctl->err, kErrWaitTimeout);
                 ok = 0;
@@ -1559,12 +1560,12 @@ __device__ __forceinline__ bool decide_wait(const VerifyArgs& a, int i, int lane
             }
             __nanosleep(128);
         }
-        __threadfence();  // the sequence's partials are read after its ready word
         if (ok) {
             st_volatile_u64(a.dready + i, 0);
             a.seq_count[i] = 0;
         }
     }
+    __syncwarp();  // every lane reads the partials after lane 0's acquire
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
