@@ -59,6 +59,26 @@ def test_workspace_sizes(lib):
     assert lib.isd_propose_workspace_bytes(64, 512, 151936, 1) > 0
 
 
+def test_noalloc_figures_in_the_header(lib):
+    """The sizes include/isd.h quotes for isd_verify_noalloc's array are the
+    library's own: ISD_NOALLOC_SCRATCH_BYTES equals the binding's constant,
+    and the bf16 and fp32 needs it gives for V = 151936, C = 256, L = 16 (and
+    their shares of the array) equal isd_verify_workspace_bytes."""
+    text = open(os.path.join(ROOT, "include", "isd.h")).read()
+    m = re.search(r"#define ISD_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m, "ISD_NOALLOC_SCRATCH_BYTES definition"
+    array = int(m.group(1)) << int(m.group(2))
+    assert array == _lib.NOALLOC_SCRATCH_BYTES
+    flat = " ".join(line.strip(" *") for line in text.splitlines())
+    m = re.search(r"V = 151936 at C = 256, L = 16 need ([\d,]+) bytes in bf16, about (\d+) % "
+                  r"of the array, and ([\d,]+) bytes in fp32, about (\d+) %", flat)
+    assert m, "the quoted figures"
+    for (nbytes, pct), dtype in (((m.group(1), m.group(2)), 0), ((m.group(3), m.group(4)), 1)):
+        need = lib.isd_verify_workspace_bytes(256, 256 * 16, 151936, dtype)
+        assert int(nbytes.replace(",", "")) == need
+        assert int(pct) == round(100 * need / array)
+
+
 # A 16-byte aligned address that is never dereferenced: every call below has
 # at least one bad argument (or an empty batch), so it returns on the host
 # before any launch.
