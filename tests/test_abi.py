@@ -117,6 +117,19 @@ def _verify_relaxed(lib, tau, **kw):
     return lib.isd_verify_relaxed(*args.values())
 
 
+def test_verify_vocabulary_limit(lib):
+    """The verify calls refuse, on the host, a vocabulary past the most tail
+    pieces a row may have (524,288 bf16 or 262,144 fp32 ids, as isd.h
+    states): UNSUPPORTED, nothing launched.  The largest vocabulary passes
+    that check and stops at the next one, a workspace too small (also on
+    the host, before any CUDA call)."""
+    for dtype, vmax in ((0, 524288), (1, 262144)):
+        v = vmax + 1
+        assert _verify(lib, dtype=dtype, vocab=v, ldp=v, ldq=v) == _lib.ISD_ERR_UNSUPPORTED
+        assert _verify(lib, dtype=dtype, vocab=vmax, ldp=vmax, ldq=vmax, wsb=1) == _lib.ISD_ERR_WORKSPACE
+        assert lib.isd_verify_workspace_bytes(64, 512, vmax, dtype) > 0
+
+
 def test_verify_relaxed_host_checks(lib):
     """tau must be finite and >= 0; the other checks are isd_verify's."""
     for bad in (-0.5, float("nan"), float("inf")):
